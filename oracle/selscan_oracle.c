@@ -1,0 +1,149 @@
+/*
+ * fp64 CPU oracle for the selective state-space (S6) recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, obviously-correct definition that
+ * the CUDA path is checked against. It shares no code, header or table with the CUDA
+ * library, and only the test suite, the smoke check and the benchmark's CPU-baseline
+ * leg may load it. The product path never calls it.
+ *
+ * What it computes, and where the definition comes from:
+ *   - "Mamba and State Space Models" (world.lapla.si), section "A State of Fixed Size":
+ *     each input updates the state once, h <- Abar*h + Bbar*x, and the output is read
+ *     from the updated state, y = C*h.
+ *   - same page, section "Chosen by the Token": Delta, B and C are computed per token,
+ *     A is fixed, and the retained fraction of the state is exp(Delta*A).
+ *   - same page, section "A Scan on the Chip": Delta, A, B, C are discretised and then
+ *     run through the recurrence (the discretisation rule of B is not stated there).
+ *   - The remaining choices are the plain reading used throughout this project:
+ *     Delta = softplus(delta + delta_bias) (or delta + delta_bias with the flag off),
+ *     Euler discretisation of B (Bbar*x = Delta*B*u), a skip term D*u added to C*h,
+ *     and the result gated by silu(z) = z*sigmoid(z). The initial state is zero unless
+ *     one is given.
+ * Everything is evaluated in double precision, strictly sequentially in t, with the
+ * readout summed in increasing n. Rows (b, d) are independent and are spread over
+ * OpenMP threads; nothing inside a row is reordered.
+ *
+ * Layouts (all contiguous, row-major):
+ *   u, delta, z, out      (batch, dim, seqlen)
+ *   B, C                  (batch, dstate, seqlen)
+ *   A                     (dim, dstate)
+ *   D, delta_bias         (dim)
+ *   initial_state, final_state, state   (batch, dim, dstate)
+ *   state-update per-token tensors: x, dt, z, out (batch, dim); B, C (batch, dstate)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(x) = log(1 + e^x), written in the form that neither overflows nor loses
+ * the small result for very negative x. */
+static double softplus(double x) { return fmax(x, 0.0) + log1p(exp(-fabs(x))); }
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* One row (b, d) of the scan: the recurrence over t = 0 .. seqlen-1. */
+static void scan_row(const double* u, const double* delta, const double* A_d, const double* Bb,
+                     const double* Cb, double D_d, const double* z, double bias, int softplus_on,
+                     int64_t dstate, int64_t seqlen, double* h, double* out) {
+    for (int64_t t = 0; t < seqlen; ++t) {
+        double x = delta[t] + bias;
+        double dlt = softplus_on ? softplus(x) : x;
+        for (int64_t n = 0; n < dstate; ++n) {
+            double abar = exp(dlt * A_d[n]);
+            double bbar_x = dlt * Bb[n * seqlen + t] * u[t];
+            h[n] = abar * h[n] + bbar_x;
+        }
+        double y = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) y += Cb[n * seqlen + t] * h[n];
+        y += D_d * u[t];
+        if (z) y *= silu(z[t]);
+        out[t] = y;
+    }
+}
+
+/* Full forward scan. Optional pointers (D, z, delta_bias, initial_state, final_state) may
+ * be NULL: D and delta_bias then count as zero, z as no gate, initial_state as zeros. */
+void oracle_scan_fwd(const double* u, const double* delta, const double* A, const double* B,
+                     const double* C, const double* D, const double* z, const double* delta_bias,
+                     int delta_softplus, const double* initial_state, double* out,
+                     double* final_state, int64_t batch, int64_t dim, int64_t dstate,
+                     int64_t seqlen) {
+    int64_t rows = batch * dim;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t b = r / dim, d = r % dim;
+        double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+        for (int64_t n = 0; n < dstate; ++n)
+            h[n] = initial_state ? initial_state[r * dstate + n] : 0.0;
+        const int64_t off = r * seqlen;
+        scan_row(u + off, delta + off, A + d * dstate, B + b * dstate * seqlen,
+                 C + b * dstate * seqlen, D ? D[d] : 0.0, z ? z + off : NULL,
+                 delta_bias ? delta_bias[d] : 0.0, delta_softplus, dstate, seqlen, h, out + off);
+        if (final_state)
+            for (int64_t n = 0; n < dstate; ++n) final_state[r * dstate + n] = h[n];
+        free(h);
+    }
+}
+
+/* Scan over a subset of rows: rows[i] = b*dim + d. Outputs are packed per listed row:
+ * out (nrows, seqlen), final_state (nrows, dstate). Inputs keep their full layouts. */
+void oracle_scan_fwd_rows(const double* u_rows, const double* delta_rows, const double* A,
+                          const double* B, const double* C, const double* D, const double* z_rows,
+                          const double* delta_bias, int delta_softplus,
+                          const double* initial_state_rows, double* out_rows,
+                          double* final_state_rows, const int64_t* rows, int64_t nrows,
+                          int64_t dim, int64_t dstate, int64_t seqlen) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t b = rows[i] / dim, d = rows[i] % dim;
+        double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+        for (int64_t n = 0; n < dstate; ++n)
+            h[n] = initial_state_rows ? initial_state_rows[i * dstate + n] : 0.0;
+        const int64_t off = i * seqlen;
+        scan_row(u_rows + off, delta_rows + off, A + d * dstate, B + b * dstate * seqlen,
+                 C + b * dstate * seqlen, D ? D[d] : 0.0, z_rows ? z_rows + off : NULL,
+                 delta_bias ? delta_bias[d] : 0.0, delta_softplus, dstate, seqlen, h,
+                 out_rows + off);
+        if (final_state_rows)
+            for (int64_t n = 0; n < dstate; ++n) final_state_rows[i * dstate + n] = h[n];
+        free(h);
+    }
+}
+
+/* One generated token ("The head reads one token and computes Delta, B and C ... That is
+ * one step", section "Taken Apart"): the same update once, with the state read from and
+ * written back to `state`. */
+void oracle_state_update(double* state, const double* x, const double* dt, const double* A,
+                         const double* B, const double* C, const double* D, const double* z,
+                         const double* dt_bias, int dt_softplus, double* out, int64_t batch,
+                         int64_t dim, int64_t dstate) {
+    int64_t rows = batch * dim;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t b = r / dim, d = r % dim;
+        double* h = state + r * dstate;
+        double xx = dt[r] + (dt_bias ? dt_bias[d] : 0.0);
+        double dlt = dt_softplus ? softplus(xx) : xx;
+        for (int64_t n = 0; n < dstate; ++n) {
+            double abar = exp(dlt * A[d * dstate + n]);
+            h[n] = abar * h[n] + dlt * B[b * dstate + n] * x[r];
+        }
+        double y = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) y += C[b * dstate + n] * h[n];
+        y += (D ? D[d] : 0.0) * x[r];
+        if (z) y *= silu(z[r]);
+        out[r] = y;
+    }
+}

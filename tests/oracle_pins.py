@@ -1,0 +1,237 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+Each pin takes an oracle object (a compiled copy of oracle/selscan_oracle.c) and returns
+the largest error it saw; the caller compares it with the pin's bound. The expected values
+are computed here by other routes: the convolution form of a time-invariant system, the
+solved (non-recursive) form of the recurrence, limits of Delta, hand-worked closed forms and
+linearity. Helper functions below use formulas different from the oracle's
+(logaddexp for softplus, the tanh form of the logistic function for silu).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def softplus_ref(x):
+    return np.logaddexp(0.0, x)
+
+
+def silu_ref(z):
+    return z * 0.5 * (1.0 + np.tanh(0.5 * z))
+
+
+def relerr(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = max(float(np.sqrt(np.mean(ref * ref))), 1e-300)
+    return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), scale)))
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _random_problem(seed, batch=2, dim=3, dstate=5, seqlen=40, lti=False):
+    r = _rng(seed)
+    A = -r.uniform(0.3, 3.0, size=(dim, dstate))
+    D = r.standard_normal(dim)
+    bias = r.uniform(-3.0, 0.5, size=dim)
+    u = r.standard_normal((batch, dim, seqlen))
+    z = r.standard_normal((batch, dim, seqlen))
+    h0 = r.standard_normal((batch, dim, dstate))
+    if lti:
+        delta = np.repeat(r.normal(0.0, 0.5, size=(batch, dim, 1)), seqlen, axis=2)
+        B = np.repeat(r.standard_normal((batch, dstate, 1)), seqlen, axis=2)
+        C = np.repeat(r.standard_normal((batch, dstate, 1)), seqlen, axis=2)
+    else:
+        delta = r.normal(0.0, 0.5, size=(batch, dim, seqlen))
+        B = r.standard_normal((batch, dstate, seqlen))
+        C = r.standard_normal((batch, dstate, seqlen))
+    return dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=bias, h0=h0)
+
+
+def pin_lti_convolution(orc, seed=11, with_state=True):
+    """'Every Step the Same' (world.lapla.si): with the same Delta, A, B, C at every token the
+    output is the input convolved with one fixed kernel K_k = sum_n C[n] Abar[n]^k Bbar[n],
+    computed here in closed form with exp(k*Delta*A) and an O(L^2) sum."""
+    p = _random_problem(seed, lti=True)
+    batch, dim, L = p["u"].shape
+    N = p["A"].shape[1]
+    h0 = p["h0"] if with_state else None
+    out, fin = orc.scan_fwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                            p["delta_bias"], True, h0)
+    ref = np.zeros_like(out)
+    ref_fin = np.zeros_like(fin)
+    k = np.arange(L)
+    for b in range(batch):
+        for d in range(dim):
+            dlt = softplus_ref(p["delta"][b, d, 0] + p["delta_bias"][d])
+            Bn, Cn, An = p["B"][b, :, 0], p["C"][b, :, 0], p["A"][d]
+            decay = np.exp(np.outer(k, dlt * An))  # (L, N): Abar^k
+            K = decay @ (Cn * dlt * Bn)  # kernel K_k
+            u = p["u"][b, d]
+            y = np.array([np.dot(K[: t + 1], u[t::-1]) for t in range(L)])
+            if h0 is not None:
+                y = y + np.exp(np.outer(k + 1, dlt * An)) @ (Cn * h0[b, d])
+            y = (y + p["D"][d] * u) * silu_ref(p["z"][b, d])
+            ref[b, d] = y
+            hf = (decay[::-1] * (dlt * Bn)[None, :] * u[:, None]).sum(axis=0)
+            if h0 is not None:
+                hf = hf + np.exp(L * dlt * An) * h0[b, d]
+            ref_fin[b, d] = hf
+    return max(relerr(out, ref), relerr(fin, ref_fin))
+
+
+def pin_solved_form(orc, seed=12, softplus=True, with_state=True):
+    """The recurrence h_t = exp(Delta_t*A) h_{t-1} + Delta_t*B_t*u_t has the solution
+    h_t = exp(A*S_t) h_init + sum_{s<=t} exp(A*(S_t - S_s)) Delta_s B_s u_s with
+    S_t = Delta_0 + ... + Delta_t. This evaluates that sum directly (no recursion) for
+    time-varying Delta, B, C and reads y_t = C_t . h_t + D u_t, gated by silu(z_t)."""
+    p = _random_problem(seed, batch=2, dim=3, dstate=5, seqlen=32)
+    batch, dim, L = p["u"].shape
+    h0 = p["h0"] if with_state else None
+    out, fin = orc.scan_fwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                            p["delta_bias"], softplus, h0)
+    ref = np.zeros_like(out)
+    ref_fin = np.zeros_like(fin)
+    for b in range(batch):
+        for d in range(dim):
+            x = p["delta"][b, d] + p["delta_bias"][d]
+            dlt = softplus_ref(x) if softplus else x
+            S = np.cumsum(dlt)
+            An = p["A"][d]
+            src = dlt[:, None] * p["B"][b].T * p["u"][b, d][:, None]  # (L, N)
+            for t in range(L):
+                w = np.exp(An[None, :] * (S[t] - S[: t + 1])[:, None])  # (t+1, N)
+                h = (w * src[: t + 1]).sum(axis=0)
+                if h0 is not None:
+                    h = h + np.exp(An * S[t]) * h0[b, d]
+                y = np.dot(p["C"][b][:, t], h) + p["D"][d] * p["u"][b, d, t]
+                ref[b, d, t] = y * silu_ref(p["z"][b, d, t])
+                if t == L - 1:
+                    ref_fin[b, d] = h
+    return max(relerr(out, ref), relerr(fin, ref_fin))
+
+
+def pin_delta_zero(orc, seed=13):
+    """'Chosen by the Token': a small Delta keeps the state and ignores the input. At Delta = 0
+    exactly (softplus off, delta = bias = 0) Abar = 1 and Bbar*x = 0, so the state must come
+    out bit-identical and y_t = (C_t . h0 + D u_t) silu(z_t)."""
+    p = _random_problem(seed)
+    zeros = np.zeros_like(p["delta"])
+    out, fin = orc.scan_fwd(p["u"], zeros, p["A"], p["B"], p["C"], p["D"], p["z"], None, False,
+                            p["h0"])
+    bit_err = float(np.max(np.abs(fin - p["h0"])))
+    ref = (np.einsum("bnt,bdn->bdt", p["C"], p["h0"]) + p["D"][None, :, None] * p["u"]) * silu_ref(p["z"])
+    return max(bit_err * 1e300, relerr(out, ref))  # any state change at all fails the pin
+
+
+def pin_large_delta(orc, seed=14):
+    """'Chosen by the Token': a large Delta resets the state and takes in the current token.
+    With Delta = 50 and A <= -1 the old state is multiplied by at most e^-50, so
+    h_t = 50 B_t u_t and y_t = C_t . h_t + D u_t up to ~1e-21 relative."""
+    p = _random_problem(seed)
+    A = -np.abs(p["A"]) - 1.0
+    big = np.full_like(p["delta"], 50.0)
+    out, fin = orc.scan_fwd(p["u"], big, A, p["B"], p["C"], p["D"], None, None, False, p["h0"])
+    h = 50.0 * p["B"][:, None, :, :] * p["u"][:, :, None, :]  # (b, d, n, t)
+    ref = np.einsum("bnt,bdnt->bdt", p["C"], h) + p["D"][None, :, None] * p["u"]
+    return max(relerr(out, ref), relerr(fin, h[..., -1]))
+
+
+def pin_linearity(orc, seed=15):
+    """Without the gate and from a zero state, y is linear in u (Delta depends on delta only)."""
+    p = _random_problem(seed)
+    r = _rng(seed + 1)
+    u1, u2 = p["u"], r.standard_normal(p["u"].shape)
+    a, c = 0.75, -1.25
+    args = lambda u: (u, p["delta"], p["A"], p["B"], p["C"], p["D"], None, p["delta_bias"], True, None)
+    y1, f1 = orc.scan_fwd(*args(u1))
+    y2, f2 = orc.scan_fwd(*args(u2))
+    y3, f3 = orc.scan_fwd(*args(a * u1 + c * u2))
+    return max(relerr(y3, a * y1 + c * y2), relerr(f3, a * f1 + c * f2))
+
+
+def load_hand_worked():
+    with open(os.path.join(GOLDEN, "hand_worked_n1.json")) as f:
+        return json.load(f)
+
+
+def _zval(zspec, L):
+    if zspec is None:
+        return None
+    if zspec == "ln3":
+        return np.full((1, 1, L), math.log(3.0))
+    return np.asarray(zspec, dtype=np.float64).reshape(1, 1, L)
+
+
+def pin_hand_worked_scan(orc):
+    g = load_hand_worked()
+    worst = 0.0
+    for c in g["scan_cases"]:
+        L = len(c["u"])
+        u = np.asarray(c["u"], dtype=np.float64).reshape(1, 1, L)
+        delta = np.asarray(c["delta"], dtype=np.float64).reshape(1, 1, L)
+        B = np.full((1, 1, L), c["B"])
+        C = np.full((1, 1, L), c["C"])
+        h0 = None if c["h0"] is None else np.full((1, 1, 1), c["h0"])
+        out, fin = orc.scan_fwd(u, delta, np.array([[c["A"]]]), B, C, np.array([c["D"]]),
+                                _zval(c["z"], L), np.array([c["bias"]]), c["softplus"], h0)
+        e = np.asarray(c["expected"])
+        worst = max(worst, float(np.max(np.abs(out[0, 0] - e) / np.maximum(np.abs(e), 1e-300)))
+                    if np.any(e != 0) else float(np.max(np.abs(out[0, 0]))) * 1e300)
+        worst = max(worst, abs(fin[0, 0, 0] - c["final"]) / abs(c["final"]))
+    return worst
+
+
+def pin_hand_worked_update(orc):
+    g = load_hand_worked()
+    worst = 0.0
+    for c in g["update_cases"]:
+        st, out = orc.state_update(np.full((1, 1, 1), c["state"]), np.array([[c["x"]]]),
+                                   np.array([[c["dt"]]]), np.array([[c["A"]]]),
+                                   np.array([[c["B"]]]), np.array([[c["C"]]]),
+                                   np.array([c["D"]]),
+                                   None if c["z"] is None else np.array([[math.log(3.0)]]),
+                                   np.array([c["bias"]]), c["softplus"])
+        worst = max(worst, abs(st[0, 0, 0] - c["state_expected"]) / abs(c["state_expected"]),
+                    abs(out[0, 0] - c["out_expected"]) / abs(c["out_expected"]))
+    return worst
+
+
+def pin_update_is_one_scan_step(orc, seed=16):
+    """The generation step is the scan's update applied once ('Taken Apart': one token read,
+    the state moves once): state_update == a length-1 scan from that state, and L updates in a
+    row == the length-L scan. The scan side is pinned by the pins above."""
+    p = _random_problem(seed, batch=3, dim=4, dstate=5, seqlen=12)
+    batch, dim, L = p["u"].shape
+    st = p["h0"].copy()
+    ys = np.zeros((batch, dim, L))
+    for t in range(L):
+        st, ys[:, :, t] = orc.state_update(st, p["u"][:, :, t], p["delta"][:, :, t], p["A"],
+                                           p["B"][:, :, t], p["C"][:, :, t], p["D"],
+                                           p["z"][:, :, t], p["delta_bias"], True)
+    out, fin = orc.scan_fwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                            p["delta_bias"], True, p["h0"])
+    return max(relerr(ys, out), relerr(st, fin))
+
+
+# (pin function, bound) pairs used by the pin tests and the mutation tests.
+ALL_PINS = [
+    (pin_lti_convolution, 1e-11),
+    (lambda o: pin_lti_convolution(o, seed=21, with_state=False), 1e-11),
+    (pin_solved_form, 1e-11),
+    (lambda o: pin_solved_form(o, seed=22, softplus=False, with_state=False), 1e-11),
+    (pin_delta_zero, 1e-13),
+    (pin_large_delta, 1e-12),
+    (pin_linearity, 1e-11),
+    (pin_hand_worked_scan, 1e-14),
+    (pin_hand_worked_update, 1e-14),
+    (pin_update_is_one_scan_step, 1e-12),
+]

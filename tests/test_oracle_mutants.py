@@ -1,0 +1,73 @@
+"""Each plausible mistake, planted in a copy of the oracle's C source, must fail a pin.
+
+The mistakes are planted in temporary copies compiled on the CPU; the real oracle is
+untouched. This shows the pins in oracle_pins.py constrain every term of the definition.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import Oracle
+from oracle.build import SRC
+from tests import oracle_pins as P
+
+_ROW_UPDATE = """            h[n] = abar * h[n] + bbar_x;
+        }
+        double y = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) y += Cb[n * seqlen + t] * h[n];"""
+
+MUTANTS = {
+    "drop_D_skip": ("y += D_d * u[t];", ""),
+    "exp_sign": ("double abar = exp(dlt * A_d[n]);", "double abar = exp(-dlt * A_d[n]);"),
+    "zoh_instead_of_euler": ("double bbar_x = dlt * Bb[n * seqlen + t] * u[t];",
+                             "double bbar_x = (exp(dlt * A_d[n]) - 1.0) / A_d[n] * Bb[n * seqlen + t] * u[t];"),
+    "missing_delta_in_B": ("double bbar_x = dlt * Bb[n * seqlen + t] * u[t];",
+                           "double bbar_x = Bb[n * seqlen + t] * u[t];"),
+    "B_transposed": ("double bbar_x = dlt * Bb[n * seqlen + t] * u[t];",
+                     "double bbar_x = dlt * Bb[t * dstate + n] * u[t];"),
+    "C_is_B": ("y += Cb[n * seqlen + t] * h[n];", "y += Bb[n * seqlen + t] * h[n];"),
+    "read_before_update": (_ROW_UPDATE, """            h[n] = abar * h[n] + bbar_x;
+        }
+        double y = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) y += Cb[n * seqlen + t] * (h[n] - dlt * Bb[n * seqlen + t] * u[t]) / exp(dlt * A_d[n]);"""),
+    "bias_after_softplus": ("double x = delta[t] + bias;\n        double dlt = softplus_on ? softplus(x) : x;",
+                            "double x = delta[t];\n        double dlt = (softplus_on ? softplus(x) : x) + bias;"),
+    "softplus_dropped_log1p": ("return fmax(x, 0.0) + log1p(exp(-fabs(x)));", "return fmax(x, 0.0);"),
+    "silu_is_sigmoid": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    "initial_state_ignored": ("h[n] = initial_state ? initial_state[r * dstate + n] : 0.0;", "h[n] = 0.0;"),
+    "A_wrong_stride": ("A + d * dstate, B + b * dstate * seqlen,\n                 C + b * dstate * seqlen, D ? D[d] : 0.0, z ? z + off : NULL,",
+                       "A + d, B + b * dstate * seqlen,\n                 C + b * dstate * seqlen, D ? D[d] : 0.0, z ? z + off : NULL,"),
+    "readout_skips_last_state": ("for (int64_t n = 0; n < dstate; ++n) y += Cb[n * seqlen + t] * h[n];",
+                                 "for (int64_t n = 0; n + 1 < dstate; ++n) y += Cb[n * seqlen + t] * h[n];"),
+    "update_drops_batch_of_B": ("h[n] = abar * h[n] + dlt * B[b * dstate + n] * x[r];",
+                                "h[n] = abar * h[n] + dlt * B[n] * x[r];"),
+    "update_bias_ignored": ("double xx = dt[r] + (dt_bias ? dt_bias[d] : 0.0);", "double xx = dt[r];"),
+    "update_gate_dropped": ("if (z) y *= silu(z[r]);", ""),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, source, tmp_path):
+    old, new = MUTANTS[name]
+    assert source.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    src = tmp_path / "mutant.c"
+    src.write_text(source.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-shared", "-o",
+                           str(lib), str(src), "-lm"])
+    orc = Oracle(str(lib))
+    failed = []
+    for i, (fn, bound) in enumerate(P.ALL_PINS):
+        with np.errstate(all="ignore"):
+            err = fn(orc)
+        if not (err <= bound):  # NaN counts as a failure
+            failed.append(i)
+    assert failed, f"mutant {name} passed every pin"
