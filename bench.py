@@ -1,0 +1,488 @@
+"""Benchmark of the selective scan (S6 forward) and the decode step on B300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+
+One step = one ssm_scan_fwd over one batch of the workload (all of: loads, Delta, discretise,
+recurrence, readout + D skip + silu gate, final state). Inputs are synthetic (seeded) and
+resident in HBM before the timed region; L2 is flushed (256 MiB write) before every step,
+outside the per-step CUDA events. The same JSON line also carries the decode sweep
+(64 layers x ssm_state_update per generated token, replayed from CUDA graphs), the
+end-to-end number through host buffers, the roofline of the dominant kernel, the SM clocks
+sampled during the run and the fp64 CPU oracle timed on a bounded sample.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent
+batches: weak scaling, no collective on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import DECODE_CONFIG, make_decode_layer_params, make_decode_state  # noqa: E402
+from workloads import make_decode_tokens, make_scan_inputs, scan_config  # noqa: E402
+
+METRIC = "selective-scan B·D·L elem/s & achieved HBM GB/s (% of peak); decode steps/s"
+SM_PER_GPU_FALLBACK = 148
+ALU_ELEM_PER_CLK_PER_SM = 2.0  # 16 SFU exp2 (32/clk/SM) and 64 FP32 lane-ops (128/clk/SM) per element
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------------------------------
+# helpers
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def scan_algorithmic_bytes(cfg) -> int:
+    """Compulsory HBM bytes of one scan: every input read once, y and the final state
+    written once (the per-token state is never stored)."""
+    ein = 2 if cfg.in_dtype == "bf16" else 4
+    eout = 2 if cfg.out_dtype == "bf16" else 4
+    act = cfg.batch * cfg.dim * cfg.seqlen
+    bc = cfg.batch * cfg.dstate * cfg.seqlen
+    nact_in = 2 + (1 if cfg.has_z else 0)
+    per_ch = cfg.dim * cfg.dstate * 4 + cfg.dim * 4 * ((1 if cfg.has_D else 0) + (1 if cfg.has_bias else 0))
+    return act * (nact_in * ein + eout) + 2 * bc * ein + per_ch + cfg.batch * cfg.dim * cfg.dstate * 4
+
+
+def decode_algorithmic_bytes(batch, dim, dstate) -> int:
+    """Per layer-step: state read + write (fp32), x/dt/z read + out write (bf16), B and C
+    (bf16), A (fp32) and D, dt_bias (fp32)."""
+    return (batch * dim * dstate * 4 * 2 + batch * dim * 2 * 4 + batch * dstate * 2 * 2
+            + dim * dstate * 4 + dim * 4 * 2)
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(p[0]), smax=float(p[1]), util=float(p[2]),
+                                 hw=p[5], hwt=p[6], swt=p[7], swp=p[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["smax"] for r in busy), "reasons": sorted(reasons),
+                "samples": len(busy)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank sets the job time)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+
+def time_scan(cfg, steps, warmup, x, flush, stream, soak_s=1.0):
+    from selective_state_space_110_b300 import ssm_scan_fwd, workspace_size
+    out_dtype = torch.bfloat16 if cfg.out_dtype == "bf16" else torch.float32
+    out = torch.empty(cfg.batch, cfg.dim, cfg.seqlen, dtype=out_dtype, device="cuda")
+    fin = torch.empty(cfg.batch, cfg.dim, cfg.dstate, dtype=torch.float32, device="cuda")
+    ws_n = workspace_size(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda") if ws_n else None
+
+    def call():
+        ssm_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                     x["delta_bias"], x["delta_softplus"], out=out, final_state=fin,
+                     workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.fill_(1)
+            call()
+        # untimed soak so the clock samples see the kernel at steady state
+        t_end = time.time() + soak_s
+        while time.time() < t_end:
+            for _ in range(20):
+                call()
+            stream.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            flush.fill_(1)
+            ev[s][0].record(stream)
+            call()
+            ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in ev]
+    launches_per_step = 2 if ws_n else 1
+    return times, launches_per_step
+
+
+def time_scan_e2e(cfg, steps, warmup, x, stream):
+    """Same scan through the public API from pinned host buffers: every step copies the
+    step's inputs host->device, runs the scan and copies y and the final state back."""
+    from selective_state_space_110_b300 import ssm_scan_fwd, workspace_size
+    names = ["u", "delta", "z", "B", "C"]
+    host = {k: x[k].cpu().pin_memory() for k in names if x[k] is not None}
+    dev = {k: torch.empty_like(x[k]) for k in host}
+    out_dtype = torch.bfloat16 if cfg.out_dtype == "bf16" else torch.float32
+    out = torch.empty(cfg.batch, cfg.dim, cfg.seqlen, dtype=out_dtype, device="cuda")
+    fin = torch.empty(cfg.batch, cfg.dim, cfg.dstate, dtype=torch.float32, device="cuda")
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    ws_n = workspace_size(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda") if ws_n else None
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        ssm_scan_fwd(dev["u"], dev["delta"], x["A"], dev["B"], dev["C"], x["D"], dev.get("z"),
+                     x["delta_bias"], x["delta_softplus"], out=out, final_state=fin,
+                     workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def time_decode(batch, steps, warmup, stream):
+    """Decode sweep: per generated token, ssm_state_update on each of 64 layers (own state,
+    A, D, dt_bias per layer); the 64 calls of a token are one CUDA graph, one graph per slot
+    of the ring of 8 token-input sets."""
+    from selective_state_space_110_b300 import ssm_state_update
+    cfg = DECODE_CONFIG
+    p = make_decode_layer_params(cfg, "cuda")
+    layers = []
+    for l in range(cfg.layers):
+        layers.append(dict(A=p["A"].clone(), D=p["D"].clone(), bias=p["dt_bias"].clone(),
+                           state=make_decode_state(cfg, batch, l, "cuda"),
+                           out=torch.empty(batch, cfg.dim, dtype=torch.bfloat16, device="cuda"),
+                           toks=[make_decode_tokens(cfg, batch, l, s, "cuda") for s in range(cfg.ring)]))
+
+    def token_step(slot):
+        for L in layers:
+            t = L["toks"][slot]
+            ssm_state_update(L["state"], t["x"], t["dt"], L["A"], t["B"], t["C"], L["D"], t["z"],
+                             out=L["out"], dt_bias=L["bias"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            token_step(s % cfg.ring)
+    torch.cuda.synchronize()
+    graphs = []
+    for slot in range(cfg.ring):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            token_step(slot)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(warmup):
+            graphs[s % cfg.ring].replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for s in range(steps):
+            graphs[s % cfg.ring].replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, cfg.layers
+
+
+def cpu_baseline(cfg, x, target_s=12.0):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of rows of the
+    same workload (all tokens of each sampled row)."""
+    import oracle
+    R = cfg.batch * cfg.dim
+    rng = torch.Generator().manual_seed(0)
+    perm = torch.randperm(R, generator=rng)
+
+    def run(nrows):
+        rows = perm[:nrows].sort().values
+        rd = rows.to("cuda")
+        flat = lambda t: t.view(R, -1)[rd].cpu()
+        args = (rows.numpy(), flat(x["u"]), flat(x["delta"]), x["A"].cpu(), x["B"].cpu(),
+                x["C"].cpu(), None if x["D"] is None else x["D"].cpu(),
+                None if x["z"] is None else flat(x["z"]),
+                None if x["delta_bias"] is None else x["delta_bias"].cpu(), x["delta_softplus"])
+        import oracle as o
+        prepared = [o._f64(a) if hasattr(a, "detach") else a for a in args]
+        t0 = time.perf_counter()
+        oracle.scan_fwd_rows(*prepared)
+        return time.perf_counter() - t0
+
+    n0 = min(R, 64)
+    t0 = run(n0)
+    n = int(min(R, max(n0, n0 * target_s / max(t0, 1e-3))))
+    t = run(n) if n > n0 else t0
+    elems = n * cfg.seqlen
+    return {"value": elems / t, "unit": "elem/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} of {R} (batch, channel) rows x all {cfg.seqlen} tokens of {cfg.name} "
+                      f"({elems} elements, {t:.1f} s)"}
+
+
+def run_ours(args):
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    from selective_state_space_110_b300 import LIB_PATH  # noqa: F401  (fails loudly if missing)
+    cfg = scan_config(args.workload)
+    hbm_peak, peak_src = read_peaks()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    x = make_scan_inputs(cfg, "cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    barrier(world)
+    with ClockSampler(local) as clk:
+        times, launches = time_scan(cfg, args.steps, args.warmup, x, flush, stream, args.soak_s)
+    barrier(world)
+    ms_total = max_over_ranks(sum(times), world)
+    ms_step = ms_total / args.steps
+    elems = cfg.elements * world
+    value = elems / (ms_step * 1e-3)
+    clocks = clk.summary()
+
+    e2e_ms, h2d, d2h = time_scan_e2e(cfg, max(2, min(args.steps, 10)), 2, x, stream)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    dec = {}
+    for b in args.decode_batches:
+        dms, nl = time_decode(b, args.decode_steps, 8, stream)
+        dms = max_over_ranks(dms, world)
+        dbytes = decode_algorithmic_bytes(b, DECODE_CONFIG.dim, DECODE_CONFIG.dstate) * nl
+        dec[f"batch{b}"] = {"steps_per_s": round(world * 1e3 / dms, 1),
+                            "tokens_per_s": round(world * b * 1e3 / dms, 1),
+                            "ms_per_step": round(dms, 4),
+                            "achieved_gbs": round(dbytes / (dms * 1e-3) / 1e9, 1),
+                            "hbm_frac": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 3),
+                            "launches_per_step": nl}
+
+    if rank != 0:
+        return
+    alg = scan_algorithmic_bytes(cfg)
+    kern_ms = statistics.mean(times)
+    achieved = alg / (kern_ms * 1e-3) / 1e9
+    sm_mhz = clocks["sm_mhz"] or 1900.0
+    alu_peak_elem = ALU_ELEM_PER_CLK_PER_SM * sms * sm_mhz * 1e6
+    alu_peak_gbs = alu_peak_elem * alg / cfg.elements / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "elem/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in/out, fp32 compute",
+        "data": "synthetic (seeded N(0,1)/N(0,0.25) activations, A=-(n+1), log-uniform dt)",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "dstate": cfg.dstate,
+                   "seqlen": cfg.seqlen, "elements_per_step": cfg.elements * world,
+                   "l2": "256 MiB write before every step, outside the per-step events",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "achieved_gbs": round(achieved, 1),
+        "hbm_frac": round(achieved / hbm_peak, 4),
+        "roofline": {"bound": "alu", "achieved": round(achieved, 1), "peak": round(alu_peak_gbs, 1),
+                     "unit": "GB/s", "frac": round(achieved / alu_peak_gbs, 4), "traffic": None,
+                     "kernel": "scan_chunked_kernel (full pass)",
+                     "peak_note": f"ALU ceiling {ALU_ELEM_PER_CLK_PER_SM} elem/clk/SM x {sms} SMs x "
+                                  f"{sm_mhz:.0f} MHz, as GB/s of compulsory bytes",
+                     "hbm_peak": hbm_peak, "hbm_peak_source": peak_src,
+                     "hbm_frac": round(achieved / hbm_peak, 4)},
+        "e2e": {"value": round(elems / (e2e_ms * 1e-3), 1), "unit": "elem/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+        "decode": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim, **dec},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, x)
+    print(json.dumps(line), flush=True)
+
+
+def run_profile(args):
+    """One scan of the workload (plus one decode layer-step at batch 64): a small, bounded
+    program for ncu captures."""
+    from selective_state_space_110_b300 import ssm_scan_fwd, ssm_state_update
+    cfg = scan_config(args.workload)
+    x = make_scan_inputs(cfg, "cuda")
+    out, fin = ssm_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                            x["delta_bias"], x["delta_softplus"])
+    p = make_decode_layer_params(DECODE_CONFIG, "cuda")
+    st = make_decode_state(DECODE_CONFIG, 64, 0, "cuda")
+    t = make_decode_tokens(DECODE_CONFIG, 64, 0, 0, "cuda")
+    ssm_state_update(st, t["x"], t["dt"], p["A"], t["B"], t["C"], p["D"], t["z"], dt_bias=p["dt_bias"])
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": cfg.name, "finite": bool(torch.isfinite(out).all().item())}))
+
+
+# ------------------------------------------------------------------------------------------
+# reference arm: the fp64 oracle, as it stands, on the host cores
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cfg = scan_config(args.workload)
+    x = make_scan_inputs(cfg.replace(batch=1), "cpu")
+    rows_per_step = 96  # a bounded sample: 96 rows x all tokens per step
+    rows = torch.arange(rows_per_step)
+    flat = lambda t: t.view(cfg.dim, -1)[rows]
+    args_ = [rows.numpy(), flat(x["u"]), flat(x["delta"]), x["A"], x["B"], x["C"], x["D"],
+             flat(x["z"]), x["delta_bias"], True]
+    prepared = [oracle._f64(a) if hasattr(a, "detach") else a for a in args_]
+    for _ in range(args.warmup):
+        oracle.scan_fwd_rows(*prepared)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan_fwd_rows(*prepared)
+    dt = (time.perf_counter() - t0) / args.steps
+    elems = rows_per_step * cfg.seqlen
+    v = elems / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "elem/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "dstate": cfg.dstate,
+                   "seqlen": cfg.seqlen},
+        "cpu_baseline": {"value": round(v, 1), "unit": "elem/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} (batch, channel) rows x all {cfg.seqlen} tokens per step"},
+        "e2e": {"value": round(v, 1), "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="c2_mamba2p8b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-batches", type=int, nargs="*", default=[1, 16, 64])
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="untimed back-to-back scans before the timed steps (clock sampling)")
+    ap.add_argument("--profile", action="store_true",
+                    help="run one scan of the workload and exit (for ncu captures)")
+    args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,123 @@
+/*
+ * libselscan: the selective state-space (S6) recurrence of Mamba on one B300 GPU.
+ *
+ * Two entry points compute the method; two more size and describe.
+ *
+ * The method ("Mamba and State Space Models", world.lapla.si):
+ *   - section "A State of Fixed Size": every token updates a state of fixed size once,
+ *     h <- Abar*h + Bbar*x, and the output is read from the updated state, y = C*h;
+ *   - section "Chosen by the Token": Delta, B and C are computed from each token, A is
+ *     fixed, and the retained fraction is Abar = exp(Delta*A);
+ *   - section "A Scan on the Chip": Delta, A, B, C are read into on-chip memory,
+ *     discretised and run through the recurrence there; only the output is written back,
+ *     never the per-token state.
+ * Per batch b, channel d, state index n and token t this library computes
+ *     Delta   = softplus(delta[b,d,t] + delta_bias[d])     (no softplus if the flag is 0)
+ *     h[n]    = exp(Delta*A[d,n]) * h[n] + Delta*B[b,n,t]*u[b,d,t]
+ *     y       = (sum_n C[b,n,t]*h[n] + D[d]*u[b,d,t]) * silu(z[b,d,t]),  silu(z) = z/(1+e^-z)
+ * with Euler discretisation of B, in fp32 arithmetic, for dstate = 16.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are device memory (or memory the device can address) owned by the caller.
+ *     The library allocates nothing, keeps no pointer after the call returns, and holds no
+ *     global state; calls on different streams are independent.
+ *   - All work is enqueued asynchronously on `stream` (NULL = the legacy default stream).
+ *     The returned status covers argument checks and the launch itself. A non-OK status
+ *     means nothing was launched and no output was written (SELSCAN_ERR_CUDA excepted:
+ *     the launch was attempted and the CUDA runtime reported an error).
+ *   - Every pointer must be 16-byte aligned (SELSCAN_ERR_ALIGNMENT otherwise).
+ *   - Outputs must not overlap inputs (SELSCAN_ERR_INVALID_ARG), except `state` of
+ *     ssm_state_update, which is updated in place by design.
+ *   - NaN and Inf in inputs propagate; they are not checked.
+ */
+#ifndef SELSCAN_H
+#define SELSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* selscan_stream_t;
+
+typedef enum {
+    SELSCAN_F32 = 0,  /* IEEE fp32 */
+    SELSCAN_BF16 = 1  /* bfloat16 */
+} selscan_dtype;
+
+typedef enum {
+    SELSCAN_OK = 0,
+    SELSCAN_ERR_INVALID_ARG = 1,  /* NULL required pointer, bad size, overlapping output */
+    SELSCAN_ERR_UNSUPPORTED = 2,  /* dstate != 16, unknown dtype, no sm_103 device */
+    SELSCAN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
+    SELSCAN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than ssm_scan_workspace_size() */
+    SELSCAN_ERR_CUDA = 5          /* the CUDA runtime reported an error at launch */
+} selscan_status;
+
+/*
+ * ssm_scan_fwd: the selective scan over a whole sequence (prefill / training forward).
+ *
+ * Layouts (contiguous, row-major, last index fastest):
+ *   u, delta, z, out      (batch, dim, seqlen)       dtype in_dtype (out: out_dtype)
+ *   B, C                  (batch, dstate, seqlen)    dtype in_dtype
+ *   A                     (dim, dstate)              fp32, the fixed (negative) A
+ *   D, delta_bias         (dim)                      fp32
+ *   initial_state         (batch, dim, dstate)       fp32, NULL = zeros
+ *   final_state           (batch, dim, dstate)       fp32, the state after token seqlen-1
+ * Optional pointers: D (NULL = no skip term), z (NULL = no gate), delta_bias (NULL = 0),
+ * initial_state, final_state (NULL = not written).
+ * delta_softplus: nonzero applies softplus to delta + delta_bias, zero uses it as is.
+ * dstate must be 16. batch, dim >= 1; seqlen >= 0 (seqlen = 0 writes final_state only).
+ * in_dtype applies to u, delta, z, B and C; out_dtype to out. Arithmetic is fp32.
+ *
+ * workspace / workspace_bytes: scratch device memory of at least
+ * ssm_scan_workspace_size(batch, dim, dstate, seqlen) bytes (NULL/0 when that is 0). Long
+ * sequences with few (batch, channel) rows are split into time segments that run in
+ * parallel; the workspace holds each segment's local end state and its summed Delta. Its
+ * contents on entry do not matter. Two calls running at the same time need two workspaces.
+ */
+selscan_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                            const void* C, const float* D, const void* z,
+                            const float* delta_bias, int delta_softplus, void* out,
+                            float* final_state, int64_t batch, int64_t dim, int64_t dstate,
+                            int64_t seqlen, selscan_dtype in_dtype, selscan_dtype out_dtype,
+                            const float* initial_state, void* workspace, size_t workspace_bytes,
+                            selscan_stream_t stream);
+
+/*
+ * Workspace bytes ssm_scan_fwd needs for this shape on the CURRENT device (the time split
+ * depends on its SM count). 0 means no workspace is needed. Returns 0 for invalid shapes
+ * (ssm_scan_fwd then reports the error).
+ */
+size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
+
+/*
+ * ssm_state_update: one generated token ("Taken Apart": the head reads one token, computes
+ * Delta, B and C, and the state moves once). The same update as one step of ssm_scan_fwd.
+ *
+ *   state                 (batch, dim, dstate)  fp32, read and overwritten in place
+ *   x, dt, z, out         (batch, dim)          dtype in_dtype (out: out_dtype)
+ *   B, C                  (batch, dstate)       dtype in_dtype
+ *   A                     (dim, dstate)         fp32
+ *   D, dt_bias            (dim)                 fp32, NULL = 0
+ * z NULL = no gate. dt_softplus as delta_softplus above. dstate must be 16.
+ * out must not overlap state or any input.
+ */
+selscan_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,
+                                const void* B, const void* C, const float* D, const void* z,
+                                void* out, const float* dt_bias, int dt_softplus, int64_t batch,
+                                int64_t dim, int64_t dstate, selscan_dtype in_dtype,
+                                selscan_dtype out_dtype, selscan_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* selscan_status_string(selscan_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SELSCAN_H */

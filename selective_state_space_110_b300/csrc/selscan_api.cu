@@ -1,0 +1,212 @@
+// C-ABI entry points of libselscan: argument checks, time-segment planning, launches.
+// The declarations and the contract (layouts, ownership, errors) are in include/selscan.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "../../include/selscan.h"
+#include "selscan_launch.h"
+
+#define SELSCAN_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr int64_t kStateN = 16;
+constexpr int64_t kMinSegTokens = 4096;  // shortest time segment worth a split
+constexpr int kWarpsPerSchedulerTarget = 3;
+constexpr size_t kWsAlign = 256;
+
+size_t dtype_size(selscan_dtype t) { return t == SELSCAN_BF16 ? 2 : 4; }
+bool dtype_ok(selscan_dtype t) { return t == SELSCAN_F32 || t == SELSCAN_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void* p, size_t bytes) {
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return {lo, lo + bytes};
+}
+bool overlaps(Range a, Range b) {
+    return a.lo != a.hi && b.lo != b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+// Current device's SM count; UNSUPPORTED unless it is compute capability 10.3 (sm_103).
+selscan_status device_sms(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SELSCAN_ERR_CUDA; }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SELSCAN_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return SELSCAN_ERR_UNSUPPORTED;
+    return SELSCAN_OK;
+}
+
+struct Plan {
+    int nseg;
+    int64_t seg_len;
+    size_t hloc_bytes, dsum_bytes, ws_bytes;
+};
+
+// Time segmentation: split the sequence only when the (b, d) rows alone give fewer than
+// half of `kWarpsPerSchedulerTarget` warps per scheduler; each extra segment costs a second
+// pass over it (the local-end pass), so rows are always preferred to segments.
+Plan make_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
+    const int64_t chunk = selscan::scan_chunk_tokens();
+    const int64_t rows = batch * dim;
+    const int64_t warps = (rows + selscan::scan_rows_per_warp() - 1) / selscan::scan_rows_per_warp();
+    const int64_t target = (int64_t)sms * 4 * kWarpsPerSchedulerTarget;
+    int64_t n = 1;
+    if (2 * warps < target) {
+        n = (target + warps - 1) / warps;
+        n = std::min<int64_t>(n, seqlen / kMinSegTokens);
+        n = std::max<int64_t>(n, 1);
+        n = std::min<int64_t>(n, 65535);
+    }
+    int64_t seg_len = (std::max<int64_t>(seqlen, 1) + n - 1) / n;
+    seg_len = (seg_len + chunk - 1) / chunk * chunk;
+    n = std::max<int64_t>(1, (seqlen + seg_len - 1) / seg_len);
+    Plan p{};
+    p.nseg = (int)n;
+    p.seg_len = seg_len;
+    if (n > 1) {
+        p.hloc_bytes = round_up((size_t)rows * (size_t)(n - 1) * kStateN * sizeof(float), kWsAlign);
+        p.dsum_bytes = round_up((size_t)rows * (size_t)(n - 1) * sizeof(float), kWsAlign);
+    }
+    p.ws_bytes = p.hloc_bytes + p.dsum_bytes;
+    return p;
+}
+
+bool shape_ok(int64_t batch, int64_t dim, int64_t seqlen) {
+    return batch >= 1 && dim >= 1 && seqlen >= 0 && batch <= 65535 &&
+           dim <= (int64_t(1) << 40) && seqlen <= (int64_t(1) << 40);
+}
+
+}  // namespace
+
+SELSCAN_EXPORT const char* selscan_status_string(selscan_status s) {
+    switch (s) {
+        case SELSCAN_OK: return "SELSCAN_OK";
+        case SELSCAN_ERR_INVALID_ARG: return "SELSCAN_ERR_INVALID_ARG: null pointer, bad size or overlapping output";
+        case SELSCAN_ERR_UNSUPPORTED: return "SELSCAN_ERR_UNSUPPORTED: dstate must be 16, dtype f32/bf16, device sm_103";
+        case SELSCAN_ERR_ALIGNMENT: return "SELSCAN_ERR_ALIGNMENT: every pointer must be 16-byte aligned";
+        case SELSCAN_ERR_WORKSPACE: return "SELSCAN_ERR_WORKSPACE: workspace missing or smaller than ssm_scan_workspace_size()";
+        case SELSCAN_ERR_CUDA: return "SELSCAN_ERR_CUDA: the CUDA runtime reported an error";
+    }
+    return "SELSCAN_ERR_UNKNOWN";
+}
+
+SELSCAN_EXPORT size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                              int64_t seqlen) {
+    if (!shape_ok(batch, dim, seqlen) || dstate != kStateN) return 0;
+    int sms = 0;
+    if (device_sms(&sms) != SELSCAN_OK) return 0;
+    return make_plan(batch, dim, seqlen, sms).ws_bytes;
+}
+
+SELSCAN_EXPORT selscan_status ssm_scan_fwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus, void* out,
+    float* final_state, int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    selscan_dtype in_dtype, selscan_dtype out_dtype, const float* initial_state,
+    void* workspace, size_t workspace_bytes, selscan_stream_t stream) {
+    // ---- checks that need no device ----
+    if (dstate != kStateN || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+        return SELSCAN_ERR_UNSUPPORTED;
+    if (!shape_ok(batch, dim, seqlen)) return SELSCAN_ERR_INVALID_ARG;
+    const bool has_tokens = seqlen > 0;
+    if (!A || (has_tokens && (!u || !delta || !B || !C || !out))) return SELSCAN_ERR_INVALID_ARG;
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, out, final_state, initial_state, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
+
+    const size_t ein = dtype_size(in_dtype), eout = dtype_size(out_dtype);
+    const size_t act = (size_t)batch * (size_t)dim * (size_t)seqlen;
+    const size_t bc = (size_t)batch * kStateN * (size_t)seqlen;
+    const size_t st = (size_t)batch * (size_t)dim * kStateN * sizeof(float);
+    const Range in_r[] = {range_of(u, act * ein), range_of(delta, act * ein),
+                          range_of(A, (size_t)dim * kStateN * 4), range_of(B, bc * ein),
+                          range_of(C, bc * ein), range_of(D, D ? (size_t)dim * 4 : 0),
+                          range_of(z, z ? act * ein : 0),
+                          range_of(delta_bias, delta_bias ? (size_t)dim * 4 : 0),
+                          range_of(initial_state, initial_state ? st : 0)};
+    const Range out_r = range_of(out, has_tokens ? act * eout : 0);
+    const Range fin_r = range_of(final_state, final_state ? st : 0);
+    for (const Range& r : in_r)
+        if (overlaps(out_r, r) || overlaps(fin_r, r)) return SELSCAN_ERR_INVALID_ARG;
+    if (overlaps(out_r, fin_r)) return SELSCAN_ERR_INVALID_ARG;
+
+    // ---- device and plan ----
+    int sms = 0;
+    selscan_status s = device_sms(&sms);
+    if (s != SELSCAN_OK) return s;
+    const Plan plan = make_plan(batch, dim, seqlen, sms);
+    if (plan.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < plan.ws_bytes) return SELSCAN_ERR_WORKSPACE;
+        const Range ws_r = range_of(workspace, plan.ws_bytes);
+        for (const Range& r : in_r)
+            if (overlaps(ws_r, r)) return SELSCAN_ERR_INVALID_ARG;
+        if (overlaps(ws_r, out_r) || overlaps(ws_r, fin_r)) return SELSCAN_ERR_INVALID_ARG;
+    }
+
+    selscan::ScanArgs a{};
+    a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.delta_bias = delta_bias; a.out = out; a.final_state = final_state;
+    a.initial_state = initial_state;
+    a.ws_hloc = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+    a.ws_dsum = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.hloc_bytes) : nullptr;
+    a.dim = dim; a.seqlen = seqlen; a.seg_len = plan.seg_len; a.nseg = plan.nseg;
+    a.softplus = delta_softplus ? 1 : 0;
+    const bool vec = (seqlen % 8) == 0;
+    const bool precise = in_dtype == SELSCAN_F32;
+    cudaError_t e = selscan::launch_scan_fwd(a, batch, in_dtype == SELSCAN_BF16,
+                                             out_dtype == SELSCAN_BF16, vec, precise,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}
+
+SELSCAN_EXPORT selscan_status ssm_state_update(float* state, const void* x, const void* dt,
+                                               const float* A, const void* B, const void* C,
+                                               const float* D, const void* z, void* out,
+                                               const float* dt_bias, int dt_softplus,
+                                               int64_t batch, int64_t dim, int64_t dstate,
+                                               selscan_dtype in_dtype, selscan_dtype out_dtype,
+                                               selscan_stream_t stream) {
+    if (dstate != kStateN || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+        return SELSCAN_ERR_UNSUPPORTED;
+    if (!shape_ok(batch, dim, 0)) return SELSCAN_ERR_INVALID_ARG;
+    if (!state || !x || !dt || !A || !B || !C || !out) return SELSCAN_ERR_INVALID_ARG;
+    const void* ptrs[] = {state, x, dt, A, B, C, D, z, out, dt_bias};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
+    const size_t ein = dtype_size(in_dtype), eout = dtype_size(out_dtype);
+    const size_t rows = (size_t)batch * (size_t)dim;
+    const Range in_r[] = {range_of(x, rows * ein), range_of(dt, rows * ein),
+                          range_of(A, (size_t)dim * kStateN * 4),
+                          range_of(B, (size_t)batch * kStateN * ein),
+                          range_of(C, (size_t)batch * kStateN * ein),
+                          range_of(D, D ? (size_t)dim * 4 : 0), range_of(z, z ? rows * ein : 0),
+                          range_of(dt_bias, dt_bias ? (size_t)dim * 4 : 0)};
+    const Range st_r = range_of(state, rows * kStateN * sizeof(float));
+    const Range out_r = range_of(out, rows * eout);
+    for (const Range& r : in_r)
+        if (overlaps(out_r, r) || overlaps(st_r, r)) return SELSCAN_ERR_INVALID_ARG;
+    if (overlaps(out_r, st_r)) return SELSCAN_ERR_INVALID_ARG;
+
+    int sms = 0;
+    selscan_status s = device_sms(&sms);
+    if (s != SELSCAN_OK) return s;
+    selscan::UpdateArgs a{};
+    a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.out = out; a.dt_bias = dt_bias; a.dim = dim; a.rows = (int64_t)rows;
+    a.softplus = dt_softplus ? 1 : 0;
+    cudaError_t e = selscan::launch_state_update(a, in_dtype == SELSCAN_BF16,
+                                                 out_dtype == SELSCAN_BF16,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}

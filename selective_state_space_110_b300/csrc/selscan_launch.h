@@ -1,0 +1,57 @@
+// Internal interface between the C-ABI entry points (selscan_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace selscan {
+
+struct ScanArgs {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    void* out;
+    float* final_state;
+    const float* initial_state;
+    float* ws_hloc;  // (batch*dim, nseg-1, 16): local end state of segments 0..nseg-2
+    float* ws_dsum;  // (batch*dim, nseg-1): sum of Delta over those segments
+    int64_t dim;
+    int64_t seqlen;
+    int64_t seg_len;  // tokens per time segment, a multiple of the chunk length
+    int nseg;         // time segments (1 = no split)
+    int softplus;
+};
+
+// Launches the local-end pass (nseg > 1) and the full pass on `stream`.
+cudaError_t launch_scan_fwd(const ScanArgs& a, int64_t batch, bool in_bf16, bool out_bf16,
+                            bool vec, bool precise, cudaStream_t stream);
+int scan_chunk_tokens();
+int scan_rows_per_cta();
+int scan_rows_per_warp();
+
+struct UpdateArgs {
+    float* state;
+    const void* x;
+    const void* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    void* out;
+    const float* dt_bias;
+    int64_t dim;
+    int64_t rows;  // batch*dim
+    int softplus;
+};
+
+cudaError_t launch_state_update(const UpdateArgs& a, bool in_bf16, bool out_bf16,
+                                cudaStream_t stream);
+
+}  // namespace selscan

@@ -1,0 +1,120 @@
+"""Torch-facing wrappers of the two libselscan entry points.
+
+torch provides device memory and the current stream; the library does all of the work.
+Shapes and layouts follow include/selscan.h:
+  u, delta, z, out (batch, dim, seqlen); B, C (batch, 16, seqlen); A (dim, 16) fp32;
+  D, delta_bias (dim) fp32; states (batch, dim, 16) fp32.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_DT = {torch.float32: _lib.F32, torch.bfloat16: _lib.BF16}
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_dev(name, t, dtype=None, shape=None, device=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _stream_handle(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
+    """Bytes of workspace ssm_scan_fwd needs on the current device (0 = none)."""
+    return int(_lib.lib().ssm_scan_workspace_size(batch, dim, dstate, seqlen))
+
+
+def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 out=None, final_state=None, initial_state=None, workspace=None,
+                 out_dtype=None, return_final_state=True, stream=None):
+    """Selective scan over whole sequences. Returns (out, final_state or None)."""
+    if u.dim() != 3:
+        raise ValueError("u must be (batch, dim, seqlen)")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise ValueError(f"unsupported input dtype {in_dt}")
+    dev = u.device
+    _check_dev("u", u, in_dt, (batch, dim, seqlen), dev)
+    _check_dev("delta", delta, in_dt, (batch, dim, seqlen), dev)
+    _check_dev("A", A, torch.float32, (dim, dstate), dev)
+    _check_dev("B", B, in_dt, (batch, dstate, seqlen), dev)
+    _check_dev("C", C, in_dt, (batch, dstate, seqlen), dev)
+    _check_dev("D", D, torch.float32, (dim,), dev)
+    _check_dev("z", z, in_dt, (batch, dim, seqlen), dev)
+    _check_dev("delta_bias", delta_bias, torch.float32, (dim,), dev)
+    _check_dev("initial_state", initial_state, torch.float32, (batch, dim, dstate), dev)
+    if out is None:
+        out = torch.empty((batch, dim, seqlen), dtype=out_dtype or in_dt, device=dev)
+    if out.dtype not in _DT:
+        raise ValueError(f"unsupported output dtype {out.dtype}")
+    _check_dev("out", out, None, (batch, dim, seqlen), dev)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
+    _check_dev("final_state", final_state, torch.float32, (batch, dim, dstate), dev)
+    with torch.cuda.device(dev):
+        need = workspace_size(batch, dim, dstate, seqlen)
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _check_dev("workspace", workspace, None, None, dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = _lib.lib().ssm_scan_fwd(
+            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(delta_softplus)), _ptr(out), _ptr(final_state), batch, dim, dstate, seqlen,
+            _DT[in_dt], _DT[out.dtype], _ptr(initial_state), _ptr(workspace), ws_bytes,
+            _stream_handle(stream))
+    _lib.check("ssm_scan_fwd", st)
+    return out, final_state
+
+
+def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, out=None, dt_bias=None,
+                     dt_softplus=True, out_dtype=None, stream=None):
+    """One token: updates `state` in place and returns out (batch, dim)."""
+    batch, dim, dstate = state.shape
+    in_dt = x.dtype
+    if in_dt not in _DT:
+        raise ValueError(f"unsupported input dtype {in_dt}")
+    dev = state.device
+    _check_dev("state", state, torch.float32, (batch, dim, dstate), dev)
+    _check_dev("x", x, in_dt, (batch, dim), dev)
+    _check_dev("dt", dt, in_dt, (batch, dim), dev)
+    _check_dev("A", A, torch.float32, (dim, dstate), dev)
+    _check_dev("B", B, in_dt, (batch, dstate), dev)
+    _check_dev("C", C, in_dt, (batch, dstate), dev)
+    _check_dev("D", D, torch.float32, (dim,), dev)
+    _check_dev("z", z, in_dt, (batch, dim), dev)
+    _check_dev("dt_bias", dt_bias, torch.float32, (dim,), dev)
+    if out is None:
+        out = torch.empty((batch, dim), dtype=out_dtype or in_dt, device=dev)
+    if out.dtype not in _DT:
+        raise ValueError(f"unsupported output dtype {out.dtype}")
+    _check_dev("out", out, None, (batch, dim), dev)
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssm_state_update(
+            _ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+            _ptr(out), _ptr(dt_bias), int(bool(dt_softplus)), batch, dim, dstate, _DT[in_dt],
+            _DT[out.dtype], _stream_handle(stream))
+    _lib.check("ssm_state_update", st)
+    return out

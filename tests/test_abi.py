@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, and rejects
+bad arguments with the documented status before touching any device (no compute here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_110_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "selscan.h")
+
+OK, INVALID, UNSUP, ALIGN, WS, CUDA = 0, 1, 2, 3, 4, 5
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) - {"defined"})
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.selscan_status_string(code).decode().startswith(name)
+    assert b"UNKNOWN" in lib.selscan_status_string(99)
+
+
+# Fake, 16-byte aligned, non-overlapping addresses: validation never dereferences them.
+BASE = 1 << 40
+GAP = 1 << 36
+
+
+def fake(i):
+    return BASE + i * GAP
+
+
+def scan_args(**kw):
+    a = dict(u=fake(0), delta=fake(1), A=fake(2), B=fake(3), C=fake(4), D=fake(5), z=fake(6),
+             delta_bias=fake(7), softplus=1, out=fake(8), final_state=fake(9), batch=2, dim=64,
+             dstate=16, seqlen=128, in_dtype=_lib.BF16, out_dtype=_lib.BF16, initial_state=None,
+             workspace=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return a
+
+
+def call_scan(lib, **kw):
+    a = scan_args(**kw)
+    return lib.ssm_scan_fwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                            a["delta_bias"], a["softplus"], a["out"], a["final_state"], a["batch"],
+                            a["dim"], a["dstate"], a["seqlen"], a["in_dtype"], a["out_dtype"],
+                            a["initial_state"], a["workspace"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dstate=8), UNSUP),
+    (dict(dstate=32), UNSUP),
+    (dict(in_dtype=7), UNSUP),
+    (dict(out_dtype=-1), UNSUP),
+    (dict(batch=0), INVALID),
+    (dict(dim=0), INVALID),
+    (dict(seqlen=-1), INVALID),
+    (dict(batch=70000), INVALID),
+    (dict(u=None), INVALID),
+    (dict(delta=None), INVALID),
+    (dict(A=None), INVALID),
+    (dict(B=None), INVALID),
+    (dict(C=None), INVALID),
+    (dict(out=None), INVALID),
+    (dict(u=fake(0) + 2), ALIGN),
+    (dict(z=fake(6) + 8), ALIGN),
+    (dict(final_state=fake(9) + 4), ALIGN),
+    (dict(out=fake(0) + 64), INVALID),          # out inside u
+    (dict(final_state=fake(8) + 16), INVALID),  # final_state inside out
+    (dict(out=fake(5)), INVALID),               # out over D
+    (dict(initial_state=fake(9)), INVALID),     # final_state over initial_state
+])
+def test_scan_rejects(lib, kw, expect):
+    assert call_scan(lib, **kw) == expect
+
+
+def test_scan_valid_args_reach_the_device_check(lib):
+    """Valid arguments pass every host check; on a machine without a CUDA device the call
+    then stops at the device query with SELSCAN_ERR_CUDA (nothing is launched)."""
+    import torch
+    st = call_scan(lib)
+    if torch.cuda.is_available():
+        pytest.skip("device present: covered by the GPU tests")
+    assert st == CUDA
+    # seqlen = 0 needs no activation pointers
+    assert call_scan(lib, seqlen=0, u=None, delta=None, B=None, C=None, out=None) == CUDA
+    assert lib.ssm_scan_workspace_size(1, 1536, 16, 1 << 20) == 0
+    assert lib.ssm_scan_workspace_size(1, 1536, 8, 1 << 20) == 0
+
+
+def call_update(lib, **kw):
+    a = dict(state=fake(0), x=fake(1), dt=fake(2), A=fake(3), B=fake(4), C=fake(5), D=fake(6),
+             z=fake(7), out=fake(8), dt_bias=fake(9), softplus=1, batch=4, dim=5120, dstate=16,
+             in_dtype=_lib.BF16, out_dtype=_lib.BF16, stream=None)
+    a.update(kw)
+    return lib.ssm_state_update(a["state"], a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"],
+                                a["z"], a["out"], a["dt_bias"], a["softplus"], a["batch"],
+                                a["dim"], a["dstate"], a["in_dtype"], a["out_dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dstate=4), UNSUP),
+    (dict(in_dtype=3), UNSUP),
+    (dict(batch=0), INVALID),
+    (dict(state=None), INVALID),
+    (dict(x=None), INVALID),
+    (dict(out=None), INVALID),
+    (dict(B=fake(4) + 2), ALIGN),
+    (dict(out=fake(0) + 32), INVALID),   # out inside state
+    (dict(state=fake(1)), INVALID),      # state over x
+])
+def test_update_rejects(lib, kw, expect):
+    assert call_update(lib, **kw) == expect
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _lib.load()
