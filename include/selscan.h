@@ -55,7 +55,9 @@ typedef enum {
     SELSCAN_ERR_UNSUPPORTED = 2,  /* dstate != 16, unknown dtype, no sm_103 device */
     SELSCAN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
     SELSCAN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than ssm_scan_workspace_size() */
-    SELSCAN_ERR_CUDA = 5          /* the CUDA runtime reported an error at launch */
+    SELSCAN_ERR_CUDA = 5,         /* the CUDA runtime reported an error at launch */
+    SELSCAN_ERR_SCRATCH_LIMIT = 6 /* ssm_scan_fwd_no_alloc: the shape needs more scratch than
+                                     SELSCAN_NO_ALLOC_SCRATCH_BYTES */
 } selscan_status;
 
 /*
@@ -112,6 +114,39 @@ selscan_status ssm_state_update(float* state, const void* x, const void* dt, con
                                 void* out, const float* dt_bias, int dt_softplus, int64_t batch,
                                 int64_t dim, int64_t dstate, selscan_dtype in_dtype,
                                 selscan_dtype out_dtype, selscan_stream_t stream);
+
+/*
+ * ssm_scan_fwd_no_alloc: ssm_scan_fwd for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers that have no way to
+ * obtain scratch memory, such as code inside a host program whose framework owns every device
+ * allocation and offers no allocator hook, or a latency-critical loop that must not call
+ * cudaMalloc because it can synchronise the device. Arguments, layouts, results and errors are
+ * those of ssm_scan_fwd without workspace / workspace_bytes: the time-split scratch is taken
+ * from a fixed array of SELSCAN_NO_ALLOC_SCRATCH_BYTES bytes that the library declares in the
+ * device memory of every GPU that loads it, held until the process exits. The call allocates
+ * nothing and calls no allocating routine.
+ *
+ *   - Shapes whose ssm_scan_workspace_size() exceeds SELSCAN_NO_ALLOC_SCRATCH_BYTES are
+ *     rejected with SELSCAN_ERR_SCRATCH_LIMIT before anything is launched; use ssm_scan_fwd
+ *     with a workspace for them.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     once per device, with that device current). Make that first call before any stream
+ *     capture on that device.
+ *   - Every call on a device shares the one array, and the array keeps what the last call
+ *     left in it (no part of it needs to start at zero). Calls that can overlap on the GPU
+ *     (other streams, other host threads) race on it: serialise them, or use ssm_scan_fwd
+ *     with one workspace per concurrent call.
+ */
+#define SELSCAN_NO_ALLOC_SCRATCH_BYTES ((size_t)524288) /* 512 KiB per device */
+
+selscan_status ssm_scan_fwd_no_alloc(const void* u, const void* delta, const float* A,
+                                     const void* B, const void* C, const float* D,
+                                     const void* z, const float* delta_bias, int delta_softplus,
+                                     void* out, float* final_state, int64_t batch, int64_t dim,
+                                     int64_t dstate, int64_t seqlen, selscan_dtype in_dtype,
+                                     selscan_dtype out_dtype, const float* initial_state,
+                                     selscan_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* selscan_status_string(selscan_status status);

@@ -21,10 +21,15 @@ STATUS = {
     3: "SELSCAN_ERR_ALIGNMENT",
     4: "SELSCAN_ERR_WORKSPACE",
     5: "SELSCAN_ERR_CUDA",
+    6: "SELSCAN_ERR_SCRATCH_LIMIT",
 }
 
 # Every symbol include/selscan.h declares.
-EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selscan_status_string")
+EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selscan_status_string",
+           "ssm_scan_fwd_no_alloc")
+
+# Size of the fixed scratch array behind ssm_scan_fwd_no_alloc (SELSCAN_NO_ALLOC_SCRATCH_BYTES).
+NO_ALLOC_SCRATCH_BYTES = 524288
 
 _VP = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -50,6 +55,9 @@ def load() -> ctypes.CDLL:
     lib.ssm_state_update.restype = ctypes.c_int
     lib.ssm_state_update.argtypes = ([_VP] * 9 + [_VP, ctypes.c_int] + [_I64] * 3 +
                                      [ctypes.c_int, ctypes.c_int, _VP])
+    lib.ssm_scan_fwd_no_alloc.restype = ctypes.c_int
+    lib.ssm_scan_fwd_no_alloc.argtypes = ([_VP] * 8 + [ctypes.c_int, _VP, _VP] + [_I64] * 4 +
+                                          [ctypes.c_int, ctypes.c_int, _VP, _VP])
     lib.selscan_status_string.restype = ctypes.c_char_p
     lib.selscan_status_string.argtypes = [ctypes.c_int]
     return lib

@@ -97,6 +97,7 @@ SELSCAN_EXPORT const char* selscan_status_string(selscan_status s) {
         case SELSCAN_ERR_ALIGNMENT: return "SELSCAN_ERR_ALIGNMENT: every pointer must be 16-byte aligned";
         case SELSCAN_ERR_WORKSPACE: return "SELSCAN_ERR_WORKSPACE: workspace missing or smaller than ssm_scan_workspace_size()";
         case SELSCAN_ERR_CUDA: return "SELSCAN_ERR_CUDA: the CUDA runtime reported an error";
+        case SELSCAN_ERR_SCRATCH_LIMIT: return "SELSCAN_ERR_SCRATCH_LIMIT: this shape needs more scratch than ssm_scan_fwd_no_alloc's static array (SELSCAN_NO_ALLOC_SCRATCH_BYTES); call ssm_scan_fwd with a workspace";
     }
     return "SELSCAN_ERR_UNKNOWN";
 }

@@ -118,3 +118,48 @@ def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, out=None, dt_bias=No
             _DT[out.dtype], _stream_handle(stream))
     _lib.check("ssm_state_update", st)
     return out
+
+
+def ssm_scan_fwd_no_alloc(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                          delta_softplus=True, out=None, final_state=None, initial_state=None,
+                          out_dtype=None, return_final_state=True, stream=None):
+    """ssm_scan_fwd without a workspace, for callers that cannot allocate device scratch.
+
+    The library's time-split scratch comes from its own fixed device array
+    (NO_ALLOC_SCRATCH_BYTES per GPU), shared by every call: calls that overlap on the GPU race.
+    Shapes that need more scratch raise SelscanError (SELSCAN_ERR_SCRATCH_LIMIT). The first
+    call on a device should come before any stream capture on it. `out` and `final_state` are
+    allocated here only when not given.
+    """
+    if u.dim() != 3:
+        raise ValueError("u must be (batch, dim, seqlen)")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise ValueError(f"unsupported input dtype {in_dt}")
+    dev = u.device
+    _check_dev("u", u, in_dt, (batch, dim, seqlen), dev)
+    _check_dev("delta", delta, in_dt, (batch, dim, seqlen), dev)
+    _check_dev("A", A, torch.float32, (dim, dstate), dev)
+    _check_dev("B", B, in_dt, (batch, dstate, seqlen), dev)
+    _check_dev("C", C, in_dt, (batch, dstate, seqlen), dev)
+    _check_dev("D", D, torch.float32, (dim,), dev)
+    _check_dev("z", z, in_dt, (batch, dim, seqlen), dev)
+    _check_dev("delta_bias", delta_bias, torch.float32, (dim,), dev)
+    _check_dev("initial_state", initial_state, torch.float32, (batch, dim, dstate), dev)
+    if out is None:
+        out = torch.empty((batch, dim, seqlen), dtype=out_dtype or in_dt, device=dev)
+    if out.dtype not in _DT:
+        raise ValueError(f"unsupported output dtype {out.dtype}")
+    _check_dev("out", out, None, (batch, dim, seqlen), dev)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
+    _check_dev("final_state", final_state, torch.float32, (batch, dim, dstate), dev)
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssm_scan_fwd_no_alloc(
+            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(delta_softplus)), _ptr(out), _ptr(final_state), batch, dim, dstate, seqlen,
+            _DT[in_dt], _DT[out.dtype], _ptr(initial_state), _stream_handle(stream))
+    _lib.check("ssm_scan_fwd_no_alloc", st)
+    return out, final_state

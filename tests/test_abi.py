@@ -134,3 +134,9 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _lib.load()
+
+
+def test_no_alloc_scratch_size_matches_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define SELSCAN_NO_ALLOC_SCRATCH_BYTES \(\(size_t\)(\d+)\)", text)
+    assert m and int(m.group(1)) == _lib.NO_ALLOC_SCRATCH_BYTES
