@@ -56,8 +56,9 @@ typedef enum {
     SELSCAN_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
     SELSCAN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than ssm_scan_workspace_size() */
     SELSCAN_ERR_CUDA = 5,         /* the CUDA runtime reported an error at launch */
-    SELSCAN_ERR_SCRATCH_LIMIT = 6 /* ssm_scan_fwd_no_alloc: the shape needs more scratch than
-                                     SELSCAN_NO_ALLOC_SCRATCH_BYTES */
+    SELSCAN_ERR_SCRATCH_LIMIT = 6, /* ssm_scan_fwd_no_alloc: the shape needs more scratch than
+                                      SELSCAN_NO_ALLOC_SCRATCH_BYTES */
+    SELSCAN_ERR_DEVICE_TIMEOUT = 7 /* selscan_device_status: a kernel gave up a bounded wait */
 } selscan_status;
 
 /*
@@ -147,6 +148,25 @@ selscan_status ssm_scan_fwd_no_alloc(const void* u, const void* delta, const flo
                                      int64_t dstate, int64_t seqlen, selscan_dtype in_dtype,
                                      selscan_dtype out_dtype, const float* initial_state,
                                      selscan_stream_t stream);
+
+/*
+ * selscan_device_status: errors that kernels of this library detected on the device.
+ *
+ * Every wait inside a kernel (for a TMA copy of B / C to land in shared memory) is bounded
+ * (about two seconds of SM clock); a kernel that gives up records it in a device-side flag of
+ * the library, leaves its outputs incomplete and exits normally, so the GPU and the context
+ * stay usable. This call synchronises `stream`, then returns SELSCAN_ERR_DEVICE_TIMEOUT if the
+ * flag is set on the current device (SELSCAN_OK otherwise); with `reset` nonzero it also clears
+ * the flag. The flag is per device and shared by all streams.
+ */
+selscan_status selscan_device_status(int reset, selscan_stream_t stream);
+
+/*
+ * selscan_selftest_wait_timeout: test hook for the bounded waits. Launches one CTA that waits
+ * on an mbarrier nothing arrives at, gives up after `limit_cycles` SM clocks (1 .. 2^32) and
+ * sets the flag that selscan_device_status reports, as a scan kernel would. Nothing faults.
+ */
+selscan_status selscan_selftest_wait_timeout(int64_t limit_cycles, selscan_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* selscan_status_string(selscan_status status);

@@ -22,11 +22,12 @@ STATUS = {
     4: "SELSCAN_ERR_WORKSPACE",
     5: "SELSCAN_ERR_CUDA",
     6: "SELSCAN_ERR_SCRATCH_LIMIT",
+    7: "SELSCAN_ERR_DEVICE_TIMEOUT",
 }
 
 # Every symbol include/selscan.h declares.
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selscan_status_string",
-           "ssm_scan_fwd_no_alloc")
+           "ssm_scan_fwd_no_alloc", "selscan_device_status", "selscan_selftest_wait_timeout")
 
 # Size of the fixed scratch array behind ssm_scan_fwd_no_alloc (SELSCAN_NO_ALLOC_SCRATCH_BYTES).
 NO_ALLOC_SCRATCH_BYTES = 524288
@@ -58,6 +59,10 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_no_alloc.restype = ctypes.c_int
     lib.ssm_scan_fwd_no_alloc.argtypes = ([_VP] * 8 + [ctypes.c_int, _VP, _VP] + [_I64] * 4 +
                                           [ctypes.c_int, ctypes.c_int, _VP, _VP])
+    lib.selscan_device_status.restype = ctypes.c_int
+    lib.selscan_device_status.argtypes = [ctypes.c_int, _VP]
+    lib.selscan_selftest_wait_timeout.restype = ctypes.c_int
+    lib.selscan_selftest_wait_timeout.argtypes = [_I64, _VP]
     lib.selscan_status_string.restype = ctypes.c_char_p
     lib.selscan_status_string.argtypes = [ctypes.c_int]
     return lib

@@ -7,280 +7,632 @@
 // As on that page, the inputs are read once from HBM, discretised and scanned on chip, and
 // only y (plus the final state) is written back; the per-token state never leaves registers.
 //
-// Work decomposition (B300: 148 SMs, 4 schedulers each, 32 SFU ex2/clk/SM, 128 FP32
-// lanes/clk/SM). The recurrence costs 16 exp2 and 64 FP32 lane-ops per (b, d, t), so the
-// kernel is bound by the SFU and FMA pipes, not by HBM; the layout below is chosen to keep
-// both pipes busy and every SM evenly loaded:
-//   - A row (b, d) is owned by a quad of 4 lanes; lane g of the quad keeps states
-//     4g..4g+3 in registers and updates them with packed f32x2 FMAs. A warp holds 8 rows,
-//     a CTA (4 warps) 32 consecutive channels of one batch.
-//   - The sequence is walked in chunks of 32 tokens. Per chunk the CTA stages B and C
-//     (shared by all channels of the batch) into shared memory as fp32, once.
-//   - Lane g loads tokens 8g..8g+7 of its row (one 128-bit load per tensor), computes
-//     Delta and Delta*u there (once per element) and hands them to its quad through shared
-//     memory. After the 32 steps the quad's partial readouts are summed through a swizzled
-//     shared-memory transpose so lane g again owns tokens 8g..8g+7, where the D skip and
-//     the silu gate are applied and y is stored with one 128-bit store.
+// Cost model on B300 (148 SMs; per SM and clock: 32 ex2 on the SFU, 128 fp32 FMA lanes, one
+// warp-instruction per scheduler, and one shared-memory wavefront = one 32-bit word delivered
+// to each of 32 lanes). Every (t, n) needs one exp2 with its own argument and four fp32
+// operations (Delta*A, k*B, the state FMA, the readout FMA): the SFU and the FMA pipe each
+// allow 2 elements per clock per SM. Every (row, t) also needs all 16 B and 16 C values of
+// token t in the registers of the lanes that hold the row's states; delivered from shared
+// memory that is 32 words, one wavefront, per element, which would cap the scan at 1 element
+// per clock. The layout below is built around those budgets:
+//   - A quad of 4 lanes owns kR rows (b, d), (b, d+1).. of one batch; lane g keeps states
+//     4g..4g+3 of each of its rows in registers and updates them with packed f32x2
+//     operations. The B and C values a lane fetches for a token serve all kR of its rows, so
+//     with kR = 2 the shared-memory delivery is half a wavefront per element.
+//   - A CTA owns 32 consecutive channels of one batch and walks the sequence in chunks of
+//     32/kR tokens. B and C of a chunk (shared by every channel of the batch) arrive by TMA
+//     into a 3-deep ring of shared-memory stages, completion tracked by mbarriers, so their
+//     fetch overlaps the scan of earlier chunks. The CTA converts them once to fp32, one
+//     128-byte row per token (chunk c of token t at position c ^ (t & 7): conflict-free both
+//     for the conversion stores and for the lanes' 16-byte loads).
+//   - Each lane owns 8 consecutive tokens of one of its quad's rows: it loads them (one
+//     128-bit load per tensor, issued one chunk ahead), computes Delta and k = Delta*u once per
+//     element in registers, and its quad receives them by width-4 shuffles, which use no
+//     shared-memory bandwidth. The exp2 arguments of two tokens come from one packed multiply.
+//   - Every 4 tokens each lane writes its partial readouts to shared memory; at the end of
+//     the chunk each lane sums the quad's partials of its 8 tokens, applies the D skip and the
+//     silu gate (packed f32x2) and stores 8 outputs with one 128-bit store.
 //   - Long sequences with few rows are cut into time segments that run in parallel
 //     (grid.y). A first pass (kLocalEnd) scans segments 0..S-2 from a zero state and keeps
-//     only each segment's end state and its summed Delta. The full pass then starts
-//     segment s from the true state, obtained by folding the earlier segments:
-//     h <- exp(A * sum(Delta)) h + h_local_end (the associative combine of the recurrence).
+//     each segment's end state and summed Delta. The full pass then starts segment s from the
+//     true state, folding the earlier segments with the associative combine of the
+//     recurrence: h <- exp(A * sum Delta) h + h_local_end.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "selscan_device.cuh"
 #include "selscan_launch.h"
 
+#ifndef SELSCAN_ROWS_PER_LANE
+#define SELSCAN_ROWS_PER_LANE 2
+#endif
+
 namespace selscan {
 
-constexpr int kChunk = 32;               // tokens per chunk
-constexpr int kWarps = 4;                // warps per CTA
-constexpr int kThreads = kWarps * 32;    // 128
-constexpr int kRowsPerWarp = 8;          // quads per warp
-constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 32 channels
-constexpr int kDkStride = 2 * kChunk + 4;  // floats per row of (Delta, k) pairs; +4 staggers
-                                           // rows across bank groups
+constexpr int kR = SELSCAN_ROWS_PER_LANE;  // rows per quad (and per lane)
+static_assert(kR == 1 || kR == 2, "rows per lane must be 1 or 2");
+constexpr int kRowsPerCta = 32;
+constexpr int kWarps = 4 / kR;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kRowsPerWarp = 8 * kR;
+constexpr int kChunk = 32 / kR;       // tokens per chunk: each lane owns 8 tokens of one row
+constexpr int kBlocks = kChunk / 4;   // 4-token blocks per chunk
+#ifndef SELSCAN_MIN_CTAS_PER_SM
+#define SELSCAN_MIN_CTAS_PER_SM (SELSCAN_ROWS_PER_LANE == 1 ? 5 : 6)
+#endif
+constexpr int kMinCtasPerSm = SELSCAN_MIN_CTAS_PER_SM;  // register budget per thread
+constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s: a TMA stage that never lands
+
+// Error bits a kernel can raise; read (and cleared) by read_device_status().
+__device__ unsigned int g_device_status;
 
 enum class Mode { kFull, kLocalEnd };
 
-// B/C staging layout: s_bc[t][32] holds B[0..15] and C[0..15] of token t as eight 16-byte
-// chunks. Even tokens store B in chunks 0..3 and C in 4..7, odd tokens the other way
-// round. Lane g then reads its 4 B values at chunk g + 4*(t&1) and its 4 C values at
-// chunk g + 4*(1-(t&1)): per token the warp touches 4 distinct chunks (conflict-free
-// broadcast), the offsets are compile-time immediates once t is unrolled, and the staging
-// stores of two adjacent tokens fall in disjoint bank groups.
-__device__ __forceinline__ int bc_chunk_b(int g, int t) { return g + 4 * (t & 1); }
-__device__ __forceinline__ int bc_chunk_c(int g, int t) { return g + 4 * (1 - (t & 1)); }
+template <int kInBytes>
+struct ScanStages {
+    static constexpr int kStages = 3;
+    static constexpr int kTileBytes = 16 * kChunk * kInBytes;
+};
+
+template <int kInBytes>
+struct __align__(128) ScanSmem {
+    using St = ScanStages<kInBytes>;
+    // TMA destinations: raw B and C tiles, [stage][B|C][n][t] in the input dtype.
+    unsigned char raw[St::kStages][2][St::kTileBytes];
+    // fp32 B/C per token: 8 chunks of 4 floats (B states 0-15, C states 0-15); chunk c of
+    // token t sits at position c ^ (t & 7).
+    float bc[2][kChunk][32];
+    // Partial readouts: [warp][row of the quad][4-token block][slot] with slot = lane ^ swz.
+    float4 red[kWarps][kR][kBlocks][32];
+    unsigned long long full[St::kStages];
+};
+
+// ---- TMA / mbarrier primitives (inline PTX) -------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for phase `parity` of `bar`; false if it has not completed after kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long start = clock64();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - start > kWaitLimitCycles) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
+                                            unsigned long long* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// ---- 8-token raw vectors of u / delta / z ---------------------------------------------------
+
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 v;
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+};
+
+// Loads p[0..7] (one or two 128-bit streaming loads; the vector path only ever sees 0 or 8
+// valid tokens) or zeros.
+__device__ __forceinline__ void load_raw(Raw8<__nv_bfloat16>& r, const __nv_bfloat16* p, bool ok) {
+    r.v = ok ? __ldcs(reinterpret_cast<const uint4*>(p)) : make_uint4(0, 0, 0, 0);
+}
+__device__ __forceinline__ void load_raw(Raw8<float>& r, const float* p, bool ok) {
+    if (ok) {
+        r.a = __ldcs(reinterpret_cast<const float4*>(p));
+        r.b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    } else {
+        r.a = r.b = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+__device__ __forceinline__ void unpack(const Raw8<__nv_bfloat16>& r, float (&v)[8]) {
+    v[0] = bf16lo(r.v.x); v[1] = bf16hi(r.v.x); v[2] = bf16lo(r.v.y); v[3] = bf16hi(r.v.y);
+    v[4] = bf16lo(r.v.z); v[5] = bf16hi(r.v.z); v[6] = bf16lo(r.v.w); v[7] = bf16hi(r.v.w);
+}
+__device__ __forceinline__ void unpack(const Raw8<float>& r, float (&v)[8]) {
+    v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w;
+    v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
+}
+
+// ---- fast softplus / silu on pairs (bf16 inputs; fp32 inputs use the exact library forms) ----
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// softplus(x) = max(x, 0) + log1p(w), w = exp(-|x|) in (0, 1]; log1p(w) = w * P(w) with P a
+// degree-6 polynomial fitted to log1p(w)/w on [0, 1] by least squares on Chebyshev nodes
+// (fit_log1p.py beside this file); relative error below 1.4e-6 in addition to the SFU exp2's.
+__device__ __forceinline__ float2 softplus2(float2 x) {
+    const float2 na = __fmul2_rn(make_float2(fabsf(x.x), fabsf(x.y)), f2(-kLog2e));
+    const float2 w = make_float2(ex2_approx(na.x), ex2_approx(na.y));
+    float2 p = __ffma2_rn(w, f2(1.420607697e-02f), f2(-6.660313159e-02f));
+    p = __ffma2_rn(p, w, f2(1.494590789e-01f));
+    p = __ffma2_rn(p, w, f2(-2.351667285e-01f));
+    p = __ffma2_rn(p, w, f2(3.311267793e-01f));
+    p = __ffma2_rn(p, w, f2(-4.998728335e-01f));
+    p = __ffma2_rn(p, w, f2(9.999988079e-01f));
+    return __ffma2_rn(p, w, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+}
+
+// silu(z) = z / (1 + e^-z). For z -> -inf the denominator is +inf and the SFU reciprocal 0.
+__device__ __forceinline__ float2 silu2(float2 z) {
+    const float2 a = __fmul2_rn(z, f2(-kLog2e));
+    const float2 den = __fadd2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), f2(1.f));
+    return __fmul2_rn(z, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
+// Owner lane (within the quad) of row j, token t of a chunk, and its register slot t & 7.
+__device__ __forceinline__ constexpr int owner_of(int j, int t) {
+    return kR == 1 ? (t >> 3) : (2 * j + (t >> 3));
+}
+// XOR swizzle of the partial-readout slots of (row j, block q); the reader of block q of row j
+// is the owner lane swz(j, q), so each quarter-warp of its loads hits 8 distinct bank groups.
+__device__ __forceinline__ constexpr int red_swz(int j, int q) {
+    return kR == 1 ? ((q >> 1) & 3) : ((2 * j + (q >> 1)) & 3);
+}
 
 template <typename Tin, typename Tout, bool kVec, bool kPrecise, Mode kMode>
-__global__ void __launch_bounds__(kThreads) scan_chunked_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
+    scan_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC) {
     constexpr bool kFull = kMode == Mode::kFull;
-    __shared__ __align__(16) float s_bc[2][kChunk][32];
-    __shared__ __align__(16) float s_dk[kWarps][kRowsPerWarp][kDkStride];
-    __shared__ __align__(16) float s_red[kFull ? kWarps : 1][kFull ? 8 * 32 * 4 : 4];
+    using St = ScanStages<sizeof(Tin)>;
+    constexpr int kS = St::kStages;
+    __shared__ ScanSmem<sizeof(Tin)> sm;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int rl = lane >> 2;  // row within the warp
-    const int g = lane & 3;    // quarter of the state owned by this lane
+    const int quad = lane >> 2;
+    const int g = lane & 3;  // quarter of the state owned by this lane
     const int64_t b = blockIdx.z;
     const int seg = blockIdx.y;
-    const int64_t d = (int64_t)blockIdx.x * kRowsPerCta + warp * kRowsPerWarp + rl;
-    const bool active = d < a.dim;
-    const int64_t dc = active ? d : 0;
-    const int64_t row = b * a.dim + dc;
+    const int64_t dim = a.dim;
+    const int64_t d0 = (int64_t)blockIdx.x * kRowsPerCta + warp * kRowsPerWarp + quad * kR;
     const int64_t L = a.seqlen;
     const int64_t t_begin = (int64_t)seg * a.seg_len;
     const int64_t t_end = min(L, t_begin + a.seg_len);
+    const int nchunks = t_end > t_begin ? (int)((t_end - t_begin + kChunk - 1) / kChunk) : 0;
     const int nprev = a.nseg - 1;  // segments with a stored local end state
 
-    // Per-lane constants: A for states 4g..4g+3 (pre-scaled by log2(e) for the SFU exp2).
-    float4 A4 = *reinterpret_cast<const float4*>(a.A + dc * kN + 4 * g);
-    if (!kPrecise) { A4.x *= kLog2e; A4.y *= kLog2e; A4.z *= kLog2e; A4.w *= kLog2e; }
-    const float2 a01 = make_float2(A4.x, A4.y), a23 = make_float2(A4.z, A4.w);
-    const float bias = a.delta_bias ? a.delta_bias[dc] : 0.f;
-    const float Dd = a.D ? a.D[dc] : 0.f;
+    // Rows of this quad; inactive rows (past dim) compute on row 0's parameters and store nothing.
+    bool act[kR];
+    int64_t row[kR];
+#pragma unroll
+    for (int j = 0; j < kR; ++j) {
+        act[j] = d0 + j < dim;
+        row[j] = b * dim + (act[j] ? d0 + j : 0);
+    }
+    // The row and tokens this lane owns: Delta, k, the epilogue and the stores.
+    const int jo = kR == 1 ? 0 : (g >> 1);
+    const int to = 8 * (kR == 1 ? g : (g & 1));
+    const bool own_act = act[jo];
+    const int64_t own_row = row[jo];
+    const int64_t own_d = own_row - b * dim;
 
-    // ---- initial state ----
-    float2 h01 = make_float2(0.f, 0.f), h23 = make_float2(0.f, 0.f);
-    if (kFull) {
-        if (a.initial_state) {
-            float4 s = *reinterpret_cast<const float4*>(a.initial_state + row * kN + 4 * g);
-            h01 = make_float2(s.x, s.y); h23 = make_float2(s.z, s.w);
+    // ---- TMA ring: initialise the barriers and start the first stages ----
+    if (kVec) {
+        if (tid == 0) {
+#pragma unroll
+            for (int s = 0; s < kS; ++s) mbar_init(&sm.full[s], 1);
+            fence_mbar_init();
         }
-        // Fold the local end states of the segments before this one.
-        for (int j = 0; j < seg; ++j) {
-            const float ds = a.ws_dsum[row * nprev + j];
-            const float4 hl = *reinterpret_cast<const float4*>(a.ws_hloc + (row * nprev + j) * kN + 4 * g);
-            if (kPrecise) {  // exp(A*S) h + h_local, with exp written as 1 + expm1
-                const float m0 = expm1f(a01.x * ds), m1 = expm1f(a01.y * ds);
-                const float m2 = expm1f(a23.x * ds), m3 = expm1f(a23.y * ds);
-                h01 = make_float2(fmaf(m0, h01.x, h01.x) + hl.x, fmaf(m1, h01.y, h01.y) + hl.y);
-                h23 = make_float2(fmaf(m2, h23.x, h23.x) + hl.z, fmaf(m3, h23.y, h23.y) + hl.w);
-            } else {
-                const float p0 = ex2_approx(a01.x * ds), p1 = ex2_approx(a01.y * ds);
-                const float p2 = ex2_approx(a23.x * ds), p3 = ex2_approx(a23.y * ds);
-                h01 = make_float2(fmaf(p0, h01.x, hl.x), fmaf(p1, h01.y, hl.y));
-                h23 = make_float2(fmaf(p2, h23.x, hl.z), fmaf(p3, h23.y, hl.w));
+        __syncthreads();
+        if (tid == 0) {
+            for (int c = 0; c < kS && c < nchunks; ++c) {
+                const int x = (int)(t_begin + (int64_t)c * kChunk);
+                mbar_arrive_expect_tx(&sm.full[c], (kFull ? 2 : 1) * St::kTileBytes);
+                tma_load_2d(sm.raw[c][0], &tmB, &sm.full[c], x, (int)(b * kN));
+                if (kFull) tma_load_2d(sm.raw[c][1], &tmC, &sm.full[c], x, (int)(b * kN));
             }
         }
     }
 
-    const Tin* __restrict__ u_row = static_cast<const Tin*>(a.u) + row * L;
-    const Tin* __restrict__ d_row = static_cast<const Tin*>(a.delta) + row * L;
-    const Tin* __restrict__ z_row = a.z ? static_cast<const Tin*>(a.z) + row * L : nullptr;
-    Tout* __restrict__ o_row = static_cast<Tout*>(a.out) + row * L;
+    // Per-row constants: A for states 4g..4g+3, pre-scaled by log2(e) for the SFU exp2, as
+    // (A_n, A_n) pairs so that one packed multiply forms the arguments of two tokens.
+    float4 A4[kR];
+    float2 aa[kR][4];
+#pragma unroll
+    for (int j = 0; j < kR; ++j) {
+        A4[j] = *reinterpret_cast<const float4*>(a.A + (row[j] - b * dim) * kN + 4 * g);
+        if (!kPrecise) {
+            A4[j].x *= kLog2e; A4[j].y *= kLog2e; A4[j].z *= kLog2e; A4[j].w *= kLog2e;
+        }
+        aa[j][0] = f2(A4[j].x); aa[j][1] = f2(A4[j].y); aa[j][2] = f2(A4[j].z); aa[j][3] = f2(A4[j].w);
+    }
+    const float bias = a.delta_bias ? a.delta_bias[own_d] : 0.f;
+    const float Dd = a.D ? a.D[own_d] : 0.f;
+
+    // ---- initial state, then fold the local end states of earlier segments ----
+    float2 h01[kR], h23[kR];
+#pragma unroll
+    for (int j = 0; j < kR; ++j) {
+        h01[j] = make_float2(0.f, 0.f);
+        h23[j] = make_float2(0.f, 0.f);
+        if (!kFull) continue;
+        if (a.initial_state) {
+            const float4 s = *reinterpret_cast<const float4*>(a.initial_state + row[j] * kN + 4 * g);
+            h01[j] = make_float2(s.x, s.y); h23[j] = make_float2(s.z, s.w);
+        }
+        for (int i = 0; i < seg; ++i) {
+            const float ds = a.ws_dsum[row[j] * nprev + i];
+            const float4 hl = *reinterpret_cast<const float4*>(a.ws_hloc + (row[j] * nprev + i) * kN + 4 * g);
+            if (kPrecise) {  // exp(A*S) h + h_local, with exp written as 1 + expm1
+                const float m0 = expm1f(A4[j].x * ds), m1 = expm1f(A4[j].y * ds);
+                const float m2 = expm1f(A4[j].z * ds), m3 = expm1f(A4[j].w * ds);
+                h01[j] = make_float2(fmaf(m0, h01[j].x, h01[j].x) + hl.x, fmaf(m1, h01[j].y, h01[j].y) + hl.y);
+                h23[j] = make_float2(fmaf(m2, h23[j].x, h23[j].x) + hl.z, fmaf(m3, h23[j].y, h23[j].y) + hl.w);
+            } else {
+                const float p0 = ex2_approx(A4[j].x * ds), p1 = ex2_approx(A4[j].y * ds);
+                const float p2 = ex2_approx(A4[j].z * ds), p3 = ex2_approx(A4[j].w * ds);
+                h01[j] = make_float2(fmaf(p0, h01[j].x, hl.x), fmaf(p1, h01[j].y, hl.y));
+                h23[j] = make_float2(fmaf(p2, h23[j].x, hl.z), fmaf(p3, h23[j].y, hl.w));
+            }
+        }
+    }
+
+    const Tin* __restrict__ u_row = static_cast<const Tin*>(a.u) + own_row * L;
+    const Tin* __restrict__ d_row = static_cast<const Tin*>(a.delta) + own_row * L;
+    const Tin* __restrict__ z_row = a.z ? static_cast<const Tin*>(a.z) + own_row * L : nullptr;
+    Tout* __restrict__ o_row = static_cast<Tout*>(a.out) + own_row * L;
     const Tin* __restrict__ Bb = static_cast<const Tin*>(a.B) + b * kN * L;
     const Tin* __restrict__ Cb = static_cast<const Tin*>(a.C) + b * kN * L;
 
-    float* dkrow = &s_dk[warp][rl][0];
-    float dsum = 0.f, dsum_c = 0.f;  // Kahan sum of Delta (kLocalEnd)
-    int buf = 0;
+    // Offsets (floats) of this lane's B chunk g ^ m within a token row, for m = 0..3; chunk
+    // positions for t & 7 = m are g ^ m (+16 floats when m >= 4) for B and the other half for C.
+    int offB[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) offB[m] = 4 * (g ^ m);
 
-    for (int64_t t0 = t_begin; t0 < t_end; t0 += kChunk) {
-        __syncwarp();
-        // ---- stage B (and C) of this chunk: thread -> (token tt, state quad j) ----
-        {
-            const int tt = tid >> 2, j = tid & 3;
-            const int64_t t = t0 + tt;
-            const bool ok = t < t_end;
-            float4 bv = make_float4(0.f, 0.f, 0.f, 0.f), cv = bv;
-            if (ok) {
-                bv.x = to_f32(Bb[(4 * j + 0) * L + t]); bv.y = to_f32(Bb[(4 * j + 1) * L + t]);
-                bv.z = to_f32(Bb[(4 * j + 2) * L + t]); bv.w = to_f32(Bb[(4 * j + 3) * L + t]);
-                if (kFull) {
-                    cv.x = to_f32(Cb[(4 * j + 0) * L + t]); cv.y = to_f32(Cb[(4 * j + 1) * L + t]);
-                    cv.z = to_f32(Cb[(4 * j + 2) * L + t]); cv.w = to_f32(Cb[(4 * j + 3) * L + t]);
-                }
-            }
-            float* r = &s_bc[buf][tt][0];
-            *reinterpret_cast<float4*>(r + 4 * bc_chunk_b(j, tt)) = bv;
-            if (kFull) *reinterpret_cast<float4*>(r + 4 * bc_chunk_c(j, tt)) = cv;
-        }
+    float dsum = 0.f, dsum_c = 0.f;  // Kahan sum of Delta over owned tokens (kLocalEnd)
 
-        // ---- this lane's 8 tokens: Delta and Delta*u, once per element ----
-        const int64_t tl = t0 + 8 * g;
+    // The vector path prefetches the next chunk's 8 owned tokens into registers.
+    Raw8<Tin> nu, nd, nz;
+    if (kVec && nchunks > 0) {
+        const int64_t tl = t_begin + to;
+        const bool ok = own_act && tl < t_end;
+        load_raw(nu, u_row + tl, ok);
+        load_raw(nd, d_row + tl, ok);
+        if (kFull && z_row) load_raw(nz, z_row + tl, ok);
+    }
+
+    bool timed_out = false;
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t t0 = t_begin + (int64_t)c * kChunk;
+        const int stage = c % kS;
+        const uint32_t parity = (uint32_t)((c / kS) & 1);
+        const int buf = c & 1;
+        const int64_t tl = t0 + to;
         const int64_t left = t_end - tl;
-        const int nval = !active || left <= 0 ? 0 : (left >= 8 ? 8 : (int)left);
+        const int nval = !own_act || left <= 0 ? 0 : (left >= 8 ? 8 : (int)left);
+
+        // ---- this lane's 8 owned tokens of u, delta (and z) ----
         float uf[8], df[8], zf[8];
-        load8<Tin, kVec>(u_row + tl, nval, uf);
-        load8<Tin, kVec>(d_row + tl, nval, df);
-        if (kFull && z_row) load8<Tin, kVec>(z_row + tl, nval, zf);
-        {
-            float dl[8], kl[8];
-            float part = 0.f;
+        if (kVec) {
+            unpack(nu, uf);
+            unpack(nd, df);
+            if (kFull && z_row) unpack(nz, zf);
+            if (c + 1 < nchunks) {  // prefetch the next chunk
+                const int64_t tn = tl + kChunk;
+                const bool ok = own_act && tn < t_end;
+                load_raw(nu, u_row + tn, ok);
+                load_raw(nd, d_row + tn, ok);
+                if (kFull && z_row) load_raw(nz, z_row + tn, ok);
+            }
+        } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float x = df[i] + bias;
-                float dt = a.softplus ? softplus_f<kPrecise>(x) : x;
-                dt = i < nval ? dt : 0.f;  // padding tokens: Abar = 1, no input -> h unchanged
-                dl[i] = dt;
-                kl[i] = dt * uf[i];
-                part += dt;
+                uf[i] = i < nval ? to_f32(u_row[tl + i]) : 0.f;
+                df[i] = i < nval ? to_f32(d_row[tl + i]) : 0.f;
+                if (kFull && z_row) zf[i] = i < nval ? to_f32(z_row[tl + i]) : 0.f;
+            }
+        }
+
+        // ---- Delta and k = Delta*u of the owned tokens; padding tokens get Delta = 0 ----
+        float dl[8], kl[8];
+        {
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                float2 x = __fadd2_rn(make_float2(df[i], df[i + 1]), f2(bias));
+                float2 dt;
+                if (!a.softplus) {
+                    dt = x;
+                } else if (kPrecise) {
+                    dt = make_float2(softplus_f<true>(x.x), softplus_f<true>(x.y));
+                } else {
+                    dt = softplus2(x);
+                }
+                dl[i] = dt.x; dl[i + 1] = dt.y;
+            }
+            if (nval < 8) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dl[i] = i < nval ? dl[i] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const float2 kv = __fmul2_rn(make_float2(dl[i], dl[i + 1]), make_float2(uf[i], uf[i + 1]));
+                kl[i] = kv.x; kl[i + 1] = kv.y;
             }
             if (!kFull) {  // Kahan-compensated running sum of Delta over the segment
+                float part = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) part += dl[i];
                 const float yk = part - dsum_c;
                 const float tk = dsum + yk;
                 dsum_c = (tk - dsum) - yk;
                 dsum = tk;
             }
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<float4*>(dkrow + 16 * g + 4 * m) =
-                    make_float4(dl[2 * m], kl[2 * m], dl[2 * m + 1], kl[2 * m + 1]);
         }
-        __syncthreads();
 
-        // ---- the recurrence over the chunk's 32 tokens ----
-        const float* pbc = &s_bc[buf][0][4 * g];
-        float yp[kChunk];
+        // ---- B and C of this chunk -> fp32 per-token rows (item = chunk-column x token) ----
+        if (kVec && !mbar_wait_bounded(&sm.full[stage], parity)) timed_out = true;
 #pragma unroll
-        for (int s = 0; s < kChunk; s += 2) {
-            const float4 q = *reinterpret_cast<const float4*>(dkrow + 2 * s);
+        for (int cc = 0; cc < (kFull ? 2 : 1); ++cc) {
+            const int item = tid + kThreads * cc;
+            const int tt = item % kChunk;
+            const int ch = item / kChunk;  // 0..7: B quads 0-3, C quads 0-3
+            const int isC = ch >> 2, q = ch & 3;
+            float4 v;
+            if (kVec) {
+                const Tin* tile = reinterpret_cast<const Tin*>(sm.raw[stage][isC]);
+                v.x = to_f32(tile[(4 * q + 0) * kChunk + tt]);
+                v.y = to_f32(tile[(4 * q + 1) * kChunk + tt]);
+                v.z = to_f32(tile[(4 * q + 2) * kChunk + tt]);
+                v.w = to_f32(tile[(4 * q + 3) * kChunk + tt]);
+            } else {
+                const Tin* src = isC ? Cb : Bb;
+                const int64_t t = t0 + tt;
+                const bool ok = t < t_end;
+                v.x = ok ? to_f32(src[(4 * q + 0) * L + t]) : 0.f;
+                v.y = ok ? to_f32(src[(4 * q + 1) * L + t]) : 0.f;
+                v.z = ok ? to_f32(src[(4 * q + 2) * L + t]) : 0.f;
+                v.w = ok ? to_f32(src[(4 * q + 3) * L + t]) : 0.f;
+            }
+            *reinterpret_cast<float4*>(&sm.bc[buf][tt][4 * (ch ^ (tt & 7))]) = v;
+        }
+        if (__syncthreads_or(timed_out)) {
+            // A B/C stage never arrived: record it and leave, after giving the copies this
+            // CTA still has in flight a bounded chance to land.
+            if (tid == 0) {
+                atomicOr(&g_device_status, 1u);
+                for (int k = 1; k < kS && c + k < nchunks; ++k)
+                    mbar_wait_bounded(&sm.full[(c + k) % kS], (uint32_t)(((c + k) / kS) & 1));
+            }
+            return;
+        }
+        // Every thread has read stage `stage`: refill it with chunk c + kS.
+        if (kVec && tid == 0 && c + kS < nchunks) {
+            const int x = (int)(t0 + (int64_t)kS * kChunk);
+            mbar_arrive_expect_tx(&sm.full[stage], (kFull ? 2 : 1) * St::kTileBytes);
+            tma_load_2d(sm.raw[stage][0], &tmB, &sm.full[stage], x, (int)(b * kN));
+            if (kFull) tma_load_2d(sm.raw[stage][1], &tmC, &sm.full[stage], x, (int)(b * kN));
+        }
+
+        // ---- the recurrence over the chunk's tokens, 4 at a time ----
+        const float* const bcb = &sm.bc[buf][0][0];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t = s + e;
-                const float dt = e ? q.z : q.x;
-                const float k = e ? q.w : q.y;
-                const float4 Bv = *reinterpret_cast<const float4*>(pbc + 32 * t + 4 * (bc_chunk_b(0, t)));
-                const float2 dd = make_float2(dt, dt);
-                const float2 e01 = __fmul2_rn(dd, a01);
-                const float2 e23 = __fmul2_rn(dd, a23);
-                const float2 kk = make_float2(k, k);
-                const float2 kb01 = __fmul2_rn(kk, make_float2(Bv.x, Bv.y));
-                const float2 kb23 = __fmul2_rn(kk, make_float2(Bv.z, Bv.w));
-                if (kPrecise) {
-                    // Abar = 1 + expm1(Delta*A): the decay's distance from 1 keeps full
-                    // relative precision, so a slowly decaying state accumulates no bias
-                    // from rounding Abar itself (h = h + em1*h in one fma, then + Bbar*x).
-                    const float2 m01 = make_float2(expm1f(e01.x), expm1f(e01.y));
-                    const float2 m23 = make_float2(expm1f(e23.x), expm1f(e23.y));
-                    h01 = __fadd2_rn(__ffma2_rn(m01, h01, h01), kb01);
-                    h23 = __fadd2_rn(__ffma2_rn(m23, h23, h23), kb23);
-                } else {
-                    const float2 ab01 = make_float2(ex2_approx(e01.x), ex2_approx(e01.y));
-                    const float2 ab23 = make_float2(ex2_approx(e23.x), ex2_approx(e23.y));
-                    h01 = __ffma2_rn(ab01, h01, kb01);
-                    h23 = __ffma2_rn(ab23, h23, kb23);
+        for (int q = 0; q < kBlocks; ++q) {
+            // exp2 arguments of tokens (4q, 4q+1) and (4q+2, 4q+3), per row and state
+            float2 ea[kR][4], eb[kR][4];
+#pragma unroll
+            for (int j = 0; j < kR; ++j) {
+                float dq[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 4 * q + e;
+                    dq[e] = __shfl_sync(0xffffffffu, dl[t & 7], owner_of(j, t), 4);
                 }
-                if (kFull) {
-                    const float4 Cv = *reinterpret_cast<const float4*>(pbc + 32 * t + 4 * (bc_chunk_c(0, t)));
-                    float2 y2 = __fmul2_rn(make_float2(Cv.x, Cv.y), h01);
-                    y2 = __ffma2_rn(make_float2(Cv.z, Cv.w), h23, y2);
-                    yp[t] = y2.x + y2.y;
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    ea[j][n] = __fmul2_rn(make_float2(dq[0], dq[1]), aa[j][n]);
+                    eb[j][n] = __fmul2_rn(make_float2(dq[2], dq[3]), aa[j][n]);
                 }
+            }
+            float yq[kR][4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = 4 * q + e;
+                const int m = t & 7;
+                const float* rowp = bcb + 32 * t + offB[m & 3];
+                const float4 Bv = *reinterpret_cast<const float4*>(rowp + ((m & 4) ? 16 : 0));
+                const float4 Cv = *reinterpret_cast<const float4*>(rowp + ((m & 4) ? 0 : 16));
+#pragma unroll
+                for (int j = 0; j < kR; ++j) {
+                    const float kt = __shfl_sync(0xffffffffu, kl[t & 7], owner_of(j, t), 4);
+                    const float2 kk = f2(kt);
+                    float arg[4];
+#pragma unroll
+                    for (int n = 0; n < 4; ++n)
+                        arg[n] = e == 0 ? ea[j][n].x : e == 1 ? ea[j][n].y : e == 2 ? eb[j][n].x : eb[j][n].y;
+                    const float2 kb01 = __fmul2_rn(kk, make_float2(Bv.x, Bv.y));
+                    const float2 kb23 = __fmul2_rn(kk, make_float2(Bv.z, Bv.w));
+                    if (kPrecise) {
+                        // Abar = 1 + expm1(Delta*A): the decay's distance from 1 keeps full
+                        // relative precision, so a slowly decaying state accumulates no bias
+                        // from rounding Abar itself.
+                        const float2 m01 = make_float2(expm1f(arg[0]), expm1f(arg[1]));
+                        const float2 m23 = make_float2(expm1f(arg[2]), expm1f(arg[3]));
+                        h01[j] = __fadd2_rn(__ffma2_rn(m01, h01[j], h01[j]), kb01);
+                        h23[j] = __fadd2_rn(__ffma2_rn(m23, h23[j], h23[j]), kb23);
+                    } else {
+                        const float2 ab01 = make_float2(ex2_approx(arg[0]), ex2_approx(arg[1]));
+                        const float2 ab23 = make_float2(ex2_approx(arg[2]), ex2_approx(arg[3]));
+                        h01[j] = __ffma2_rn(ab01, h01[j], kb01);
+                        h23[j] = __ffma2_rn(ab23, h23[j], kb23);
+                    }
+                    if (kFull) {
+                        float2 y2 = __fmul2_rn(make_float2(Cv.x, Cv.y), h01[j]);
+                        y2 = __ffma2_rn(make_float2(Cv.z, Cv.w), h23[j], y2);
+                        yq[j][e] = y2.x + y2.y;
+                    }
+                }
+            }
+            if (kFull) {
+#pragma unroll
+                for (int j = 0; j < kR; ++j)
+                    sm.red[warp][j][q][lane ^ red_swz(j, q)] =
+                        make_float4(yq[j][0], yq[j][1], yq[j][2], yq[j][3]);
             }
         }
 
         if (kFull) {
-            // ---- sum the quad's partial readouts; lane g ends with tokens 8g..8g+7 ----
-            // Lane l stores its partials of tokens 4j..4j+3 at slot l ^ ((j >> 1) & 3) of
-            // block j: conflict-free stores, and conflict-free loads below.
-            float* red = &s_red[warp][0];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<float4*>(red + 4 * (32 * j + (lane ^ ((j >> 1) & 3)))) =
-                    make_float4(yp[4 * j], yp[4 * j + 1], yp[4 * j + 2], yp[4 * j + 3]);
+            // ---- sum the quad's partial readouts of the owned tokens ----
             __syncwarp();
-            float Y[8];
+            float2 Y[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) Y[i] = 0.f;
+            for (int i = 0; i < 4; ++i) Y[i] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
-                const int j = 2 * g + jj;
+                const int q = to / 4 + jj;
 #pragma unroll
                 for (int gp = 0; gp < 4; ++gp) {
-                    const float4 v = *reinterpret_cast<const float4*>(
-                        red + 4 * (32 * j + ((4 * rl + gp) ^ g)));
-                    Y[4 * jj + 0] += v.x; Y[4 * jj + 1] += v.y;
-                    Y[4 * jj + 2] += v.z; Y[4 * jj + 3] += v.w;
+                    const float4 v = sm.red[warp][jo][q][(4 * quad + gp) ^ g];
+                    Y[2 * jj] = __fadd2_rn(Y[2 * jj], make_float2(v.x, v.y));
+                    Y[2 * jj + 1] = __fadd2_rn(Y[2 * jj + 1], make_float2(v.z, v.w));
                 }
             }
             // ---- D skip, silu gate, store ----
+            float out8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float y = fmaf(Dd, uf[i], Y[i]);
-                if (z_row) y *= silu_f<kPrecise>(zf[i]);
-                Y[i] = y;
+            for (int i = 0; i < 4; ++i) {
+                float2 y = __ffma2_rn(f2(Dd), make_float2(uf[2 * i], uf[2 * i + 1]), Y[i]);
+                if (z_row) {
+                    const float2 zz = make_float2(zf[2 * i], zf[2 * i + 1]);
+                    y = __fmul2_rn(y, kPrecise ? make_float2(silu_f<true>(zz.x), silu_f<true>(zz.y))
+                                               : silu2(zz));
+                }
+                out8[2 * i] = y.x; out8[2 * i + 1] = y.y;
             }
-            store8<Tout, kVec>(o_row + tl, nval, Y);
+            store8<Tout, kVec>(o_row + tl, nval, out8);
+            __syncwarp();  // the quad's partials are consumed before the next chunk rewrites them
         }
-        buf ^= 1;
     }
 
     if (kFull) {
-        if (active && a.final_state && seg == a.nseg - 1)
-            *reinterpret_cast<float4*>(a.final_state + row * kN + 4 * g) =
-                make_float4(h01.x, h01.y, h23.x, h23.y);
+        if (a.final_state && seg == a.nseg - 1) {
+#pragma unroll
+            for (int j = 0; j < kR; ++j)
+                if (act[j])
+                    *reinterpret_cast<float4*>(a.final_state + row[j] * kN + 4 * g) =
+                        make_float4(h01[j].x, h01[j].y, h23[j].x, h23[j].y);
+        }
     } else {
-        // Lane g summed Delta over tokens 8g..8g+7 of every chunk; the row's total is the
-        // sum over its quad (all 32 lanes take part in the shuffles).
+        // Each owner lane summed Delta over its tokens of every chunk; the row's total is the
+        // sum over the row's owner lanes (all 32 lanes take part in the shuffles).
         float s = dsum - dsum_c;
         s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        if (active) {
-            *reinterpret_cast<float4*>(a.ws_hloc + (row * nprev + seg) * kN + 4 * g) =
-                make_float4(h01.x, h01.y, h23.x, h23.y);
-            if (g == 0) a.ws_dsum[row * nprev + seg] = s;
-        }
+        if (kR == 1) s += __shfl_xor_sync(0xffffffffu, s, 2);
+#pragma unroll
+        for (int j = 0; j < kR; ++j)
+            if (act[j])
+                *reinterpret_cast<float4*>(a.ws_hloc + (row[j] * nprev + seg) * kN + 4 * g) =
+                    make_float4(h01[j].x, h01[j].y, h23[j].x, h23[j].y);
+        if (own_act && (kR == 1 ? g == 0 : (g & 1) == 0)) a.ws_dsum[own_row * nprev + seg] = s;
     }
 }
 
+// ---- host side ---------------------------------------------------------------------------------
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Map of B or C viewed as a 2-D array (batch*16 rows, seqlen tokens); box = one chunk x 16 rows.
+cudaError_t make_bc_map(CUtensorMap* m, const void* base, int64_t batch, int64_t seqlen,
+                        bool bf16) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const size_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)seqlen, (cuuint64_t)(batch * kN)};
+    cuuint64_t strides[1] = {(cuuint64_t)(seqlen * es)};
+    cuuint32_t box[2] = {(cuuint32_t)kChunk, (cuuint32_t)kN};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename Tin, typename Tout, bool kVec, bool kPrecise>
-static cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) {
+cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) {
+    CUtensorMap mB{}, mC{};
+    if (kVec && a.seqlen > 0) {
+        const bool bf = sizeof(Tin) == 2;
+        cudaError_t e = make_bc_map(&mB, a.B, batch, a.seqlen, bf);
+        if (e == cudaSuccess) e = make_bc_map(&mC, a.C, batch, a.seqlen, bf);
+        if (e != cudaSuccess) return e;
+    }
     const unsigned gx = (unsigned)((a.dim + kRowsPerCta - 1) / kRowsPerCta);
     if (a.nseg > 1) {
         dim3 grid(gx, (unsigned)(a.nseg - 1), (unsigned)batch);
-        scan_chunked_kernel<Tin, Tout, kVec, kPrecise, Mode::kLocalEnd><<<grid, kThreads, 0, stream>>>(a);
+        scan_kernel<Tin, Tout, kVec, kPrecise, Mode::kLocalEnd><<<grid, kThreads, 0, stream>>>(a, mB, mC);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     dim3 grid(gx, (unsigned)a.nseg, (unsigned)batch);
-    scan_chunked_kernel<Tin, Tout, kVec, kPrecise, Mode::kFull><<<grid, kThreads, 0, stream>>>(a);
+    scan_kernel<Tin, Tout, kVec, kPrecise, Mode::kFull><<<grid, kThreads, 0, stream>>>(a, mB, mC);
     return cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
-static cudaError_t launch_io(const ScanArgs& a, int64_t batch, bool vec, bool precise,
-                             cudaStream_t stream) {
+cudaError_t launch_io(const ScanArgs& a, int64_t batch, bool vec, bool precise,
+                      cudaStream_t stream) {
     if (vec) {
         return precise ? launch_typed<Tin, Tout, true, true>(a, batch, stream)
                        : launch_typed<Tin, Tout, true, false>(a, batch, stream);
@@ -288,6 +640,8 @@ static cudaError_t launch_io(const ScanArgs& a, int64_t batch, bool vec, bool pr
     return precise ? launch_typed<Tin, Tout, false, true>(a, batch, stream)
                    : launch_typed<Tin, Tout, false, false>(a, batch, stream);
 }
+
+}  // namespace
 
 cudaError_t launch_scan_fwd(const ScanArgs& a, int64_t batch, bool in_bf16, bool out_bf16,
                             bool vec, bool precise, cudaStream_t stream) {
@@ -300,8 +654,41 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, int64_t batch, bool in_bf16, bool
                     : launch_io<float, float>(a, batch, vec, precise, stream);
 }
 
+cudaError_t read_device_status(unsigned int* status, bool reset, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(status, g_device_status, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && reset && *status) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(zero), 0,
+                                    cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    return e;
+}
+
+__global__ void wait_selftest_kernel(long long limit_cycles) {
+    __shared__ unsigned long long bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // Phase 0 of `bar` never completes: nothing arrives on it.
+    const long long start = clock64();
+    bool done = false;
+    while (!done && clock64() - start < limit_cycles) done = mbar_try_wait(&bar, 0);
+    if (!done && threadIdx.x == 0) atomicOr(&g_device_status, 1u);
+}
+
+cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_cycles);
+    return cudaGetLastError();
+}
+
 int scan_chunk_tokens() { return kChunk; }
 int scan_rows_per_cta() { return kRowsPerCta; }
 int scan_rows_per_warp() { return kRowsPerWarp; }
+int scan_ctas_per_sm() { return kMinCtasPerSm; }
 
 }  // namespace selscan

@@ -13,7 +13,6 @@ namespace {
 
 constexpr int64_t kStateN = 16;
 constexpr int64_t kMinSegTokens = 4096;  // shortest time segment worth a split
-constexpr int kWarpsPerSchedulerTarget = 3;
 constexpr size_t kWsAlign = 256;
 
 size_t dtype_size(selscan_dtype t) { return t == SELSCAN_BF16 ? 2 : 4; }
@@ -53,17 +52,18 @@ struct Plan {
     size_t hloc_bytes, dsum_bytes, ws_bytes;
 };
 
-// Time segmentation: split the sequence only when the (b, d) rows alone give fewer than
-// half of `kWarpsPerSchedulerTarget` warps per scheduler; each extra segment costs a second
-// pass over it (the local-end pass), so rows are always preferred to segments.
+// Time segmentation: split the sequence only when the (b, d) rows alone fill less than half of
+// the CTA slots of the GPU (scan_ctas_per_sm per SM). Each extra segment costs a second pass
+// over it (the local-end pass), so rows are always preferred to segments; the number of
+// segments is the largest that still fits every CTA of the full pass into one wave.
 Plan make_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
     const int64_t chunk = selscan::scan_chunk_tokens();
     const int64_t rows = batch * dim;
-    const int64_t warps = (rows + selscan::scan_rows_per_warp() - 1) / selscan::scan_rows_per_warp();
-    const int64_t target = (int64_t)sms * 4 * kWarpsPerSchedulerTarget;
+    const int64_t ctas = batch * ((dim + selscan::scan_rows_per_cta() - 1) / selscan::scan_rows_per_cta());
+    const int64_t slots = (int64_t)sms * selscan::scan_ctas_per_sm();
     int64_t n = 1;
-    if (2 * warps < target) {
-        n = (target + warps - 1) / warps;
+    if (2 * ctas <= slots) {
+        n = slots / ctas;
         n = std::min<int64_t>(n, seqlen / kMinSegTokens);
         n = std::max<int64_t>(n, 1);
         n = std::min<int64_t>(n, 65535);
@@ -97,6 +97,7 @@ SELSCAN_EXPORT const char* selscan_status_string(selscan_status s) {
         case SELSCAN_ERR_ALIGNMENT: return "SELSCAN_ERR_ALIGNMENT: every pointer must be 16-byte aligned";
         case SELSCAN_ERR_WORKSPACE: return "SELSCAN_ERR_WORKSPACE: workspace missing or smaller than ssm_scan_workspace_size()";
         case SELSCAN_ERR_CUDA: return "SELSCAN_ERR_CUDA: the CUDA runtime reported an error";
+        case SELSCAN_ERR_DEVICE_TIMEOUT: return "SELSCAN_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait on the device (results of that launch are invalid)";
         case SELSCAN_ERR_SCRATCH_LIMIT: return "SELSCAN_ERR_SCRATCH_LIMIT: this shape needs more scratch than ssm_scan_fwd_no_alloc's static array (SELSCAN_NO_ALLOC_SCRATCH_BYTES); call ssm_scan_fwd with a workspace";
     }
     return "SELSCAN_ERR_UNKNOWN";
@@ -163,7 +164,9 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
     a.ws_dsum = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.hloc_bytes) : nullptr;
     a.dim = dim; a.seqlen = seqlen; a.seg_len = plan.seg_len; a.nseg = plan.nseg;
     a.softplus = delta_softplus ? 1 : 0;
-    const bool vec = (seqlen % 8) == 0;
+    // 128-bit loads of 8 tokens and TMA tiles of B / C need seqlen % 8 == 0 (16-byte row
+    // strides) and 32-bit token coordinates.
+    const bool vec = (seqlen % 8) == 0 && seqlen < (int64_t(1) << 31) - 64;
     const bool precise = in_dtype == SELSCAN_F32;
     cudaError_t e = selscan::launch_scan_fwd(a, batch, in_dtype == SELSCAN_BF16,
                                              out_dtype == SELSCAN_BF16, vec, precise,
@@ -210,4 +213,26 @@ SELSCAN_EXPORT selscan_status ssm_state_update(float* state, const void* x, cons
                                                  out_dtype == SELSCAN_BF16,
                                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}
+
+SELSCAN_EXPORT selscan_status selscan_device_status(int reset, selscan_stream_t stream) {
+    unsigned int bits = 0;
+    if (selscan::read_device_status(&bits, reset != 0, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SELSCAN_ERR_CUDA;
+    }
+    return bits ? SELSCAN_ERR_DEVICE_TIMEOUT : SELSCAN_OK;
+}
+
+SELSCAN_EXPORT selscan_status selscan_selftest_wait_timeout(int64_t limit_cycles,
+                                                            selscan_stream_t stream) {
+    if (limit_cycles <= 0 || limit_cycles > (int64_t(1) << 32)) return SELSCAN_ERR_INVALID_ARG;
+    int sms = 0;
+    selscan_status s = device_sms(&sms);
+    if (s != SELSCAN_OK) return s;
+    return selscan::launch_wait_selftest(limit_cycles, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SELSCAN_OK
+               : SELSCAN_ERR_CUDA;
 }

@@ -34,6 +34,14 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, int64_t batch, bool in_bf16, bool
 int scan_chunk_tokens();
 int scan_rows_per_cta();
 int scan_rows_per_warp();
+int scan_ctas_per_sm();  // CTAs per SM the scan kernels are built to fit
+
+// Copies the device error bits raised by kernels of this library (synchronises `stream`);
+// with `reset`, clears them afterwards.
+cudaError_t read_device_status(unsigned int* status, bool reset, cudaStream_t stream);
+// Launches one CTA that waits on an mbarrier no one arrives at, for at most `limit_cycles`
+// SM clocks, and then raises the timeout bit exactly as a scan kernel would.
+cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t stream);
 
 struct UpdateArgs {
     float* state;
