@@ -34,6 +34,37 @@ __device__ __forceinline__ float silu_f(float z) {
     return kPrecise ? z / (1.f + expf(-z)) : __fdividef(z, 1.f + __expf(-z));
 }
 
+// ---- fast softplus / silu on pairs (bf16 inputs; fp32 inputs use the exact library forms) ----
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// softplus(x) = max(x, 0) + log1p(w), w = exp(-|x|) in (0, 1]; log1p(w) = w * P(w) with P a
+// degree-6 polynomial fitted to log1p(w)/w on [0, 1] by least squares on Chebyshev nodes
+// (fit_log1p.py in this directory); relative error below 1.4e-6 in addition to the SFU exp2's.
+__device__ __forceinline__ float2 softplus2(float2 x) {
+    const float2 na = __fmul2_rn(make_float2(fabsf(x.x), fabsf(x.y)), f2(-kLog2e));
+    const float2 w = make_float2(ex2_approx(na.x), ex2_approx(na.y));
+    float2 p = __ffma2_rn(w, f2(1.420607697e-02f), f2(-6.660313159e-02f));
+    p = __ffma2_rn(p, w, f2(1.494590789e-01f));
+    p = __ffma2_rn(p, w, f2(-2.351667285e-01f));
+    p = __ffma2_rn(p, w, f2(3.311267793e-01f));
+    p = __ffma2_rn(p, w, f2(-4.998728335e-01f));
+    p = __ffma2_rn(p, w, f2(9.999988079e-01f));
+    return __ffma2_rn(p, w, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+}
+
+// silu(z) = z / (1 + e^-z). For z -> -inf the denominator is +inf and the SFU reciprocal 0.
+__device__ __forceinline__ float2 silu2(float2 z) {
+    const float2 a = __fmul2_rn(z, f2(-kLog2e));
+    const float2 den = __fadd2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), f2(1.f));
+    return __fmul2_rn(z, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
 // ---- element loads / stores ---------------------------------------------------------------
 
 __device__ __forceinline__ float to_f32(float v) { return v; }

@@ -8,10 +8,17 @@
 //   y = (sum_n C[b,n] h[n] + D[d] x) * silu(z).
 //
 // The step is bound by HBM: per (b, d) it reads and writes 64 bytes of fp32 state and does
-// 16 exps. Each quad of lanes owns one row; lane g streams states 4g..4g+3 (one 16-byte load
-// and one 16-byte store), so a warp moves 8 full rows of contiguous state, fully coalesced.
-// The 16-term readout is summed with two quad shuffles. Transcendentals use the accurate
-// library functions (softplus via log1p, the decay via expm1): they hide under the traffic.
+// 16 exps. A quad of lanes owns one row; lane g streams states 4g..4g+3 (one 16-byte load and
+// one 16-byte store, evict-first), so a warp moves 8 full rows of contiguous state, fully
+// coalesced; A (per channel) comes through L2. The grid is (channel blocks, batch), so no
+// lane divides. The readout is summed with two quad shuffles. bf16 tokens use the SFU exp2 and
+// the fitted softplus of the scan; fp32 tokens use the accurate library functions.
+//
+// Successive decode steps of a model are dependent launches on one stream. The kernel is
+// launched with programmatic stream serialization: it lets the next launch in the stream
+// start its setup at once and waits (griddepcontrol.wait) for every earlier grid to complete
+// and publish its memory before it reads anything, so the launch latency of layer l+1 hides
+// under layer l without changing what either computes.
 #include "selscan_device.cuh"
 #include "selscan_launch.h"
 
@@ -19,57 +26,108 @@ namespace selscan {
 
 constexpr int kUpdThreads = 256;
 
-template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(kUpdThreads) state_update_kernel(const UpdateArgs a) {
-    const int64_t q = (int64_t)blockIdx.x * kUpdThreads + threadIdx.x;
-    const int g = threadIdx.x & 3;
-    const int64_t row_raw = q >> 2;
-    const bool active = row_raw < a.rows;
-    const int64_t row = active ? row_raw : 0;
-    const int64_t d = row % a.dim, b = row / a.dim;
+template <typename Tin>
+__device__ __forceinline__ void load4(const Tin* p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+    const float4 r = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 r = __ldg(reinterpret_cast<const uint2*>(p));
+    v[0] = bf16lo(r.x); v[1] = bf16hi(r.x); v[2] = bf16lo(r.y); v[3] = bf16hi(r.y);
+}
 
-    float4 h = *reinterpret_cast<const float4*>(a.state + row * kN + 4 * g);
-    const float4 A4 = *reinterpret_cast<const float4*>(a.A + d * kN + 4 * g);
-    const Tin* Bp = static_cast<const Tin*>(a.B) + b * kN + 4 * g;
-    const Tin* Cp = static_cast<const Tin*>(a.C) + b * kN + 4 * g;
+template <typename Tin, typename Tout, bool kPrecise>
+__global__ void __launch_bounds__(kUpdThreads) state_update_kernel(const UpdateArgs a) {
+    // Wait for earlier grids in the stream (a no-op without programmatic serialization),
+    // then let the next one begin its launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int64_t b = blockIdx.y;
+    const int64_t d_raw = ((int64_t)blockIdx.x * kUpdThreads + threadIdx.x) >> 2;
+    const int g = threadIdx.x & 3;
+    const bool active = d_raw < a.dim;
+    const int64_t d = active ? d_raw : 0;
+    const int64_t row = b * a.dim + d;
+
+    float4* const sp = reinterpret_cast<float4*>(a.state + row * kN + 4 * g);
+    float4 h = __ldcs(sp);
+    float4 A4 = __ldg(reinterpret_cast<const float4*>(a.A + d * kN + 4 * g));
+    float Bv[4], Cv[4];
+    load4<Tin>(static_cast<const Tin*>(a.B) + b * kN + 4 * g, Bv);
+    load4<Tin>(static_cast<const Tin*>(a.C) + b * kN + 4 * g, Cv);
     const float x = to_f32(static_cast<const Tin*>(a.x)[row]);
     const float xdt = to_f32(static_cast<const Tin*>(a.dt)[row]) + (a.dt_bias ? a.dt_bias[d] : 0.f);
-    const float dt = a.softplus ? softplus_f<true>(xdt) : xdt;
+    const float zv = a.z ? to_f32(static_cast<const Tin*>(a.z)[row]) : 0.f;
+    const float Dd = a.D ? a.D[d] : 0.f;
+
+    float dt;
+    if (!a.softplus) dt = xdt;
+    else if (kPrecise) dt = softplus_f<true>(xdt);
+    else dt = softplus2(make_float2(xdt, xdt)).x;
     const float k = dt * x;
 
-    // exp(Delta*A) h = h + expm1(Delta*A) h: the decay's distance from 1 keeps full relative
-    // precision, so thousands of generated tokens accumulate no bias from rounding Abar.
-    h.x = fmaf(expm1f(dt * A4.x), h.x, h.x) + k * to_f32(Bp[0]);
-    h.y = fmaf(expm1f(dt * A4.y), h.y, h.y) + k * to_f32(Bp[1]);
-    h.z = fmaf(expm1f(dt * A4.z), h.z, h.z) + k * to_f32(Bp[2]);
-    h.w = fmaf(expm1f(dt * A4.w), h.w, h.w) + k * to_f32(Bp[3]);
-    float y = to_f32(Cp[0]) * h.x;
-    y = fmaf(to_f32(Cp[1]), h.y, y);
-    y = fmaf(to_f32(Cp[2]), h.z, y);
-    y = fmaf(to_f32(Cp[3]), h.w, y);
+    if (kPrecise) {
+        // exp(Delta*A) h = h + expm1(Delta*A) h: the decay's distance from 1 keeps full
+        // relative precision over thousands of generated tokens.
+        h.x = fmaf(expm1f(dt * A4.x), h.x, h.x) + k * Bv[0];
+        h.y = fmaf(expm1f(dt * A4.y), h.y, h.y) + k * Bv[1];
+        h.z = fmaf(expm1f(dt * A4.z), h.z, h.z) + k * Bv[2];
+        h.w = fmaf(expm1f(dt * A4.w), h.w, h.w) + k * Bv[3];
+    } else {
+        const float s = dt * kLog2e;
+        h.x = fmaf(ex2_approx(s * A4.x), h.x, k * Bv[0]);
+        h.y = fmaf(ex2_approx(s * A4.y), h.y, k * Bv[1]);
+        h.z = fmaf(ex2_approx(s * A4.z), h.z, k * Bv[2]);
+        h.w = fmaf(ex2_approx(s * A4.w), h.w, k * Bv[3]);
+    }
+    float y = Cv[0] * h.x;
+    y = fmaf(Cv[1], h.y, y);
+    y = fmaf(Cv[2], h.z, y);
+    y = fmaf(Cv[3], h.w, y);
     y += __shfl_xor_sync(0xffffffffu, y, 1);
     y += __shfl_xor_sync(0xffffffffu, y, 2);
     if (!active) return;
-    *reinterpret_cast<float4*>(a.state + row * kN + 4 * g) = h;
+    __stcs(sp, h);
     if (g == 0) {
-        y = fmaf(a.D ? a.D[d] : 0.f, x, y);
-        if (a.z) y *= silu_f<true>(to_f32(static_cast<const Tin*>(a.z)[row]));
+        y = fmaf(Dd, x, y);
+        if (a.z) y *= kPrecise ? silu_f<true>(zv) : silu2(make_float2(zv, zv)).x;
         static_cast<Tout*>(a.out)[row] = from_f32<Tout>(y);
     }
+}
+
+template <typename Tin, typename Tout, bool kPrecise>
+static cudaError_t launch_one(const UpdateArgs& a, int64_t batch, cudaStream_t stream) {
+    const int64_t lanes = a.dim * 4;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((lanes + kUpdThreads - 1) / kUpdThreads), (unsigned)batch, 1);
+    cfg.blockDim = dim3(kUpdThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, state_update_kernel<Tin, Tout, kPrecise>, a);
 }
 
 cudaError_t launch_state_update(const UpdateArgs& a, bool in_bf16, bool out_bf16,
                                 cudaStream_t stream) {
     using bf = __nv_bfloat16;
-    const int64_t threads = a.rows * 4;
-    const unsigned grid = (unsigned)((threads + kUpdThreads - 1) / kUpdThreads);
+    const int64_t batch = a.rows / a.dim;
+    cudaError_t e;
     if (in_bf16) {
-        if (out_bf16) state_update_kernel<bf, bf><<<grid, kUpdThreads, 0, stream>>>(a);
-        else state_update_kernel<bf, float><<<grid, kUpdThreads, 0, stream>>>(a);
+        e = out_bf16 ? launch_one<bf, bf, false>(a, batch, stream)
+                     : launch_one<bf, float, false>(a, batch, stream);
     } else {
-        if (out_bf16) state_update_kernel<float, bf><<<grid, kUpdThreads, 0, stream>>>(a);
-        else state_update_kernel<float, float><<<grid, kUpdThreads, 0, stream>>>(a);
+        e = out_bf16 ? launch_one<float, bf, true>(a, batch, stream)
+                     : launch_one<float, float, true>(a, batch, stream);
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
