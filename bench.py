@@ -386,7 +386,7 @@ def run_ours(args):
         "hbm_frac": round(achieved / hbm_peak, 4),
         "roofline": {"bound": "alu", "achieved": round(achieved, 1), "peak": round(alu_peak_gbs, 1),
                      "unit": "GB/s", "frac": round(achieved / alu_peak_gbs, 4), "traffic": None,
-                     "kernel": "scan_chunked_kernel (full pass)",
+                     "kernel": "scan_kernel (full pass)",
                      "peak_note": f"ALU ceiling {ALU_ELEM_PER_CLK_PER_SM} elem/clk/SM x {sms} SMs x "
                                   f"{sm_mhz:.0f} MHz, as GB/s of compulsory bytes",
                      "hbm_peak": hbm_peak, "hbm_peak_source": peak_src,

@@ -45,24 +45,23 @@
 #include "selscan_device.cuh"
 #include "selscan_launch.h"
 
-#ifndef SELSCAN_ROWS_PER_LANE
-#define SELSCAN_ROWS_PER_LANE 2
-#endif
-
 namespace selscan {
 
-constexpr int kR = SELSCAN_ROWS_PER_LANE;  // rows per quad (and per lane)
-static_assert(kR == 1 || kR == 2, "rows per lane must be 1 or 2");
 constexpr int kRowsPerCta = 32;
-constexpr int kWarps = 4 / kR;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kRowsPerWarp = 8 * kR;
-constexpr int kChunk = 32 / kR;       // tokens per chunk: each lane owns 8 tokens of one row
-constexpr int kBlocks = kChunk / 4;   // 4-token blocks per chunk
-#ifndef SELSCAN_MIN_CTAS_PER_SM
-#define SELSCAN_MIN_CTAS_PER_SM (SELSCAN_ROWS_PER_LANE == 1 ? 5 : 6)
-#endif
-constexpr int kMinCtasPerSm = SELSCAN_MIN_CTAS_PER_SM;  // register budget per thread
+constexpr int kMaxChunk = 32;  // time segments are multiples of this many tokens
+
+// Geometry for kR rows per quad (and per lane). kR = 2 halves the B/C shared-memory traffic
+// per element but also the number of warps; the launcher picks it per shape.
+template <int kR>
+struct Geo {
+    static_assert(kR == 1 || kR == 2, "rows per lane must be 1 or 2");
+    static constexpr int kWarps = 4 / kR;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int kRowsPerWarp = 8 * kR;
+    static constexpr int kChunk = 32 / kR;      // tokens per chunk: each lane owns 8 of one row
+    static constexpr int kBlocks = kChunk / 4;  // 4-token blocks per chunk
+    static constexpr int kMinCtas = kR == 1 ? 5 : 6;  // register budget per thread
+};
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s: a TMA stage that never lands
 
 // Error bits a kernel can raise; read (and cleared) by read_device_status().
@@ -70,22 +69,23 @@ __device__ unsigned int g_device_status;
 
 enum class Mode { kFull, kLocalEnd };
 
-template <int kInBytes>
+template <int kInBytes, int kR>
 struct ScanStages {
     static constexpr int kStages = 3;
-    static constexpr int kTileBytes = 16 * kChunk * kInBytes;
+    static constexpr int kTileBytes = 16 * Geo<kR>::kChunk * kInBytes;
 };
 
-template <int kInBytes>
+template <int kInBytes, int kR>
 struct __align__(128) ScanSmem {
-    using St = ScanStages<kInBytes>;
+    using St = ScanStages<kInBytes, kR>;
+    static constexpr int kChunk = Geo<kR>::kChunk;
     // TMA destinations: raw B and C tiles, [stage][B|C][n][t] in the input dtype.
     unsigned char raw[St::kStages][2][St::kTileBytes];
     // fp32 B/C per token: 8 chunks of 4 floats (B states 0-15, C states 0-15); chunk c of
     // token t sits at position c ^ (t & 7).
     float bc[2][kChunk][32];
     // Partial readouts: [warp][row of the quad][4-token block][slot] with slot = lane ^ swz.
-    float4 red[kWarps][kR][kBlocks][32];
+    float4 red[Geo<kR>::kWarps][kR][Geo<kR>::kBlocks][32];
     unsigned long long full[St::kStages];
 };
 
@@ -173,23 +173,29 @@ __device__ __forceinline__ void unpack(const Raw8<float>& r, float (&v)[8]) {
 }
 
 // Owner lane (within the quad) of row j, token t of a chunk, and its register slot t & 7.
+template <int kR>
 __device__ __forceinline__ constexpr int owner_of(int j, int t) {
     return kR == 1 ? (t >> 3) : (2 * j + (t >> 3));
 }
 // XOR swizzle of the partial-readout slots of (row j, block q); the reader of block q of row j
 // is the owner lane swz(j, q), so each quarter-warp of its loads hits 8 distinct bank groups.
+template <int kR>
 __device__ __forceinline__ constexpr int red_swz(int j, int q) {
     return kR == 1 ? ((q >> 1) & 3) : ((2 * j + (q >> 1)) & 3);
 }
 
-template <typename Tin, typename Tout, bool kVec, bool kPrecise, Mode kMode>
-__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
+template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, Mode kMode>
+__global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
     scan_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC) {
     constexpr bool kFull = kMode == Mode::kFull;
-    using St = ScanStages<sizeof(Tin)>;
+    constexpr int kThreads = Geo<kR>::kThreads;
+    constexpr int kRowsPerWarp = Geo<kR>::kRowsPerWarp;
+    constexpr int kChunk = Geo<kR>::kChunk;
+    constexpr int kBlocks = Geo<kR>::kBlocks;
+    using St = ScanStages<sizeof(Tin), kR>;
     constexpr int kS = St::kStages;
-    __shared__ ScanSmem<sizeof(Tin)> sm;
+    __shared__ ScanSmem<sizeof(Tin), kR> sm;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -430,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int t = 4 * q + e;
-                    dq[e] = __shfl_sync(0xffffffffu, dl[t & 7], owner_of(j, t), 4);
+                    dq[e] = __shfl_sync(0xffffffffu, dl[t & 7], owner_of<kR>(j, t), 4);
                 }
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {
@@ -448,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                 const float4 Cv = *reinterpret_cast<const float4*>(rowp + ((m & 4) ? 0 : 16));
 #pragma unroll
                 for (int j = 0; j < kR; ++j) {
-                    const float kt = __shfl_sync(0xffffffffu, kl[t & 7], owner_of(j, t), 4);
+                    const float kt = __shfl_sync(0xffffffffu, kl[t & 7], owner_of<kR>(j, t), 4);
                     const float2 kk = f2(kt);
                     float arg[4];
 #pragma unroll
@@ -480,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
             if (kFull) {
 #pragma unroll
                 for (int j = 0; j < kR; ++j)
-                    sm.red[warp][j][q][lane ^ red_swz(j, q)] =
+                    sm.red[warp][j][q][lane ^ red_swz<kR>(j, q)] =
                         make_float4(yq[j][0], yq[j][1], yq[j][2], yq[j][3]);
             }
         }
@@ -563,13 +569,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Map of B or C viewed as a 2-D array (batch*16 rows, seqlen tokens); box = one chunk x 16 rows.
 cudaError_t make_bc_map(CUtensorMap* m, const void* base, int64_t batch, int64_t seqlen,
-                        bool bf16) {
+                        bool bf16, int chunk) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     const size_t es = bf16 ? 2 : 4;
     cuuint64_t dims[2] = {(cuuint64_t)seqlen, (cuuint64_t)(batch * kN)};
     cuuint64_t strides[1] = {(cuuint64_t)(seqlen * es)};
-    cuuint32_t box[2] = {(cuuint32_t)kChunk, (cuuint32_t)kN};
+    cuuint32_t box[2] = {(cuuint32_t)chunk, (cuuint32_t)kN};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                     const_cast<void*>(base), dims, strides, box, estr,
@@ -578,36 +584,43 @@ cudaError_t make_bc_map(CUtensorMap* m, const void* base, int64_t batch, int64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <typename Tin, typename Tout, bool kVec, bool kPrecise>
+template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise>
 cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) {
+    using G = Geo<kR>;
     CUtensorMap mB{}, mC{};
     if (kVec && a.seqlen > 0) {
         const bool bf = sizeof(Tin) == 2;
-        cudaError_t e = make_bc_map(&mB, a.B, batch, a.seqlen, bf);
-        if (e == cudaSuccess) e = make_bc_map(&mC, a.C, batch, a.seqlen, bf);
+        cudaError_t e = make_bc_map(&mB, a.B, batch, a.seqlen, bf, G::kChunk);
+        if (e == cudaSuccess) e = make_bc_map(&mC, a.C, batch, a.seqlen, bf, G::kChunk);
         if (e != cudaSuccess) return e;
     }
     const unsigned gx = (unsigned)((a.dim + kRowsPerCta - 1) / kRowsPerCta);
     if (a.nseg > 1) {
         dim3 grid(gx, (unsigned)(a.nseg - 1), (unsigned)batch);
-        scan_kernel<Tin, Tout, kVec, kPrecise, Mode::kLocalEnd><<<grid, kThreads, 0, stream>>>(a, mB, mC);
+        scan_kernel<kR, Tin, Tout, kVec, kPrecise, Mode::kLocalEnd><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     dim3 grid(gx, (unsigned)a.nseg, (unsigned)batch);
-    scan_kernel<Tin, Tout, kVec, kPrecise, Mode::kFull><<<grid, kThreads, 0, stream>>>(a, mB, mC);
+    scan_kernel<kR, Tin, Tout, kVec, kPrecise, Mode::kFull><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
     return cudaGetLastError();
 }
 
+// Two rows per lane only for the fast bf16 vector path (the shapes where it pays off); every
+// other input combination runs one row per lane.
 template <typename Tin, typename Tout>
 cudaError_t launch_io(const ScanArgs& a, int64_t batch, bool vec, bool precise,
                       cudaStream_t stream) {
-    if (vec) {
-        return precise ? launch_typed<Tin, Tout, true, true>(a, batch, stream)
-                       : launch_typed<Tin, Tout, true, false>(a, batch, stream);
+    if constexpr (sizeof(Tin) == 2) {
+        if (vec && !precise && a.rows_per_lane == 2)
+            return launch_typed<2, Tin, Tout, true, false>(a, batch, stream);
     }
-    return precise ? launch_typed<Tin, Tout, false, true>(a, batch, stream)
-                   : launch_typed<Tin, Tout, false, false>(a, batch, stream);
+    if (vec) {
+        return precise ? launch_typed<1, Tin, Tout, true, true>(a, batch, stream)
+                       : launch_typed<1, Tin, Tout, true, false>(a, batch, stream);
+    }
+    return precise ? launch_typed<1, Tin, Tout, false, true>(a, batch, stream)
+                   : launch_typed<1, Tin, Tout, false, false>(a, batch, stream);
 }
 
 }  // namespace
@@ -655,9 +668,10 @@ cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-int scan_chunk_tokens() { return kChunk; }
+int scan_chunk_tokens() { return kMaxChunk; }
 int scan_rows_per_cta() { return kRowsPerCta; }
-int scan_rows_per_warp() { return kRowsPerWarp; }
-int scan_ctas_per_sm() { return kMinCtasPerSm; }
+int scan_ctas_per_sm(int rows_per_lane) {
+    return rows_per_lane == 2 ? Geo<2>::kMinCtas : Geo<1>::kMinCtas;
+}
 
 }  // namespace selscan

@@ -13,6 +13,7 @@ namespace {
 
 constexpr int64_t kStateN = 16;
 constexpr int64_t kMinSegTokens = 4096;  // shortest time segment worth a split
+constexpr int64_t kTwoRowsMinRows = 16384;  // rows from which two rows per lane pay off
 constexpr size_t kWsAlign = 256;
 
 size_t dtype_size(selscan_dtype t) { return t == SELSCAN_BF16 ? 2 : 4; }
@@ -60,7 +61,7 @@ Plan make_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
     const int64_t chunk = selscan::scan_chunk_tokens();
     const int64_t rows = batch * dim;
     const int64_t ctas = batch * ((dim + selscan::scan_rows_per_cta() - 1) / selscan::scan_rows_per_cta());
-    const int64_t slots = (int64_t)sms * selscan::scan_ctas_per_sm();
+    const int64_t slots = (int64_t)sms * selscan::scan_ctas_per_sm(2);
     int64_t n = 1;
     if (2 * ctas <= slots) {
         n = slots / ctas;
@@ -164,6 +165,10 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
     a.ws_dsum = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.hloc_bytes) : nullptr;
     a.dim = dim; a.seqlen = seqlen; a.seg_len = plan.seg_len; a.nseg = plan.nseg;
     a.softplus = delta_softplus ? 1 : 0;
+    // Two rows per lane halves the shared-memory traffic of B and C but also the warps: worth it
+    // once the rows alone give about two warps per scheduler, or when time segments supply
+    // the parallelism.
+    a.rows_per_lane = (plan.nseg > 1 || batch * dim >= kTwoRowsMinRows) ? 2 : 1;
     // 128-bit loads of 8 tokens and TMA tiles of B / C need seqlen % 8 == 0 (16-byte row
     // strides) and 32-bit token coordinates.
     const bool vec = (seqlen % 8) == 0 && seqlen < (int64_t(1) << 31) - 64;

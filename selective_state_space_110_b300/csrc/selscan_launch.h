@@ -26,15 +26,15 @@ struct ScanArgs {
     int64_t seg_len;  // tokens per time segment, a multiple of the chunk length
     int nseg;         // time segments (1 = no split)
     int softplus;
+    int rows_per_lane;  // 1 or 2 (2 only honoured on the bf16 vector path)
 };
 
 // Launches the local-end pass (nseg > 1) and the full pass on `stream`.
 cudaError_t launch_scan_fwd(const ScanArgs& a, int64_t batch, bool in_bf16, bool out_bf16,
                             bool vec, bool precise, cudaStream_t stream);
-int scan_chunk_tokens();
+int scan_chunk_tokens();  // time segments are multiples of this
 int scan_rows_per_cta();
-int scan_rows_per_warp();
-int scan_ctas_per_sm();  // CTAs per SM the scan kernels are built to fit
+int scan_ctas_per_sm(int rows_per_lane);  // CTAs per SM the scan kernels are built to fit
 
 // Copies the device error bits raised by kernels of this library (synchronises `stream`);
 // with `reset`, clears them afterwards.

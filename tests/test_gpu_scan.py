@@ -96,6 +96,27 @@ def test_initial_state(dt):
     assert_close(fin, rfin, tol, "final state")
 
 
+# Two rows per lane (taken from 16,384 rows on, bf16 with seqlen % 8 == 0), every element
+# checked: a ragged channel count leaves the last CTA partly inactive.
+TWO_ROWS = [
+    (8, 2048, 256, torch.float32, False),
+    (2, 8200, 96, torch.bfloat16, True),
+]
+
+
+@pytest.mark.parametrize("case", TWO_ROWS, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{str(c[3])[6:]}-h0{int(c[4])}")
+def test_two_rows_per_lane_full_check(case):
+    b, d, L, odt, with_h0 = case
+    assert b * d >= 16384 and workspace_size(b, d, 16, L) == 0
+    cfg = small_cfg(b, d, L, "bf16", 40 + d)
+    x = make_scan_inputs(cfg, DEV)
+    h0 = torch.randn(b, d, 16, device=DEV, generator=torch.Generator(DEV).manual_seed(6)) if with_h0 else None
+    out, fin = run_gpu(x, out_dtype=odt, initial_state=h0)
+    ref, rfin = run_oracle(x, initial_state=h0)
+    assert_close(out, ref, TOL[torch.bfloat16], "y")
+    assert_close(fin, rfin, TOL[torch.bfloat16], "final state")
+
+
 SEGMENTED = [
     # few rows, long sequences: the time split (local-end pass + folding) is taken
     (1, 64, 40960, "bf16", False),
