@@ -9,8 +9,9 @@ independent (batch, channel) rows). Definition, from "Mamba and State Space Mode
 (world.lapla.si): section "A State of Fixed Size" (h <- Abar*h + Bbar*x, then y = C*h),
 section "Chosen by the Token" (Delta, B, C per token, A fixed, Abar = exp(Delta*A)) and
 section "A Scan on the Chip" (discretise, then recur). Readings where the pages are silent:
-Delta = softplus(delta + delta_bias); Euler Bbar*x = Delta*B*u; y = C*h + D*u, then times
-silu(z); zero initial state unless one is given.
+Delta = softplus(delta + delta_bias); Euler Bbar*x = Delta*B*u (zero-order hold
+((exp(Delta*A) - 1)/A)*B*u as an option); y = C*h + D*u, then times silu(z); zero initial state
+unless one is given.
 
 Every function here is pinned by tests/test_oracle_pins.py (LTI convolution, solved form of
 the recurrence, Delta -> 0, large Delta, hand-worked N = 1 sequences, linearity in u).
@@ -48,12 +49,12 @@ class Oracle:
     def __init__(self, path: str):
         lib = ctypes.CDLL(path)
         lib.oracle_scan_fwd.restype = None
-        lib.oracle_scan_fwd.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP, _DP] + [_I64] * 4
+        lib.oracle_scan_fwd.argtypes = [_DP] * 8 + [ctypes.c_int, ctypes.c_int, _DP, _DP, _DP] + [_I64] * 4
         lib.oracle_scan_fwd_rows.restype = None
-        lib.oracle_scan_fwd_rows.argtypes = ([_DP] * 8 + [ctypes.c_int, _DP, _DP, _DP,
+        lib.oracle_scan_fwd_rows.argtypes = ([_DP] * 8 + [ctypes.c_int, ctypes.c_int, _DP, _DP, _DP,
                                              ctypes.POINTER(ctypes.c_int64)] + [_I64] * 4)
         lib.oracle_state_update.restype = None
-        lib.oracle_state_update.argtypes = [_DP] * 9 + [ctypes.c_int, _DP] + [_I64] * 3
+        lib.oracle_state_update.argtypes = [_DP] * 9 + [ctypes.c_int, ctypes.c_int, _DP] + [_I64] * 3
         lib.oracle_max_threads.restype = ctypes.c_int
         self._lib = lib
         self.path = path
@@ -62,8 +63,9 @@ class Oracle:
         return int(self._lib.oracle_max_threads())
 
     def scan_fwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-                 initial_state=None):
-        """Returns (out (batch, dim, seqlen), final_state (batch, dim, dstate)), float64."""
+                 initial_state=None, zoh=False):
+        """Returns (out (batch, dim, seqlen), final_state (batch, dim, dstate)), float64.
+        zoh: zero-order-hold discretisation of B instead of Euler."""
         u, delta, A, B, C = map(_f64, (u, delta, A, B, C))
         D, z, delta_bias, initial_state = map(_f64, (D, z, delta_bias, initial_state))
         batch, dim, seqlen = u.shape
@@ -77,12 +79,13 @@ class Oracle:
         out = np.empty((batch, dim, seqlen), dtype=np.float64)
         fin = np.empty((batch, dim, dstate), dtype=np.float64)
         self._lib.oracle_scan_fwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z),
-                                  _p(delta_bias), int(bool(delta_softplus)), _p(initial_state),
+                                  _p(delta_bias), int(bool(delta_softplus)), int(bool(zoh)),
+                                  _p(initial_state),
                                   _p(out), _p(fin), batch, dim, dstate, seqlen)
         return out, fin
 
     def scan_fwd_rows(self, rows, u_rows, delta_rows, A, B, C, D=None, z_rows=None,
-                      delta_bias=None, delta_softplus=True, initial_state_rows=None):
+                      delta_bias=None, delta_softplus=True, initial_state_rows=None, zoh=False):
         """Scan of selected rows (flat indices b*dim + d) only.
 
         u_rows, delta_rows, z_rows: (nrows, seqlen) slices of the full tensors for those rows;
@@ -101,11 +104,12 @@ class Oracle:
         fin = np.empty((nrows, dstate), dtype=np.float64)
         self._lib.oracle_scan_fwd_rows(
             _p(u_rows), _p(delta_rows), _p(A), _p(B), _p(C), _p(D), _p(z_rows), _p(delta_bias),
-            int(bool(delta_softplus)), _p(initial_state_rows), _p(out), _p(fin),
+            int(bool(delta_softplus)), int(bool(zoh)), _p(initial_state_rows), _p(out), _p(fin),
             rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), nrows, dim, dstate, seqlen)
         return out, fin
 
-    def state_update(self, state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True):
+    def state_update(self, state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True,
+                     zoh=False):
         """One token. Returns (new_state (batch, dim, dstate), out (batch, dim)); inputs untouched."""
         st = _f64(state).copy()
         x, dt, A, B, C = map(_f64, (x, dt, A, B, C))
@@ -115,7 +119,8 @@ class Oracle:
         assert B.shape == (batch, dstate) and C.shape == B.shape
         out = np.empty((batch, dim), dtype=np.float64)
         self._lib.oracle_state_update(_p(st), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(z),
-                                      _p(dt_bias), int(bool(dt_softplus)), _p(out), batch, dim,
+                                      _p(dt_bias), int(bool(dt_softplus)), int(bool(zoh)), _p(out),
+                                      batch, dim,
                                       dstate)
         return st, out
 

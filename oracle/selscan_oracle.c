@@ -16,7 +16,8 @@
  *     run through the recurrence (the discretisation rule of B is not stated there).
  *   - The remaining choices are the plain reading used throughout this project:
  *     Delta = softplus(delta + delta_bias) (or delta + delta_bias with the flag off),
- *     Euler discretisation of B (Bbar*x = Delta*B*u), a skip term D*u added to C*h,
+ *     Euler discretisation of B (Bbar*x = Delta*B*u; zero-order hold as an option, which
+ *     makes the one-number gate of "Chosen by the Token" exact), a skip term D*u added to C*h,
  *     and the result gated by silu(z) = z*sigmoid(z). The initial state is zero unless
  *     one is given.
  * Everything is evaluated in double precision, strictly sequentially in t, with the
@@ -45,6 +46,14 @@ static double softplus(double x) { return fmax(x, 0.0) + log1p(exp(-fabs(x))); }
 /* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* Factor f with Bbar*x = f * B * x for one state with decay rate a. Euler (the default):
+ * f = Delta. Zero-order hold of the continuous system h' = a h + B x over a step of length
+ * Delta (option, zoh != 0): f = (exp(Delta*a) - 1) / a, which tends to Delta as a -> 0. */
+static double bbar_factor(double dlt, double a, int zoh) {
+    if (!zoh || a == 0.0) return dlt;
+    return expm1(dlt * a) / a;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -56,13 +65,13 @@ int oracle_max_threads(void) {
 /* One row (b, d) of the scan: the recurrence over t = 0 .. seqlen-1. */
 static void scan_row(const double* u, const double* delta, const double* A_d, const double* Bb,
                      const double* Cb, double D_d, const double* z, double bias, int softplus_on,
-                     int64_t dstate, int64_t seqlen, double* h, double* out) {
+                     int zoh, int64_t dstate, int64_t seqlen, double* h, double* out) {
     for (int64_t t = 0; t < seqlen; ++t) {
         double x = delta[t] + bias;
         double dlt = softplus_on ? softplus(x) : x;
         for (int64_t n = 0; n < dstate; ++n) {
             double abar = exp(dlt * A_d[n]);
-            double bbar_x = dlt * Bb[n * seqlen + t] * u[t];
+            double bbar_x = bbar_factor(dlt, A_d[n], zoh) * Bb[n * seqlen + t] * u[t];
             h[n] = abar * h[n] + bbar_x;
         }
         double y = 0.0;
@@ -77,7 +86,7 @@ static void scan_row(const double* u, const double* delta, const double* A_d, co
  * be NULL: D and delta_bias then count as zero, z as no gate, initial_state as zeros. */
 void oracle_scan_fwd(const double* u, const double* delta, const double* A, const double* B,
                      const double* C, const double* D, const double* z, const double* delta_bias,
-                     int delta_softplus, const double* initial_state, double* out,
+                     int delta_softplus, int zoh, const double* initial_state, double* out,
                      double* final_state, int64_t batch, int64_t dim, int64_t dstate,
                      int64_t seqlen) {
     int64_t rows = batch * dim;
@@ -90,7 +99,8 @@ void oracle_scan_fwd(const double* u, const double* delta, const double* A, cons
         const int64_t off = r * seqlen;
         scan_row(u + off, delta + off, A + d * dstate, B + b * dstate * seqlen,
                  C + b * dstate * seqlen, D ? D[d] : 0.0, z ? z + off : NULL,
-                 delta_bias ? delta_bias[d] : 0.0, delta_softplus, dstate, seqlen, h, out + off);
+                 delta_bias ? delta_bias[d] : 0.0, delta_softplus, zoh, dstate, seqlen, h,
+                 out + off);
         if (final_state)
             for (int64_t n = 0; n < dstate; ++n) final_state[r * dstate + n] = h[n];
         free(h);
@@ -101,7 +111,7 @@ void oracle_scan_fwd(const double* u, const double* delta, const double* A, cons
  * out (nrows, seqlen), final_state (nrows, dstate). Inputs keep their full layouts. */
 void oracle_scan_fwd_rows(const double* u_rows, const double* delta_rows, const double* A,
                           const double* B, const double* C, const double* D, const double* z_rows,
-                          const double* delta_bias, int delta_softplus,
+                          const double* delta_bias, int delta_softplus, int zoh,
                           const double* initial_state_rows, double* out_rows,
                           double* final_state_rows, const int64_t* rows, int64_t nrows,
                           int64_t dim, int64_t dstate, int64_t seqlen) {
@@ -114,7 +124,7 @@ void oracle_scan_fwd_rows(const double* u_rows, const double* delta_rows, const 
         const int64_t off = i * seqlen;
         scan_row(u_rows + off, delta_rows + off, A + d * dstate, B + b * dstate * seqlen,
                  C + b * dstate * seqlen, D ? D[d] : 0.0, z_rows ? z_rows + off : NULL,
-                 delta_bias ? delta_bias[d] : 0.0, delta_softplus, dstate, seqlen, h,
+                 delta_bias ? delta_bias[d] : 0.0, delta_softplus, zoh, dstate, seqlen, h,
                  out_rows + off);
         if (final_state_rows)
             for (int64_t n = 0; n < dstate; ++n) final_state_rows[i * dstate + n] = h[n];
@@ -127,8 +137,8 @@ void oracle_scan_fwd_rows(const double* u_rows, const double* delta_rows, const 
  * written back to `state`. */
 void oracle_state_update(double* state, const double* x, const double* dt, const double* A,
                          const double* B, const double* C, const double* D, const double* z,
-                         const double* dt_bias, int dt_softplus, double* out, int64_t batch,
-                         int64_t dim, int64_t dstate) {
+                         const double* dt_bias, int dt_softplus, int zoh, double* out,
+                         int64_t batch, int64_t dim, int64_t dstate) {
     int64_t rows = batch * dim;
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
@@ -138,7 +148,8 @@ void oracle_state_update(double* state, const double* x, const double* dt, const
         double dlt = dt_softplus ? softplus(xx) : xx;
         for (int64_t n = 0; n < dstate; ++n) {
             double abar = exp(dlt * A[d * dstate + n]);
-            h[n] = abar * h[n] + dlt * B[b * dstate + n] * x[r];
+            double f = bbar_factor(dlt, A[d * dstate + n], zoh);
+            h[n] = abar * h[n] + f * B[b * dstate + n] * x[r];
         }
         double y = 0.0;
         for (int64_t n = 0; n < dstate; ++n) y += C[b * dstate + n] * h[n];

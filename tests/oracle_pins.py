@@ -56,7 +56,13 @@ def _random_problem(seed, batch=2, dim=3, dstate=5, seqlen=40, lti=False):
     return dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=bias, h0=h0)
 
 
-def pin_lti_convolution(orc, seed=11, with_state=True):
+def _bbar_ref(dlt, An, zoh):
+    """Factor of B*u per state: Delta (Euler) or (exp(Delta*A) - 1)/A (zero-order hold),
+    written with numpy's expm1 independently of the oracle."""
+    return np.expm1(dlt * An) / An if zoh else dlt * np.ones_like(An)
+
+
+def pin_lti_convolution(orc, seed=11, with_state=True, zoh=False):
     """'Every Step the Same' (world.lapla.si): with the same Delta, A, B, C at every token the
     output is the input convolved with one fixed kernel K_k = sum_n C[n] Abar[n]^k Bbar[n],
     computed here in closed form with exp(k*Delta*A) and an O(L^2) sum."""
@@ -65,7 +71,7 @@ def pin_lti_convolution(orc, seed=11, with_state=True):
     N = p["A"].shape[1]
     h0 = p["h0"] if with_state else None
     out, fin = orc.scan_fwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
-                            p["delta_bias"], True, h0)
+                            p["delta_bias"], True, h0, zoh=zoh)
     ref = np.zeros_like(out)
     ref_fin = np.zeros_like(fin)
     k = np.arange(L)
@@ -74,21 +80,22 @@ def pin_lti_convolution(orc, seed=11, with_state=True):
             dlt = softplus_ref(p["delta"][b, d, 0] + p["delta_bias"][d])
             Bn, Cn, An = p["B"][b, :, 0], p["C"][b, :, 0], p["A"][d]
             decay = np.exp(np.outer(k, dlt * An))  # (L, N): Abar^k
-            K = decay @ (Cn * dlt * Bn)  # kernel K_k
+            bb = _bbar_ref(dlt, An, zoh) * Bn  # Bbar
+            K = decay @ (Cn * bb)  # kernel K_k
             u = p["u"][b, d]
             y = np.array([np.dot(K[: t + 1], u[t::-1]) for t in range(L)])
             if h0 is not None:
                 y = y + np.exp(np.outer(k + 1, dlt * An)) @ (Cn * h0[b, d])
             y = (y + p["D"][d] * u) * silu_ref(p["z"][b, d])
             ref[b, d] = y
-            hf = (decay[::-1] * (dlt * Bn)[None, :] * u[:, None]).sum(axis=0)
+            hf = (decay[::-1] * bb[None, :] * u[:, None]).sum(axis=0)
             if h0 is not None:
                 hf = hf + np.exp(L * dlt * An) * h0[b, d]
             ref_fin[b, d] = hf
     return max(relerr(out, ref), relerr(fin, ref_fin))
 
 
-def pin_solved_form(orc, seed=12, softplus=True, with_state=True):
+def pin_solved_form(orc, seed=12, softplus=True, with_state=True, zoh=False):
     """The recurrence h_t = exp(Delta_t*A) h_{t-1} + Delta_t*B_t*u_t has the solution
     h_t = exp(A*S_t) h_init + sum_{s<=t} exp(A*(S_t - S_s)) Delta_s B_s u_s with
     S_t = Delta_0 + ... + Delta_t. This evaluates that sum directly (no recursion) for
@@ -97,7 +104,7 @@ def pin_solved_form(orc, seed=12, softplus=True, with_state=True):
     batch, dim, L = p["u"].shape
     h0 = p["h0"] if with_state else None
     out, fin = orc.scan_fwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
-                            p["delta_bias"], softplus, h0)
+                            p["delta_bias"], softplus, h0, zoh=zoh)
     ref = np.zeros_like(out)
     ref_fin = np.zeros_like(fin)
     for b in range(batch):
@@ -106,7 +113,8 @@ def pin_solved_form(orc, seed=12, softplus=True, with_state=True):
             dlt = softplus_ref(x) if softplus else x
             S = np.cumsum(dlt)
             An = p["A"][d]
-            src = dlt[:, None] * p["B"][b].T * p["u"][b, d][:, None]  # (L, N)
+            fac = np.stack([_bbar_ref(dl, An, zoh) for dl in dlt])  # (L, N)
+            src = fac * p["B"][b].T * p["u"][b, d][:, None]  # (L, N)
             for t in range(L):
                 w = np.exp(An[None, :] * (S[t] - S[: t + 1])[:, None])  # (t+1, N)
                 h = (w * src[: t + 1]).sum(axis=0)
@@ -205,7 +213,7 @@ def pin_hand_worked_update(orc):
     return worst
 
 
-def pin_update_is_one_scan_step(orc, seed=16):
+def pin_update_is_one_scan_step(orc, seed=16, zoh=False):
     """The generation step is the scan's update applied once ('Taken Apart': one token read,
     the state moves once): state_update == a length-1 scan from that state, and L updates in a
     row == the length-L scan. The scan side is pinned by the pins above."""
@@ -216,10 +224,46 @@ def pin_update_is_one_scan_step(orc, seed=16):
     for t in range(L):
         st, ys[:, :, t] = orc.state_update(st, p["u"][:, :, t], p["delta"][:, :, t], p["A"],
                                            p["B"][:, :, t], p["C"][:, :, t], p["D"],
-                                           p["z"][:, :, t], p["delta_bias"], True)
+                                           p["z"][:, :, t], p["delta_bias"], True, zoh=zoh)
     out, fin = orc.scan_fwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
-                            p["delta_bias"], True, p["h0"])
+                            p["delta_bias"], True, p["h0"], zoh=zoh)
     return max(relerr(ys, out), relerr(st, fin))
+
+
+def gate_reference(x, u, h0):
+    """The recurrent gate of 'Chosen by the Token' (the paper's Theorem 1):
+    h_t = (1 - g_t) h_{t-1} + g_t u_t with g_t = sigmoid(x_t), evaluated with the logistic
+    function. x, u: (..., L); h0: (...). Returns the sequence h (..., L)."""
+    g = 1.0 / (1.0 + np.exp(-x))
+    h = np.array(h0, dtype=np.float64)
+    out = np.empty_like(u)
+    for t in range(u.shape[-1]):
+        h = (1.0 - g[..., t]) * h + g[..., t] * u[..., t]
+        out[..., t] = h
+    return out
+
+
+def pin_theorem1_gate(orc, seed=17):
+    """'Chosen by the Token': with a state of a single number the selective update is exactly
+    a recurrent network's gate h <- (1 - g) h + g x. That holds for the zero-order hold with
+    A = -1, B = C = 1, D = 0 and Delta = softplus(x): then Abar = exp(-Delta) = 1 - sigmoid(x)
+    and Bbar = 1 - exp(-Delta) = sigmoid(x). Checked for the scan and for L state updates."""
+    r = _rng(seed)
+    batch, dim, L = 2, 3, 60
+    delta = r.normal(0.0, 1.5, size=(batch, dim, L))
+    bias = r.uniform(-3.0, 2.0, size=dim)
+    u = r.standard_normal((batch, dim, L))
+    h0 = r.standard_normal((batch, dim, 1))
+    A = -np.ones((dim, 1))
+    ones = np.ones((batch, 1, L))
+    out, fin = orc.scan_fwd(u, delta, A, ones, ones, np.zeros(dim), None, bias, True, h0, zoh=True)
+    ref = gate_reference(delta + bias[None, :, None], u, h0[..., 0])
+    st = h0.copy()
+    ys = np.empty_like(u)
+    for t in range(L):
+        st, ys[:, :, t] = orc.state_update(st, u[:, :, t], delta[:, :, t], A, ones[:, :, t],
+                                           ones[:, :, t], None, None, bias, True, zoh=True)
+    return max(relerr(out, ref), relerr(fin[..., 0], ref[..., -1]), relerr(ys, ref))
 
 
 # (pin function, bound) pairs used by the pin tests and the mutation tests.
@@ -234,4 +278,8 @@ ALL_PINS = [
     (pin_hand_worked_scan, 1e-14),
     (pin_hand_worked_update, 1e-14),
     (pin_update_is_one_scan_step, 1e-12),
+    (pin_theorem1_gate, 1e-12),
+    (lambda o: pin_lti_convolution(o, seed=23, zoh=True), 1e-11),
+    (lambda o: pin_solved_form(o, seed=24, zoh=True), 1e-11),
+    (lambda o: pin_update_is_one_scan_step(o, seed=25, zoh=True), 1e-12),
 ]

@@ -21,17 +21,18 @@ _ROW_UPDATE = """            h[n] = abar * h[n] + bbar_x;
 MUTANTS = {
     "drop_D_skip": ("y += D_d * u[t];", ""),
     "exp_sign": ("double abar = exp(dlt * A_d[n]);", "double abar = exp(-dlt * A_d[n]);"),
-    "zoh_instead_of_euler": ("double bbar_x = dlt * Bb[n * seqlen + t] * u[t];",
-                             "double bbar_x = (exp(dlt * A_d[n]) - 1.0) / A_d[n] * Bb[n * seqlen + t] * u[t];"),
-    "missing_delta_in_B": ("double bbar_x = dlt * Bb[n * seqlen + t] * u[t];",
+    "zoh_instead_of_euler": ("if (!zoh || a == 0.0) return dlt;", "if (a == 0.0) return dlt;"),
+    "euler_instead_of_zoh": ("return expm1(dlt * a) / a;", "return dlt;"),
+    "zoh_without_divide": ("return expm1(dlt * a) / a;", "return expm1(dlt * a);"),
+    "missing_delta_in_B": ("double bbar_x = bbar_factor(dlt, A_d[n], zoh) * Bb[n * seqlen + t] * u[t];",
                            "double bbar_x = Bb[n * seqlen + t] * u[t];"),
-    "B_transposed": ("double bbar_x = dlt * Bb[n * seqlen + t] * u[t];",
-                     "double bbar_x = dlt * Bb[t * dstate + n] * u[t];"),
+    "B_transposed": ("double bbar_x = bbar_factor(dlt, A_d[n], zoh) * Bb[n * seqlen + t] * u[t];",
+                     "double bbar_x = bbar_factor(dlt, A_d[n], zoh) * Bb[t * dstate + n] * u[t];"),
     "C_is_B": ("y += Cb[n * seqlen + t] * h[n];", "y += Bb[n * seqlen + t] * h[n];"),
     "read_before_update": (_ROW_UPDATE, """            h[n] = abar * h[n] + bbar_x;
         }
         double y = 0.0;
-        for (int64_t n = 0; n < dstate; ++n) y += Cb[n * seqlen + t] * (h[n] - dlt * Bb[n * seqlen + t] * u[t]) / exp(dlt * A_d[n]);"""),
+        for (int64_t n = 0; n < dstate; ++n) y += Cb[n * seqlen + t] * (h[n] - bbar_factor(dlt, A_d[n], zoh) * Bb[n * seqlen + t] * u[t]) / exp(dlt * A_d[n]);"""),
     "bias_after_softplus": ("double x = delta[t] + bias;\n        double dlt = softplus_on ? softplus(x) : x;",
                             "double x = delta[t];\n        double dlt = (softplus_on ? softplus(x) : x) + bias;"),
     "softplus_dropped_log1p": ("return fmax(x, 0.0) + log1p(exp(-fabs(x)));", "return fmax(x, 0.0);"),
@@ -39,10 +40,12 @@ MUTANTS = {
     "initial_state_ignored": ("h[n] = initial_state ? initial_state[r * dstate + n] : 0.0;", "h[n] = 0.0;"),
     "A_wrong_stride": ("A + d * dstate, B + b * dstate * seqlen,\n                 C + b * dstate * seqlen, D ? D[d] : 0.0, z ? z + off : NULL,",
                        "A + d, B + b * dstate * seqlen,\n                 C + b * dstate * seqlen, D ? D[d] : 0.0, z ? z + off : NULL,"),
+    "update_zoh_ignored": ("double f = bbar_factor(dlt, A[d * dstate + n], zoh);",
+                           "double f = dlt;"),
     "readout_skips_last_state": ("for (int64_t n = 0; n < dstate; ++n) y += Cb[n * seqlen + t] * h[n];",
                                  "for (int64_t n = 0; n + 1 < dstate; ++n) y += Cb[n * seqlen + t] * h[n];"),
-    "update_drops_batch_of_B": ("h[n] = abar * h[n] + dlt * B[b * dstate + n] * x[r];",
-                                "h[n] = abar * h[n] + dlt * B[n] * x[r];"),
+    "update_drops_batch_of_B": ("h[n] = abar * h[n] + f * B[b * dstate + n] * x[r];",
+                                "h[n] = abar * h[n] + f * B[n] * x[r];"),
     "update_bias_ignored": ("double xx = dt[r] + (dt_bias ? dt_bias[d] : 0.0);", "double xx = dt[r];"),
     "update_gate_dropped": ("if (z) y *= silu(z[r]);", ""),
 }
