@@ -49,6 +49,13 @@ typedef enum {
     SELSCAN_BF16 = 1  /* bfloat16 */
 } selscan_dtype;
 
+/* Bits of the `delta_softplus` / `dt_softplus` argument. Other bits are rejected. */
+enum {
+    SELSCAN_FLAG_SOFTPLUS = 1, /* Delta = softplus(delta + bias); else Delta = delta + bias */
+    SELSCAN_FLAG_ZOH = 2       /* zero-order hold: Bbar = ((exp(Delta*A) - 1)/A) * B instead of
+                                  the Euler Bbar = Delta*B (the limit Delta*B where A = 0) */
+};
+
 typedef enum {
     SELSCAN_OK = 0,
     SELSCAN_ERR_INVALID_ARG = 1,  /* NULL required pointer, bad size, overlapping output */
@@ -73,7 +80,11 @@ typedef enum {
  *   final_state           (batch, dim, dstate)       fp32, the state after token seqlen-1
  * Optional pointers: D (NULL = no skip term), z (NULL = no gate), delta_bias (NULL = 0),
  * initial_state, final_state (NULL = not written).
- * delta_softplus: nonzero applies softplus to delta + delta_bias, zero uses it as is.
+ * delta_softplus: flag bits. SELSCAN_FLAG_SOFTPLUS applies softplus to delta + delta_bias
+ * (without it Delta = delta + delta_bias as is); SELSCAN_FLAG_ZOH selects the zero-order-hold
+ * discretisation of B. With the zero-order hold and a single state number (A = -1, B = C = 1)
+ * the update is the recurrent gate h <- (1 - g) h + g x, g = sigmoid(delta + delta_bias),
+ * that "Chosen by the Token" describes. Unknown bits: SELSCAN_ERR_INVALID_ARG.
  * dstate must be 16. batch, dim >= 1; seqlen >= 0 (seqlen = 0 writes final_state only).
  * in_dtype applies to u, delta, z, B and C; out_dtype to out. Arithmetic is fp32.
  *
@@ -107,7 +118,7 @@ size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64
  *   B, C                  (batch, dstate)       dtype in_dtype
  *   A                     (dim, dstate)         fp32
  *   D, dt_bias            (dim)                 fp32, NULL = 0
- * z NULL = no gate. dt_softplus as delta_softplus above. dstate must be 16.
+ * z NULL = no gate. dt_softplus: the flag bits of delta_softplus above. dstate must be 16.
  * out must not overlap state or any input.
  */
 selscan_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,

@@ -13,6 +13,7 @@ import os
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libselscan.so")
 
 F32, BF16 = 0, 1
+FLAG_SOFTPLUS, FLAG_ZOH = 1, 2  # bits of the softplus argument (SELSCAN_FLAG_*)
 
 STATUS = {
     0: "SELSCAN_OK",

@@ -172,6 +172,19 @@ __device__ __forceinline__ void unpack(const Raw8<float>& r, float (&v)[8]) {
     v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
 }
 
+// ---- zero-order hold: Bbar = Delta*B * phi(x), phi(x) = (exp(x) - 1)/x, x = Delta*A ----
+__device__ __forceinline__ float inv_or_zero(float v) { return v != 0.f ? 1.f / v : 0.f; }
+// fp32 inputs: m = expm1(x) from the library; phi(0) = 1.
+__device__ __forceinline__ float phi_exact(float m, float x) { return x != 0.f ? m / x : 1.f; }
+// bf16 inputs: x2 = x*log2(e) (the SFU argument), abar = 2^x2, inv_a = 1/A, dinv = 1/Delta.
+// For |x| < 1/16 the Taylor series 1 + x/2 + x^2/6 + x^3/24 (truncation below 1e-7
+// relative); above, (abar - 1)/(A*Delta), where abar - 1 has lost no significant digits.
+__device__ __forceinline__ float phi_fast(float x2, float abar, float inv_a, float dinv) {
+    const float x = x2 * 0.69314718055994531f;
+    const float p = fmaf(fmaf(fmaf(x, 1.f / 24.f, 1.f / 6.f), x, 0.5f), x, 1.f);
+    return fabsf(x) < 0.0625f ? p : (abar - 1.f) * inv_a * dinv;
+}
+
 // Owner lane (within the quad) of row j, token t of a chunk, and its register slot t & 7.
 template <int kR>
 __device__ __forceinline__ constexpr int owner_of(int j, int t) {
@@ -184,7 +197,7 @@ __device__ __forceinline__ constexpr int red_swz(int j, int q) {
     return kR == 1 ? ((q >> 1) & 3) : ((2 * j + (q >> 1)) & 3);
 }
 
-template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, Mode kMode>
+template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, bool kZoh, Mode kMode>
 __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
     scan_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC) {
@@ -246,11 +259,13 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
 
     // Per-row constants: A for states 4g..4g+3, pre-scaled by log2(e) for the SFU exp2, as
     // (A_n, A_n) pairs so that one packed multiply forms the arguments of two tokens.
-    float4 A4[kR];
+    float4 A4[kR], invA[kR];  // invA: 1/A (natural units), zero-order hold only
     float2 aa[kR][4];
 #pragma unroll
     for (int j = 0; j < kR; ++j) {
         A4[j] = *reinterpret_cast<const float4*>(a.A + (row[j] - b * dim) * kN + 4 * g);
+        if (kZoh) invA[j] = make_float4(inv_or_zero(A4[j].x), inv_or_zero(A4[j].y),
+                                        inv_or_zero(A4[j].z), inv_or_zero(A4[j].w));
         if (!kPrecise) {
             A4[j].x *= kLog2e; A4[j].y *= kLog2e; A4[j].z *= kLog2e; A4[j].w *= kLog2e;
         }
@@ -430,18 +445,18 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
         for (int q = 0; q < kBlocks; ++q) {
             // exp2 arguments of tokens (4q, 4q+1) and (4q+2, 4q+3), per row and state
             float2 ea[kR][4], eb[kR][4];
+            float dq[kR][4];
 #pragma unroll
             for (int j = 0; j < kR; ++j) {
-                float dq[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int t = 4 * q + e;
-                    dq[e] = __shfl_sync(0xffffffffu, dl[t & 7], owner_of<kR>(j, t), 4);
+                    dq[j][e] = __shfl_sync(0xffffffffu, dl[t & 7], owner_of<kR>(j, t), 4);
                 }
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {
-                    ea[j][n] = __fmul2_rn(make_float2(dq[0], dq[1]), aa[j][n]);
-                    eb[j][n] = __fmul2_rn(make_float2(dq[2], dq[3]), aa[j][n]);
+                    ea[j][n] = __fmul2_rn(make_float2(dq[j][0], dq[j][1]), aa[j][n]);
+                    eb[j][n] = __fmul2_rn(make_float2(dq[j][2], dq[j][3]), aa[j][n]);
                 }
             }
             float yq[kR][4];
@@ -460,19 +475,30 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
 #pragma unroll
                     for (int n = 0; n < 4; ++n)
                         arg[n] = e == 0 ? ea[j][n].x : e == 1 ? ea[j][n].y : e == 2 ? eb[j][n].x : eb[j][n].y;
-                    const float2 kb01 = __fmul2_rn(kk, make_float2(Bv.x, Bv.y));
-                    const float2 kb23 = __fmul2_rn(kk, make_float2(Bv.z, Bv.w));
+                    float2 kb01 = __fmul2_rn(kk, make_float2(Bv.x, Bv.y));
+                    float2 kb23 = __fmul2_rn(kk, make_float2(Bv.z, Bv.w));
                     if (kPrecise) {
                         // Abar = 1 + expm1(Delta*A): the decay's distance from 1 keeps full
                         // relative precision, so a slowly decaying state accumulates no bias
                         // from rounding Abar itself.
                         const float2 m01 = make_float2(expm1f(arg[0]), expm1f(arg[1]));
                         const float2 m23 = make_float2(expm1f(arg[2]), expm1f(arg[3]));
+                        if (kZoh) {  // Bbar = Delta*B * (exp(x)-1)/x with x = Delta*A
+                            kb01 = __fmul2_rn(kb01, make_float2(phi_exact(m01.x, arg[0]), phi_exact(m01.y, arg[1])));
+                            kb23 = __fmul2_rn(kb23, make_float2(phi_exact(m23.x, arg[2]), phi_exact(m23.y, arg[3])));
+                        }
                         h01[j] = __fadd2_rn(__ffma2_rn(m01, h01[j], h01[j]), kb01);
                         h23[j] = __fadd2_rn(__ffma2_rn(m23, h23[j], h23[j]), kb23);
                     } else {
                         const float2 ab01 = make_float2(ex2_approx(arg[0]), ex2_approx(arg[1]));
                         const float2 ab23 = make_float2(ex2_approx(arg[2]), ex2_approx(arg[3]));
+                        if (kZoh) {  // Bbar = Delta*B * (exp(x)-1)/x with x = Delta*A
+                            const float dinv = rcp_approx(dq[j][e]);
+                            kb01 = __fmul2_rn(kb01, make_float2(phi_fast(arg[0], ab01.x, invA[j].x, dinv),
+                                                                phi_fast(arg[1], ab01.y, invA[j].y, dinv)));
+                            kb23 = __fmul2_rn(kb23, make_float2(phi_fast(arg[2], ab23.x, invA[j].z, dinv),
+                                                                phi_fast(arg[3], ab23.y, invA[j].w, dinv)));
+                        }
                         h01[j] = __ffma2_rn(ab01, h01[j], kb01);
                         h23[j] = __ffma2_rn(ab23, h23[j], kb23);
                     }
@@ -584,7 +610,7 @@ cudaError_t make_bc_map(CUtensorMap* m, const void* base, int64_t batch, int64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise>
+template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, bool kZoh = false>
 cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) {
     using G = Geo<kR>;
     CUtensorMap mB{}, mC{};
@@ -597,12 +623,12 @@ cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) 
     const unsigned gx = (unsigned)((a.dim + kRowsPerCta - 1) / kRowsPerCta);
     if (a.nseg > 1) {
         dim3 grid(gx, (unsigned)(a.nseg - 1), (unsigned)batch);
-        scan_kernel<kR, Tin, Tout, kVec, kPrecise, Mode::kLocalEnd><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
+        scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kLocalEnd><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     dim3 grid(gx, (unsigned)a.nseg, (unsigned)batch);
-    scan_kernel<kR, Tin, Tout, kVec, kPrecise, Mode::kFull><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
+    scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kFull><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
     return cudaGetLastError();
 }
 
@@ -611,6 +637,14 @@ cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) 
 template <typename Tin, typename Tout>
 cudaError_t launch_io(const ScanArgs& a, int64_t batch, bool vec, bool precise,
                       cudaStream_t stream) {
+    if (a.zoh) {  // zero-order hold: one row per lane, every load path
+        if (vec) {
+            return precise ? launch_typed<1, Tin, Tout, true, true, true>(a, batch, stream)
+                           : launch_typed<1, Tin, Tout, true, false, true>(a, batch, stream);
+        }
+        return precise ? launch_typed<1, Tin, Tout, false, true, true>(a, batch, stream)
+                       : launch_typed<1, Tin, Tout, false, false, true>(a, batch, stream);
+    }
     if constexpr (sizeof(Tin) == 2) {
         if (vec && !precise && a.rows_per_lane == 2)
             return launch_typed<2, Tin, Tout, true, false>(a, batch, stream);

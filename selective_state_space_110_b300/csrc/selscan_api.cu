@@ -14,6 +14,7 @@ namespace {
 constexpr int64_t kStateN = 16;
 constexpr int64_t kMinSegTokens = 4096;  // shortest time segment worth a split
 constexpr int64_t kTwoRowsMinRows = 16384;  // rows from which two rows per lane pay off
+constexpr int kKnownFlags = SELSCAN_FLAG_SOFTPLUS | SELSCAN_FLAG_ZOH;
 constexpr size_t kWsAlign = 256;
 
 size_t dtype_size(selscan_dtype t) { return t == SELSCAN_BF16 ? 2 : 4; }
@@ -121,7 +122,7 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
     // ---- checks that need no device ----
     if (dstate != kStateN || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
         return SELSCAN_ERR_UNSUPPORTED;
-    if (!shape_ok(batch, dim, seqlen)) return SELSCAN_ERR_INVALID_ARG;
+    if (!shape_ok(batch, dim, seqlen) || (delta_softplus & ~kKnownFlags)) return SELSCAN_ERR_INVALID_ARG;
     const bool has_tokens = seqlen > 0;
     if (!A || (has_tokens && (!u || !delta || !B || !C || !out))) return SELSCAN_ERR_INVALID_ARG;
     const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, out, final_state, initial_state, workspace};
@@ -164,7 +165,8 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
     a.ws_hloc = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
     a.ws_dsum = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.hloc_bytes) : nullptr;
     a.dim = dim; a.seqlen = seqlen; a.seg_len = plan.seg_len; a.nseg = plan.nseg;
-    a.softplus = delta_softplus ? 1 : 0;
+    a.softplus = (delta_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
+    a.zoh = (delta_softplus & SELSCAN_FLAG_ZOH) ? 1 : 0;
     // Two rows per lane halves the shared-memory traffic of B and C but also the warps: worth it
     // once the rows alone give about two warps per scheduler, or when time segments supply
     // the parallelism.
@@ -188,7 +190,7 @@ SELSCAN_EXPORT selscan_status ssm_state_update(float* state, const void* x, cons
                                                selscan_stream_t stream) {
     if (dstate != kStateN || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
         return SELSCAN_ERR_UNSUPPORTED;
-    if (!shape_ok(batch, dim, 0)) return SELSCAN_ERR_INVALID_ARG;
+    if (!shape_ok(batch, dim, 0) || (dt_softplus & ~kKnownFlags)) return SELSCAN_ERR_INVALID_ARG;
     if (!state || !x || !dt || !A || !B || !C || !out) return SELSCAN_ERR_INVALID_ARG;
     const void* ptrs[] = {state, x, dt, A, B, C, D, z, out, dt_bias};
     for (const void* p : ptrs)
@@ -213,7 +215,8 @@ SELSCAN_EXPORT selscan_status ssm_state_update(float* state, const void* x, cons
     selscan::UpdateArgs a{};
     a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.out = out; a.dt_bias = dt_bias; a.dim = dim; a.rows = (int64_t)rows;
-    a.softplus = dt_softplus ? 1 : 0;
+    a.softplus = (dt_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
+    a.zoh = (dt_softplus & SELSCAN_FLAG_ZOH) ? 1 : 0;
     cudaError_t e = selscan::launch_state_update(a, in_dtype == SELSCAN_BF16,
                                                  out_dtype == SELSCAN_BF16,
                                                  reinterpret_cast<cudaStream_t>(stream));

@@ -27,6 +27,7 @@ struct ScanArgs {
     int nseg;         // time segments (1 = no split)
     int softplus;
     int rows_per_lane;  // 1 or 2 (2 only honoured on the bf16 vector path)
+    int zoh;            // zero-order-hold discretisation of B instead of Euler
 };
 
 // Launches the local-end pass (nseg > 1) and the full pass on `stream`.
@@ -57,6 +58,7 @@ struct UpdateArgs {
     int64_t dim;
     int64_t rows;  // batch*dim
     int softplus;
+    int zoh;
 };
 
 cudaError_t launch_state_update(const UpdateArgs& a, bool in_bf16, bool out_bf16,

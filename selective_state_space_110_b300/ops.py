@@ -45,10 +45,15 @@ def workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
     return int(_lib.lib().ssm_scan_workspace_size(batch, dim, dstate, seqlen))
 
 
+def _flags(softplus, zoh):
+    return (_lib.FLAG_SOFTPLUS if softplus else 0) | (_lib.FLAG_ZOH if zoh else 0)
+
+
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
                  out=None, final_state=None, initial_state=None, workspace=None,
-                 out_dtype=None, return_final_state=True, stream=None):
-    """Selective scan over whole sequences. Returns (out, final_state or None)."""
+                 out_dtype=None, return_final_state=True, stream=None, zoh=False):
+    """Selective scan over whole sequences. Returns (out, final_state or None).
+    zoh: zero-order-hold discretisation of B instead of Euler."""
     if u.dim() != 3:
         raise ValueError("u must be (batch, dim, seqlen)")
     batch, dim, seqlen = u.shape
@@ -82,7 +87,7 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         st = _lib.lib().ssm_scan_fwd(
             _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-            int(bool(delta_softplus)), _ptr(out), _ptr(final_state), batch, dim, dstate, seqlen,
+            _flags(delta_softplus, zoh), _ptr(out), _ptr(final_state), batch, dim, dstate, seqlen,
             _DT[in_dt], _DT[out.dtype], _ptr(initial_state), _ptr(workspace), ws_bytes,
             _stream_handle(stream))
     _lib.check("ssm_scan_fwd", st)
@@ -90,7 +95,7 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
 
 
 def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, out=None, dt_bias=None,
-                     dt_softplus=True, out_dtype=None, stream=None):
+                     dt_softplus=True, out_dtype=None, stream=None, zoh=False):
     """One token: updates `state` in place and returns out (batch, dim)."""
     batch, dim, dstate = state.shape
     in_dt = x.dtype
@@ -114,7 +119,7 @@ def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, out=None, dt_bias=No
     with torch.cuda.device(dev):
         st = _lib.lib().ssm_state_update(
             _ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-            _ptr(out), _ptr(dt_bias), int(bool(dt_softplus)), batch, dim, dstate, _DT[in_dt],
+            _ptr(out), _ptr(dt_bias), _flags(dt_softplus, zoh), batch, dim, dstate, _DT[in_dt],
             _DT[out.dtype], _stream_handle(stream))
     _lib.check("ssm_state_update", st)
     return out
@@ -122,7 +127,7 @@ def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, out=None, dt_bias=No
 
 def ssm_scan_fwd_no_alloc(u, delta, A, B, C, D=None, z=None, delta_bias=None,
                           delta_softplus=True, out=None, final_state=None, initial_state=None,
-                          out_dtype=None, return_final_state=True, stream=None):
+                          out_dtype=None, return_final_state=True, stream=None, zoh=False):
     """ssm_scan_fwd without a workspace, for callers that cannot allocate device scratch.
 
     The library's time-split scratch comes from its own fixed device array
@@ -159,7 +164,7 @@ def ssm_scan_fwd_no_alloc(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     with torch.cuda.device(dev):
         st = _lib.lib().ssm_scan_fwd_no_alloc(
             _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-            int(bool(delta_softplus)), _ptr(out), _ptr(final_state), batch, dim, dstate, seqlen,
+            _flags(delta_softplus, zoh), _ptr(out), _ptr(final_state), batch, dim, dstate, seqlen,
             _DT[in_dt], _DT[out.dtype], _ptr(initial_state), _stream_handle(stream))
     _lib.check("ssm_scan_fwd_no_alloc", st)
     return out, final_state

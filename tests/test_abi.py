@@ -86,6 +86,8 @@ def call_scan(lib, **kw):
     (dict(final_state=fake(8) + 16), INVALID),  # final_state inside out
     (dict(out=fake(5)), INVALID),               # out over D
     (dict(initial_state=fake(9)), INVALID),     # final_state over initial_state
+    (dict(softplus=4), INVALID),                # unknown flag bit
+    (dict(softplus=-1), INVALID),
 ])
 def test_scan_rejects(lib, kw, expect):
     assert call_scan(lib, **kw) == expect
@@ -125,6 +127,7 @@ def call_update(lib, **kw):
     (dict(B=fake(4) + 2), ALIGN),
     (dict(out=fake(0) + 32), INVALID),   # out inside state
     (dict(state=fake(1)), INVALID),      # state over x
+    (dict(softplus=8), INVALID),         # unknown flag bit
 ])
 def test_update_rejects(lib, kw, expect):
     assert call_update(lib, **kw) == expect
