@@ -55,6 +55,8 @@ class Oracle:
                                              ctypes.POINTER(ctypes.c_int64)] + [_I64] * 4)
         lib.oracle_state_update.restype = None
         lib.oracle_state_update.argtypes = [_DP] * 9 + [ctypes.c_int, ctypes.c_int, _DP] + [_I64] * 3
+        lib.oracle_conv_step.restype = None
+        lib.oracle_conv_step.argtypes = [_DP] * 4 + [ctypes.c_int, _DP] + [_I64] * 3
         lib.oracle_max_threads.restype = ctypes.c_int
         self._lib = lib
         self.path = path
@@ -125,6 +127,28 @@ class Oracle:
         return st, out
 
 
+    def conv_step(self, conv_state, x, weight, bias=None, silu=True):
+        """One step of the short causal convolution. Returns (new_conv_state (batch, dim,
+        width), u (batch, dim)); inputs untouched."""
+        st = _f64(conv_state).copy()
+        x, weight, bias = map(_f64, (x, weight, bias))
+        batch, dim, width = st.shape
+        assert x.shape == (batch, dim) and weight.shape == (dim, width)
+        assert bias is None or bias.shape == (dim,)
+        u = np.empty((batch, dim), dtype=np.float64)
+        self._lib.oracle_conv_step(_p(st), _p(x), _p(weight), _p(bias), int(bool(silu)), _p(u),
+                                   batch, dim, width)
+        return st, u
+
+    def conv_state_update(self, conv_state, x, weight, conv_bias, conv_silu, state, dt, A, B, C,
+                          D=None, z=None, dt_bias=None, dt_softplus=True, zoh=False):
+        """The decode step of a layer: the convolution step, then the state update with the
+        convolution output as the input x. Returns (conv_state, state, u, out)."""
+        cst, u = self.conv_step(conv_state, x, weight, conv_bias, conv_silu)
+        st, out = self.state_update(state, u, dt, A, B, C, D, z, dt_bias, dt_softplus, zoh=zoh)
+        return cst, st, u, out
+
+
 _default = None
 
 
@@ -149,3 +173,11 @@ def scan_fwd_rows(*a, **k):
 
 def state_update(*a, **k):
     return default().state_update(*a, **k)
+
+
+def conv_step(*a, **k):
+    return default().conv_step(*a, **k)
+
+
+def conv_state_update(*a, **k):
+    return default().conv_state_update(*a, **k)

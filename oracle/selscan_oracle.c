@@ -158,3 +158,24 @@ void oracle_state_update(double* state, const double* x, const double* dt, const
         out[r] = y;
     }
 }
+
+/* One decode step of the short causal convolution of the Mamba block ("Mamba and State Space
+ * Models", section "A State of Fixed Size": each channel keeps "a short convolution that holds
+ * the last 4 inputs"). conv_state (batch, dim, width) holds the last `width` inputs of each
+ * channel, oldest first. The new input x enters at the end and the oldest leaves; the output is
+ * the depthwise convolution over the window, u = sum_k w[d,k] * window[k] + bias[d], optionally
+ * passed through silu. u: (batch, dim). */
+void oracle_conv_step(double* conv_state, const double* x, const double* w, const double* bias,
+                      int silu_on, double* u, int64_t batch, int64_t dim, int64_t width) {
+    int64_t rows = batch * dim;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t d = r % dim;
+        double* s = conv_state + r * width;
+        for (int64_t k = 0; k + 1 < width; ++k) s[k] = s[k + 1];
+        s[width - 1] = x[r];
+        double acc = bias ? bias[d] : 0.0;
+        for (int64_t k = 0; k < width; ++k) acc += w[d * width + k] * s[k];
+        u[r] = silu_on ? silu(acc) : acc;
+    }
+}

@@ -266,6 +266,29 @@ def pin_theorem1_gate(orc, seed=17):
     return max(relerr(out, ref), relerr(fin[..., 0], ref[..., -1]), relerr(ys, ref))
 
 
+def pin_conv_step_is_causal_convolution(orc, seed=18):
+    """'A State of Fixed Size': the block's short convolution holds the last 4 inputs. Run
+    step by step from a zero window, its outputs must be the causal depthwise convolution of
+    the input sequence with the 4 taps, evaluated here with numpy.convolve (then silu)."""
+    r = _rng(seed)
+    batch, dim, width, L = 2, 5, 4, 23
+    x = r.standard_normal((batch, dim, L))
+    w = r.standard_normal((dim, width))
+    bias = r.standard_normal(dim)
+    st = np.zeros((batch, dim, width))
+    got = np.empty((batch, dim, L))
+    for t in range(L):
+        st, got[:, :, t] = orc.conv_step(st, x[:, :, t], w, bias, True)
+    ref = np.empty_like(got)
+    for b in range(batch):
+        for d in range(dim):
+            # window oldest-first: u_t = sum_k w[k] x[t - (width-1) + k]
+            full = np.convolve(x[b, d], w[d][::-1])[:L] + bias[d]
+            ref[b, d] = silu_ref(full)
+    last = x[:, :, L - width:]
+    return max(relerr(got, ref), float(np.max(np.abs(st - last))) * 1e300)
+
+
 # (pin function, bound) pairs used by the pin tests and the mutation tests.
 ALL_PINS = [
     (pin_lti_convolution, 1e-11),
@@ -282,4 +305,5 @@ ALL_PINS = [
     (lambda o: pin_lti_convolution(o, seed=23, zoh=True), 1e-11),
     (lambda o: pin_solved_form(o, seed=24, zoh=True), 1e-11),
     (lambda o: pin_update_is_one_scan_step(o, seed=25, zoh=True), 1e-12),
+    (pin_conv_step_is_causal_convolution, 1e-13),
 ]

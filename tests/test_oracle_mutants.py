@@ -48,6 +48,10 @@ MUTANTS = {
                                 "h[n] = abar * h[n] + f * B[n] * x[r];"),
     "update_bias_ignored": ("double xx = dt[r] + (dt_bias ? dt_bias[d] : 0.0);", "double xx = dt[r];"),
     "update_gate_dropped": ("if (z) y *= silu(z[r]);", ""),
+    "conv_window_not_shifted": ("for (int64_t k = 0; k + 1 < width; ++k) s[k] = s[k + 1];", ""),
+    "conv_taps_reversed": ("acc += w[d * width + k] * s[k];", "acc += w[d * width + (width - 1 - k)] * s[k];"),
+    "conv_bias_dropped": ("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
+    "conv_silu_dropped": ("u[r] = silu_on ? silu(acc) : acc;", "u[r] = acc;"),
 }
 
 
