@@ -64,11 +64,15 @@ def scan_algorithmic_bytes(cfg) -> int:
     return act * (nact_in * ein + eout) + 2 * bc * ein + per_ch + cfg.batch * cfg.dim * cfg.dstate * 4
 
 
-def decode_algorithmic_bytes(batch, dim, dstate) -> int:
+def decode_algorithmic_bytes(batch, dim, dstate, conv=False) -> int:
     """Per layer-step: state read + write (fp32), x/dt/z read + out write (bf16), B and C
-    (bf16), A (fp32) and D, dt_bias (fp32)."""
-    return (batch * dim * dstate * 4 * 2 + batch * dim * 2 * 4 + batch * dstate * 2 * 2
-            + dim * dstate * 4 + dim * 4 * 2)
+    (bf16), A (fp32) and D, dt_bias (fp32); with the convolution also its bf16 window of 4
+    read + write and its fp32 taps and bias."""
+    n = (batch * dim * dstate * 4 * 2 + batch * dim * 2 * 4 + batch * dstate * 2 * 2
+         + dim * dstate * 4 + dim * 4 * 2)
+    if conv:
+        n += batch * dim * 4 * 2 * 2 + dim * 4 * 4 + dim * 4
+    return n
 
 
 class ClockSampler:
@@ -243,25 +247,38 @@ def time_scan_e2e(cfg, steps, warmup, x, stream):
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
-def time_decode(batch, steps, warmup, stream):
+def time_decode(batch, steps, warmup, stream, conv=False):
     """Decode sweep: per generated token, ssm_state_update on each of 64 layers (own state,
     A, D, dt_bias per layer); the 64 calls of a token are one CUDA graph, one graph per slot
-    of the ring of 8 token-input sets."""
-    from selective_state_space_110_b300 import ssm_state_update
+    of the ring of 8 token-input sets. conv=True: the fused step of the short convolution
+    (own bf16 window of 4 inputs and fp32 taps per layer) and the state update,
+    ssm_conv_state_update."""
+    from selective_state_space_110_b300 import ssm_conv_state_update, ssm_state_update
     cfg = DECODE_CONFIG
     p = make_decode_layer_params(cfg, "cuda")
+    gen = torch.Generator("cuda").manual_seed(cfg.seed + 17)
     layers = []
     for l in range(cfg.layers):
         layers.append(dict(A=p["A"].clone(), D=p["D"].clone(), bias=p["dt_bias"].clone(),
                            state=make_decode_state(cfg, batch, l, "cuda"),
                            out=torch.empty(batch, cfg.dim, dtype=torch.bfloat16, device="cuda"),
                            toks=[make_decode_tokens(cfg, batch, l, s, "cuda") for s in range(cfg.ring)]))
+        if conv:
+            layers[-1].update(
+                cs=torch.randn(batch, cfg.dim, 4, generator=gen, device="cuda").to(torch.bfloat16),
+                w=torch.randn(cfg.dim, 4, generator=gen, device="cuda") * 0.5,
+                cb=torch.randn(cfg.dim, generator=gen, device="cuda") * 0.1)
 
     def token_step(slot):
         for L in layers:
             t = L["toks"][slot]
-            ssm_state_update(L["state"], t["x"], t["dt"], L["A"], t["B"], t["C"], L["D"], t["z"],
-                             out=L["out"], dt_bias=L["bias"], stream=stream)
+            if conv:
+                ssm_conv_state_update(L["cs"], t["x"], L["w"], L["cb"], True, L["state"], t["dt"],
+                                      L["A"], t["B"], t["C"], L["D"], t["z"], out=L["out"],
+                                      dt_bias=L["bias"], stream=stream)
+            else:
+                ssm_state_update(L["state"], t["x"], t["dt"], L["A"], t["B"], t["C"], L["D"],
+                                 t["z"], out=L["out"], dt_bias=L["bias"], stream=stream)
 
     with torch.cuda.stream(stream):
         for s in range(3):
@@ -345,17 +362,18 @@ def run_ours(args):
 
     e2e_ms, h2d, d2h = time_scan_e2e(cfg, max(2, min(args.steps, 10)), 2, x, stream)
     e2e_ms = max_over_ranks(e2e_ms, world)
-    dec = {}
-    for b in args.decode_batches:
-        dms, nl = time_decode(b, args.decode_steps, 8, stream)
-        dms = max_over_ranks(dms, world)
-        dbytes = decode_algorithmic_bytes(b, DECODE_CONFIG.dim, DECODE_CONFIG.dstate) * nl
-        dec[f"batch{b}"] = {"steps_per_s": round(world * 1e3 / dms, 1),
-                            "tokens_per_s": round(world * b * 1e3 / dms, 1),
-                            "ms_per_step": round(dms, 4),
-                            "achieved_gbs": round(dbytes / (dms * 1e-3) / 1e9, 1),
-                            "hbm_frac": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 3),
-                            "launches_per_step": nl}
+    dec, dec_conv = {}, {}
+    for conv, sink in ((False, dec), (True, dec_conv)):
+        for b in (args.decode_batches if not conv else args.decode_conv_batches):
+            dms, nl = time_decode(b, args.decode_steps, 8, stream, conv=conv)
+            dms = max_over_ranks(dms, world)
+            dbytes = decode_algorithmic_bytes(b, DECODE_CONFIG.dim, DECODE_CONFIG.dstate, conv) * nl
+            sink[f"batch{b}"] = {"steps_per_s": round(world * 1e3 / dms, 1),
+                                 "tokens_per_s": round(world * b * 1e3 / dms, 1),
+                                 "ms_per_step": round(dms, 4),
+                                 "achieved_gbs": round(dbytes / (dms * 1e-3) / 1e9, 1),
+                                 "hbm_frac": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 3),
+                                 "launches_per_step": nl}
 
     if rank != 0:
         return
@@ -396,6 +414,9 @@ def run_ours(args):
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "decode": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim, **dec},
+        "decode_conv": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim,
+                        "what": "ssm_conv_state_update: width-4 convolution step + state update",
+                        **dec_conv},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, x)
@@ -467,6 +488,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-batches", type=int, nargs="*", default=[1, 16, 64])
     ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--decode-conv-batches", type=int, nargs="*", default=[1, 64])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="untimed back-to-back scans before the timed steps (clock sampling)")

@@ -128,6 +128,33 @@ selscan_status ssm_state_update(float* state, const void* x, const void* dt, con
                                 selscan_dtype out_dtype, selscan_stream_t stream);
 
 /*
+ * ssm_conv_state_update: the decode step of one layer's two fixed-size states. "A State of
+ * Fixed Size" gives each channel its 16 state numbers "plus a short convolution that holds the
+ * last 4 inputs"; this call moves both once per generated token in one kernel:
+ *   1. the convolution window of each (b, d) drops its oldest input and takes x[b,d];
+ *      u = sum_k conv_weight[d,k] * window[k] + conv_bias[d], then silu(u) if conv_silu;
+ *   2. the state update of ssm_state_update with u as its input x (dt, B, C, z as given).
+ *
+ *   conv_state   (batch, dim, conv_width)  in_dtype, oldest input first, rolled in place
+ *   x            (batch, dim)              in_dtype, the new input to the convolution
+ *   conv_weight  (dim, conv_width) fp32;   conv_bias (dim) fp32, NULL = 0
+ *   conv_out     (batch, dim)              in_dtype, u, NULL = not written
+ *   state, dt, A, B, C, D, z, out, dt_bias, dt_flags: as ssm_state_update.
+ * conv_width must be 4. With state == NULL only step 1 runs (conv_out is then required and the
+ * state-update arguments are ignored): in a Mamba-1 block dt, B and C are projected from u by a
+ * dense layer, so the caller runs step 1, the projection, then ssm_state_update. The fused
+ * form fits blocks whose dt, B and C do not depend on u. Outputs must not overlap inputs or one
+ * another (SELSCAN_ERR_INVALID_ARG); every pointer 16-byte aligned.
+ */
+selscan_status ssm_conv_state_update(void* conv_state, const void* x, const float* conv_weight,
+                                     const float* conv_bias, int conv_silu, int64_t conv_width,
+                                     void* conv_out, float* state, const void* dt, const float* A,
+                                     const void* B, const void* C, const float* D, const void* z,
+                                     void* out, const float* dt_bias, int dt_flags, int64_t batch,
+                                     int64_t dim, int64_t dstate, selscan_dtype in_dtype,
+                                     selscan_dtype out_dtype, selscan_stream_t stream);
+
+/*
  * ssm_scan_fwd_no_alloc: ssm_scan_fwd for callers that cannot allocate device memory.
  *
  * The paper has no counterpart to this entry point; it exists for callers that have no way to

@@ -28,7 +28,8 @@ STATUS = {
 
 # Every symbol include/selscan.h declares.
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selscan_status_string",
-           "ssm_scan_fwd_no_alloc", "selscan_device_status", "selscan_selftest_wait_timeout")
+           "ssm_scan_fwd_no_alloc", "selscan_device_status", "selscan_selftest_wait_timeout",
+           "ssm_conv_state_update")
 
 # Size of the fixed scratch array behind ssm_scan_fwd_no_alloc (SELSCAN_NO_ALLOC_SCRATCH_BYTES).
 NO_ALLOC_SCRATCH_BYTES = 524288
@@ -60,6 +61,10 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_no_alloc.restype = ctypes.c_int
     lib.ssm_scan_fwd_no_alloc.argtypes = ([_VP] * 8 + [ctypes.c_int, _VP, _VP] + [_I64] * 4 +
                                           [ctypes.c_int, ctypes.c_int, _VP, _VP])
+    lib.ssm_conv_state_update.restype = ctypes.c_int
+    lib.ssm_conv_state_update.argtypes = ([_VP] * 4 + [ctypes.c_int, _I64] + [_VP] * 9 +
+                                          [_VP, ctypes.c_int] + [_I64] * 3 +
+                                          [ctypes.c_int, ctypes.c_int, _VP])
     lib.selscan_device_status.restype = ctypes.c_int
     lib.selscan_device_status.argtypes = [ctypes.c_int, _VP]
     lib.selscan_selftest_wait_timeout.restype = ctypes.c_int

@@ -15,6 +15,7 @@ constexpr int64_t kStateN = 16;
 constexpr int64_t kMinSegTokens = 4096;  // shortest time segment worth a split
 constexpr int64_t kTwoRowsMinRows = 16384;  // rows from which two rows per lane pay off
 constexpr int kKnownFlags = SELSCAN_FLAG_SOFTPLUS | SELSCAN_FLAG_ZOH;
+constexpr int64_t kConvTaps = 4;  // width of the block's short convolution
 constexpr size_t kWsAlign = 256;
 
 size_t dtype_size(selscan_dtype t) { return t == SELSCAN_BF16 ? 2 : 4; }
@@ -243,4 +244,59 @@ SELSCAN_EXPORT selscan_status selscan_selftest_wait_timeout(int64_t limit_cycles
                    cudaSuccess
                ? SELSCAN_OK
                : SELSCAN_ERR_CUDA;
+}
+
+SELSCAN_EXPORT selscan_status ssm_conv_state_update(
+    void* conv_state, const void* x, const float* conv_weight, const float* conv_bias,
+    int conv_silu, int64_t conv_width, void* conv_out, float* state, const void* dt,
+    const float* A, const void* B, const void* C, const float* D, const void* z, void* out,
+    const float* dt_bias, int dt_flags, int64_t batch, int64_t dim, int64_t dstate,
+    selscan_dtype in_dtype, selscan_dtype out_dtype, selscan_stream_t stream) {
+    const bool ssm = state != nullptr;
+    if (conv_width != kConvTaps || !dtype_ok(in_dtype) || (ssm && !dtype_ok(out_dtype)) ||
+        (ssm && dstate != kStateN))
+        return SELSCAN_ERR_UNSUPPORTED;
+    if (!shape_ok(batch, dim, 0) || (dt_flags & ~kKnownFlags)) return SELSCAN_ERR_INVALID_ARG;
+    if (!conv_state || !x || !conv_weight) return SELSCAN_ERR_INVALID_ARG;
+    if (ssm ? (!dt || !A || !B || !C || !out) : !conv_out) return SELSCAN_ERR_INVALID_ARG;
+    const void* ptrs[] = {conv_state, x, conv_weight, conv_bias, conv_out, state, dt, A, B, C,
+                          D, z, out, dt_bias};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
+    const size_t ein = dtype_size(in_dtype), eout = dtype_size(out_dtype);
+    const size_t rows = (size_t)batch * (size_t)dim;
+    const Range in_r[] = {range_of(x, rows * ein), range_of(conv_weight, (size_t)dim * kConvTaps * 4),
+                          range_of(conv_bias, conv_bias ? (size_t)dim * 4 : 0),
+                          range_of(dt, ssm ? rows * ein : 0),
+                          range_of(A, ssm ? (size_t)dim * kStateN * 4 : 0),
+                          range_of(B, ssm ? (size_t)batch * kStateN * ein : 0),
+                          range_of(C, ssm ? (size_t)batch * kStateN * ein : 0),
+                          range_of(D, ssm && D ? (size_t)dim * 4 : 0),
+                          range_of(z, ssm && z ? rows * ein : 0),
+                          range_of(dt_bias, ssm && dt_bias ? (size_t)dim * 4 : 0)};
+    const Range out_r[] = {range_of(conv_state, rows * kConvTaps * ein),
+                           range_of(conv_out, conv_out ? rows * ein : 0),
+                           range_of(state, ssm ? rows * kStateN * sizeof(float) : 0),
+                           range_of(out, ssm ? rows * eout : 0)};
+    for (size_t i = 0; i < 4; ++i) {
+        for (const Range& r : in_r)
+            if (overlaps(out_r[i], r)) return SELSCAN_ERR_INVALID_ARG;
+        for (size_t j = i + 1; j < 4; ++j)
+            if (overlaps(out_r[i], out_r[j])) return SELSCAN_ERR_INVALID_ARG;
+    }
+
+    int sms = 0;
+    selscan_status st = device_sms(&sms);
+    if (st != SELSCAN_OK) return st;
+    selscan::UpdateArgs a{};
+    a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.out = out; a.dt_bias = dt_bias; a.dim = dim; a.rows = (int64_t)rows;
+    a.softplus = (dt_flags & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
+    a.zoh = (dt_flags & SELSCAN_FLAG_ZOH) ? 1 : 0;
+    a.conv_state = conv_state; a.conv_weight = conv_weight; a.conv_bias = conv_bias;
+    a.conv_silu = conv_silu ? 1 : 0; a.conv_out = conv_out;
+    cudaError_t e = selscan::launch_state_update(a, in_dtype == SELSCAN_BF16,
+                                                 out_dtype == SELSCAN_BF16,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
 }

@@ -59,6 +59,13 @@ struct UpdateArgs {
     int64_t rows;  // batch*dim
     int softplus;
     int zoh;
+    // Short causal convolution before the update (conv_state NULL = none); state NULL with a
+    // conv_state runs the convolution step alone.
+    void* conv_state;          // (rows, 4), input dtype, rolled in place
+    const float* conv_weight;  // (dim, 4)
+    const float* conv_bias;    // (dim) or NULL
+    int conv_silu;
+    void* conv_out;            // (rows), input dtype, or NULL
 };
 
 cudaError_t launch_state_update(const UpdateArgs& a, bool in_bf16, bool out_bf16,

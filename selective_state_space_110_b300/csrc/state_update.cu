@@ -25,6 +25,7 @@
 namespace selscan {
 
 constexpr int kUpdThreads = 256;
+constexpr int kConvWidth = 4;  // taps of the short convolution (one per lane of a quad)
 
 template <typename Tin>
 __device__ __forceinline__ void load4(const Tin* p, float (&v)[4]);
@@ -48,7 +49,10 @@ __device__ __forceinline__ float upd_phi_fast(float x, float abar, float a, floa
     return fabsf(x) < 0.0625f ? p : (abar - 1.f) / a * dinv;
 }
 
-template <typename Tin, typename Tout, bool kPrecise, bool kZoh>
+// kConv: first the decode step of the block's short causal convolution (width 4 = the quad:
+// lane g holds tap g of the window, the window moves by one quad shuffle and the four taps are
+// summed by two), whose output is the input x of the state update. kSsm: the state update.
+template <typename Tin, typename Tout, bool kPrecise, bool kZoh, bool kConv, bool kSsm>
 __global__ void __launch_bounds__(kUpdThreads) state_update_kernel(const UpdateArgs a) {
     // Wait for earlier grids in the stream (a no-op without programmatic serialization),
     // then let the next one begin its launch.
@@ -62,16 +66,46 @@ __global__ void __launch_bounds__(kUpdThreads) state_update_kernel(const UpdateA
     const int64_t d = active ? d_raw : 0;
     const int64_t row = b * a.dim + d;
 
+    // Every load is issued before any store: the state stream starts at once and nothing
+    // waits on a possible alias of the convolution window.
     float4* const sp = reinterpret_cast<float4*>(a.state + row * kN + 4 * g);
-    float4 h = __ldcs(sp);
-    float4 A4 = __ldg(reinterpret_cast<const float4*>(a.A + d * kN + 4 * g));
-    float Bv[4], Cv[4];
-    load4<Tin>(static_cast<const Tin*>(a.B) + b * kN + 4 * g, Bv);
-    load4<Tin>(static_cast<const Tin*>(a.C) + b * kN + 4 * g, Cv);
-    const float x = to_f32(static_cast<const Tin*>(a.x)[row]);
-    const float xdt = to_f32(static_cast<const Tin*>(a.dt)[row]) + (a.dt_bias ? a.dt_bias[d] : 0.f);
-    const float zv = a.z ? to_f32(static_cast<const Tin*>(a.z)[row]) : 0.f;
-    const float Dd = a.D ? a.D[d] : 0.f;
+    float4 h = make_float4(0.f, 0.f, 0.f, 0.f), A4 = h;
+    float Bv[4] = {0.f, 0.f, 0.f, 0.f}, Cv[4] = {0.f, 0.f, 0.f, 0.f};
+    float xdt = 0.f, zv = 0.f, Dd = 0.f;
+    if (kSsm) {
+        h = __ldcs(sp);
+        A4 = __ldg(reinterpret_cast<const float4*>(a.A + d * kN + 4 * g));
+        load4<Tin>(static_cast<const Tin*>(a.B) + b * kN + 4 * g, Bv);
+        load4<Tin>(static_cast<const Tin*>(a.C) + b * kN + 4 * g, Cv);
+        xdt = to_f32(static_cast<const Tin*>(a.dt)[row]) + (a.dt_bias ? a.dt_bias[d] : 0.f);
+        zv = a.z ? to_f32(static_cast<const Tin*>(a.z)[row]) : 0.f;
+        Dd = a.D ? a.D[d] : 0.f;
+    }
+
+    float x;
+    if (kConv) {
+        Tin* const cs = static_cast<Tin*>(a.conv_state) + row * kConvWidth + g;
+        const float s_old = to_f32(*cs);
+        const float x_in = to_f32(static_cast<const Tin*>(a.x)[row]);
+        const float w = a.conv_weight[d * kConvWidth + g];
+        const float cb = a.conv_bias ? a.conv_bias[d] : 0.f;
+        // Window oldest first: the new window is old[1..3] followed by the new input.
+        const float s_next = __shfl_down_sync(0xffffffffu, s_old, 1, kConvWidth);
+        const float s_new = g == kConvWidth - 1 ? x_in : s_next;
+        float acc = w * s_new;
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += cb;
+        if (a.conv_silu) acc = kPrecise ? silu_f<true>(acc) : silu2(make_float2(acc, acc)).x;
+        x = acc;
+        if (active) {
+            *cs = from_f32<Tin>(s_new);  // a copy of an input value: exact
+            if (a.conv_out && g == 0) static_cast<Tin*>(a.conv_out)[row] = from_f32<Tin>(acc);
+        }
+        if (!kSsm) return;
+    } else {
+        x = to_f32(static_cast<const Tin*>(a.x)[row]);
+    }
 
     float dt;
     if (!a.softplus) dt = xdt;
@@ -86,9 +120,9 @@ __global__ void __launch_bounds__(kUpdThreads) state_update_kernel(const UpdateA
         // relative precision over thousands of generated tokens.
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-            const float x = dt * Av[n];
-            const float m = expm1f(x);
-            const float f = kZoh ? upd_phi_exact(m, x) : 1.f;
+            const float xa = dt * Av[n];
+            const float m = expm1f(xa);
+            const float f = kZoh ? upd_phi_exact(m, xa) : 1.f;
             hv[n] = fmaf(m, hv[n], hv[n]) + k * Bv[n] * f;
         }
     } else {
@@ -117,7 +151,7 @@ __global__ void __launch_bounds__(kUpdThreads) state_update_kernel(const UpdateA
     }
 }
 
-template <typename Tin, typename Tout, bool kPrecise, bool kZoh>
+template <typename Tin, typename Tout, bool kPrecise, bool kZoh, bool kConv, bool kSsm>
 static cudaError_t launch_one(const UpdateArgs& a, int64_t batch, cudaStream_t stream) {
     const int64_t lanes = a.dim * 4;
     cudaLaunchConfig_t cfg{};
@@ -130,7 +164,18 @@ static cudaError_t launch_one(const UpdateArgs& a, int64_t batch, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, state_update_kernel<Tin, Tout, kPrecise, kZoh>, a);
+    return cudaLaunchKernelEx(&cfg, state_update_kernel<Tin, Tout, kPrecise, kZoh, kConv, kSsm>, a);
+}
+
+template <typename Tin, typename Tout, bool kPrecise>
+static cudaError_t launch_mode(const UpdateArgs& a, int64_t batch, cudaStream_t stream) {
+    if (a.conv_state && !a.state)  // convolution step only
+        return launch_one<Tin, Tout, kPrecise, false, true, false>(a, batch, stream);
+    if (a.conv_state)
+        return a.zoh ? launch_one<Tin, Tout, kPrecise, true, true, true>(a, batch, stream)
+                     : launch_one<Tin, Tout, kPrecise, false, true, true>(a, batch, stream);
+    return a.zoh ? launch_one<Tin, Tout, kPrecise, true, false, true>(a, batch, stream)
+                 : launch_one<Tin, Tout, kPrecise, false, false, true>(a, batch, stream);
 }
 
 cudaError_t launch_state_update(const UpdateArgs& a, bool in_bf16, bool out_bf16,
@@ -138,20 +183,12 @@ cudaError_t launch_state_update(const UpdateArgs& a, bool in_bf16, bool out_bf16
     using bf = __nv_bfloat16;
     const int64_t batch = a.rows / a.dim;
     cudaError_t e;
-    if (a.zoh) {
-        if (in_bf16) {
-            e = out_bf16 ? launch_one<bf, bf, false, true>(a, batch, stream)
-                         : launch_one<bf, float, false, true>(a, batch, stream);
-        } else {
-            e = out_bf16 ? launch_one<float, bf, true, true>(a, batch, stream)
-                         : launch_one<float, float, true, true>(a, batch, stream);
-        }
-    } else if (in_bf16) {
-        e = out_bf16 ? launch_one<bf, bf, false, false>(a, batch, stream)
-                     : launch_one<bf, float, false, false>(a, batch, stream);
+    if (in_bf16) {
+        e = out_bf16 ? launch_mode<bf, bf, false>(a, batch, stream)
+                     : launch_mode<bf, float, false>(a, batch, stream);
     } else {
-        e = out_bf16 ? launch_one<float, bf, true, false>(a, batch, stream)
-                     : launch_one<float, float, true, false>(a, batch, stream);
+        e = out_bf16 ? launch_mode<float, bf, true>(a, batch, stream)
+                     : launch_mode<float, float, true>(a, batch, stream);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

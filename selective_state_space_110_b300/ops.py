@@ -168,3 +168,47 @@ def ssm_scan_fwd_no_alloc(u, delta, A, B, C, D=None, z=None, delta_bias=None,
             _DT[in_dt], _DT[out.dtype], _ptr(initial_state), _stream_handle(stream))
     _lib.check("ssm_scan_fwd_no_alloc", st)
     return out, final_state
+
+
+def ssm_conv_state_update(conv_state, x, conv_weight, conv_bias=None, conv_silu=True,
+                          state=None, dt=None, A=None, B=None, C=None, D=None, z=None, out=None,
+                          dt_bias=None, dt_softplus=True, out_dtype=None, conv_out=None,
+                          return_conv_out=False, stream=None, zoh=False):
+    """Decode step of the short convolution (conv_state (batch, dim, 4) rolled in place) and,
+    when `state` is given, of the selective state with the convolution output as its input.
+    Returns (out or None, conv_out or None)."""
+    batch, dim, width = conv_state.shape
+    in_dt = x.dtype
+    if in_dt not in _DT:
+        raise ValueError(f"unsupported input dtype {in_dt}")
+    dev = conv_state.device
+    _check_dev("conv_state", conv_state, in_dt, (batch, dim, width), dev)
+    _check_dev("x", x, in_dt, (batch, dim), dev)
+    _check_dev("conv_weight", conv_weight, torch.float32, (dim, width), dev)
+    _check_dev("conv_bias", conv_bias, torch.float32, (dim,), dev)
+    if conv_out is None and (return_conv_out or state is None):
+        conv_out = torch.empty((batch, dim), dtype=in_dt, device=dev)
+    _check_dev("conv_out", conv_out, in_dt, (batch, dim), dev)
+    dstate = 16
+    if state is not None:
+        dstate = state.shape[-1]
+        _check_dev("state", state, torch.float32, (batch, dim, dstate), dev)
+        _check_dev("dt", dt, in_dt, (batch, dim), dev)
+        _check_dev("A", A, torch.float32, (dim, dstate), dev)
+        _check_dev("B", B, in_dt, (batch, dstate), dev)
+        _check_dev("C", C, in_dt, (batch, dstate), dev)
+        _check_dev("D", D, torch.float32, (dim,), dev)
+        _check_dev("z", z, in_dt, (batch, dim), dev)
+        _check_dev("dt_bias", dt_bias, torch.float32, (dim,), dev)
+        if out is None:
+            out = torch.empty((batch, dim), dtype=out_dtype or in_dt, device=dev)
+        _check_dev("out", out, None, (batch, dim), dev)
+    odt = _DT[out.dtype] if out is not None else _DT[in_dt]
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssm_conv_state_update(
+            _ptr(conv_state), _ptr(x), _ptr(conv_weight), _ptr(conv_bias), int(bool(conv_silu)),
+            width, _ptr(conv_out), _ptr(state), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+            _ptr(z), _ptr(out), _ptr(dt_bias), _flags(dt_softplus, zoh), batch, dim, dstate,
+            _DT[in_dt], odt, _stream_handle(stream))
+    _lib.check("ssm_conv_state_update", st)
+    return out, conv_out

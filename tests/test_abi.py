@@ -143,3 +143,41 @@ def test_no_alloc_scratch_size_matches_header():
     text = open(HEADER).read()
     m = re.search(r"#define SELSCAN_NO_ALLOC_SCRATCH_BYTES \(\(size_t\)(\d+)\)", text)
     assert m and int(m.group(1)) == _lib.NO_ALLOC_SCRATCH_BYTES
+
+
+def call_conv(lib, **kw):
+    a = dict(conv_state=fake(0), x=fake(1), w=fake(2), cb=fake(3), silu=1, width=4, conv_out=fake(4),
+             state=fake(5), dt=fake(6), A=fake(7), B=fake(8), C=fake(9), D=fake(10), z=fake(11),
+             out=fake(12), dt_bias=fake(13), flags=1, batch=4, dim=512, dstate=16,
+             in_dtype=_lib.BF16, out_dtype=_lib.BF16, stream=None)
+    a.update(kw)
+    return lib.ssm_conv_state_update(a["conv_state"], a["x"], a["w"], a["cb"], a["silu"], a["width"],
+                                     a["conv_out"], a["state"], a["dt"], a["A"], a["B"], a["C"], a["D"],
+                                     a["z"], a["out"], a["dt_bias"], a["flags"], a["batch"], a["dim"],
+                                     a["dstate"], a["in_dtype"], a["out_dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(width=3), UNSUP),
+    (dict(dstate=8), UNSUP),
+    (dict(conv_state=None), INVALID),
+    (dict(x=None), INVALID),
+    (dict(w=None), INVALID),
+    (dict(dt=None), INVALID),                  # needed when state is given
+    (dict(state=None, conv_out=None), INVALID),  # conv step alone must write conv_out
+    (dict(flags=4), INVALID),
+    (dict(x=fake(1) + 2), ALIGN),
+    (dict(conv_out=fake(0) + 16), INVALID),    # conv_out inside conv_state
+    (dict(out=fake(5) + 64), INVALID),         # out inside state
+    (dict(conv_state=fake(2)), INVALID),       # conv_state over the weights
+])
+def test_conv_update_rejects(lib, kw, expect):
+    assert call_conv(lib, **kw) == expect
+
+
+def test_conv_update_valid_args_reach_the_device_check(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("device present: covered by the GPU tests")
+    assert call_conv(lib) == CUDA
+    assert call_conv(lib, state=None, dt=None, A=None, B=None, C=None, out=None) == CUDA
