@@ -55,6 +55,8 @@ class Oracle:
                                              ctypes.POINTER(ctypes.c_int64)] + [_I64] * 4)
         lib.oracle_state_update.restype = None
         lib.oracle_state_update.argtypes = [_DP] * 9 + [ctypes.c_int, ctypes.c_int, _DP] + [_I64] * 3
+        lib.oracle_scan_bwd.restype = None
+        lib.oracle_scan_bwd.argtypes = [_DP] * 8 + [ctypes.c_int] + [_DP] * 12 + [_I64] * 4
         lib.oracle_conv_step.restype = None
         lib.oracle_conv_step.argtypes = [_DP] * 4 + [ctypes.c_int, _DP] + [_I64] * 3
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -127,6 +129,33 @@ class Oracle:
         return st, out
 
 
+    def scan_bwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 initial_state=None, dout=None, dfinal=None):
+        """Gradients of sum(dout*out) + sum(dfinal*final_state) with respect to every input of
+        scan_fwd (Euler). Returns a dict of float64 arrays: du, ddelta, dA, dB, dC, dD, dz,
+        ddelta_bias, dinitial_state (dD / dz / ddelta_bias / dinitial_state None when the
+        corresponding input is None)."""
+        u, delta, A, B, C = map(_f64, (u, delta, A, B, C))
+        D, z, delta_bias, initial_state, dout, dfinal = map(
+            _f64, (D, z, delta_bias, initial_state, dout, dfinal))
+        batch, dim, seqlen = u.shape
+        dstate = A.shape[1]
+        assert dout is not None and dout.shape == u.shape
+        g = {k: np.zeros(u.shape) for k in ("du", "ddelta")}
+        g["dA"] = np.zeros(A.shape)
+        g["dB"] = np.zeros(B.shape)
+        g["dC"] = np.zeros(C.shape)
+        g["dD"] = np.zeros(dim) if D is not None else None
+        g["dz"] = np.zeros(u.shape) if z is not None else None
+        g["ddelta_bias"] = np.zeros(dim) if delta_bias is not None else None
+        g["dinitial_state"] = np.zeros((batch, dim, dstate)) if initial_state is not None else None
+        self._lib.oracle_scan_bwd(
+            _p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+            int(bool(delta_softplus)), _p(initial_state), _p(dout), _p(dfinal), _p(g["du"]),
+            _p(g["ddelta"]), _p(g["dA"]), _p(g["dB"]), _p(g["dC"]), _p(g["dD"]), _p(g["dz"]),
+            _p(g["ddelta_bias"]), _p(g["dinitial_state"]), batch, dim, dstate, seqlen)
+        return g
+
     def conv_step(self, conv_state, x, weight, bias=None, silu=True):
         """One step of the short causal convolution. Returns (new_conv_state (batch, dim,
         width), u (batch, dim)); inputs untouched."""
@@ -177,6 +206,10 @@ def state_update(*a, **k):
 
 def conv_step(*a, **k):
     return default().conv_step(*a, **k)
+
+
+def scan_bwd(*a, **k):
+    return default().scan_bwd(*a, **k)
 
 
 def conv_state_update(*a, **k):

@@ -179,3 +179,81 @@ void oracle_conv_step(double* conv_state, const double* x, const double* w, cons
         u[r] = silu_on ? silu(acc) : acc;
     }
 }
+
+/* Gradients of the scan (Euler discretisation) by reverse-mode differentiation of the loss
+ * sum_t dout[t]*out[t] + sum_n dfinal[n]*final_state[n]. Every forward state of the row is
+ * kept (this is the slow reference; the library recomputes them instead). Recurrences, per
+ * row, with x_t = delta_t + bias, Delta_t = softplus(x_t) (or x_t), Abar = exp(Delta*A),
+ * k = Delta*u, s_t = C_t . h_t + D u_t, out_t = s_t * silu(z_t):
+ *   ds_t = dout_t * silu(z_t),       dz_t = dout_t * s_t * silu'(z_t)
+ *   g_t  = ds_t * C_t + Abar_{t+1} * g_{t+1}     (g_{L-1} also receives dfinal)
+ *   dAbar_t[n] = g_t[n] * h_{t-1}[n],  dk_t = sum_n g_t[n] * B_t[n]
+ *   dDelta_t = sum_n dAbar_t[n] * Abar_t[n] * A[n] + dk_t * u_t,  du_t = dk_t * Delta_t + ds_t * D
+ *   ddelta_t = dDelta_t * sigmoid(x_t) (softplus) or dDelta_t;  dbias += ddelta_t
+ *   dA[n] += dAbar_t[n] * Abar_t[n] * Delta_t;  dD += ds_t * u_t
+ *   dB_t[n] += g_t[n] * k_t;  dC_t[n] += ds_t * h_t[n];  dinitial = Abar_0 * g_0
+ * dA, dB, dC, dD, dbias accumulate over rows (they are shared by channels or batches) and must
+ * be zeroed by the caller; the others are written. */
+void oracle_scan_bwd(const double* u, const double* delta, const double* A, const double* B,
+                     const double* C, const double* D, const double* z, const double* delta_bias,
+                     int delta_softplus, const double* initial_state, const double* dout,
+                     const double* dfinal, double* du, double* ddelta, double* dA, double* dB,
+                     double* dC, double* dD, double* dz, double* dbias, double* dinitial,
+                     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+    const int64_t L = seqlen, N = dstate;
+    for (int64_t r = 0; r < batch * dim; ++r) {  /* sequential: shared gradients accumulate */
+        const int64_t b = r / dim, d = r % dim, off = r * L;
+        const double* Bb = B + b * N * L;
+        const double* Cb = C + b * N * L;
+        double* hs = (double*)malloc(sizeof(double) * (size_t)((L + 1) * N));  /* h_{-1} .. h_{L-1} */
+        double* dl = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double* sg = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));  /* s_t */
+        double* g = (double*)malloc(sizeof(double) * (size_t)N);
+        const double bias = delta_bias ? delta_bias[d] : 0.0;
+        const double Dd = D ? D[d] : 0.0;
+        for (int64_t n = 0; n < N; ++n) hs[n] = initial_state ? initial_state[r * N + n] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {  /* forward, keeping every state */
+            const double x = delta[off + t] + bias;
+            const double dlt = delta_softplus ? softplus(x) : x;
+            dl[t] = dlt;
+            double s = Dd * u[off + t];
+            for (int64_t n = 0; n < N; ++n) {
+                const double h = exp(dlt * A[d * N + n]) * hs[t * N + n] + dlt * Bb[n * L + t] * u[off + t];
+                hs[(t + 1) * N + n] = h;
+                s += Cb[n * L + t] * h;
+            }
+            sg[t] = s;
+        }
+        for (int64_t n = 0; n < N; ++n) g[n] = dfinal ? dfinal[r * N + n] : 0.0;
+        for (int64_t t = L - 1; t >= 0; --t) {
+            const double x = delta[off + t] + bias;
+            double ds = dout[off + t];
+            if (z) {
+                const double zz = z[off + t], sig = 1.0 / (1.0 + exp(-zz));
+                dz[off + t] = dout[off + t] * sg[t] * (sig * (1.0 + zz * (1.0 - sig)));
+                ds = dout[off + t] * zz * sig;
+            }
+            double dk = 0.0, dDelta = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double abar = exp(dl[t] * A[d * N + n]);
+                g[n] += ds * Cb[n * L + t];
+                dC[b * N * L + n * L + t] += ds * hs[(t + 1) * N + n];
+                dB[b * N * L + n * L + t] += g[n] * dl[t] * u[off + t];
+                dk += g[n] * Bb[n * L + t];
+                const double dabar = g[n] * hs[t * N + n];
+                dDelta += dabar * abar * A[d * N + n];
+                dA[d * N + n] += dabar * abar * dl[t];
+                g[n] *= abar;  /* now Abar_t * g_t: the part that flows into h_{t-1} */
+            }
+            dDelta += dk * u[off + t];
+            du[off + t] = dk * dl[t] + ds * Dd;
+            const double dx = delta_softplus ? dDelta / (1.0 + exp(-x)) : dDelta;
+            ddelta[off + t] = dx;
+            if (dbias) dbias[d] += dx;
+            if (dD) dD[d] += ds * u[off + t];
+        }
+        if (dinitial)
+            for (int64_t n = 0; n < N; ++n) dinitial[r * N + n] = g[n];
+        free(hs); free(dl); free(sg); free(g);
+    }
+}

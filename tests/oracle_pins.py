@@ -289,6 +289,49 @@ def pin_conv_step_is_causal_convolution(orc, seed=18):
     return max(relerr(got, ref), float(np.max(np.abs(st - last))) * 1e300)
 
 
+def pin_backward_finite_differences(orc, seed=19, softplus=True, full=True):
+    """The backward pass (the training half of 'A Scan on the Chip') against central finite
+    differences of the forward: for loss = sum(dout*out) + sum(dfinal*final_state), each
+    gradient entry sampled below must equal (loss(x+eps) - loss(x-eps)) / (2 eps) of the
+    oracle's own forward. Every input is probed: u, delta, A, B, C, D, z, delta_bias, h0."""
+    r = _rng(seed)
+    p = _random_problem(seed, batch=2, dim=3, dstate=4, seqlen=14)
+    if not full:
+        p["z"], p["D"], p["delta_bias"], p["h0"] = None, None, None, None
+    if not softplus:  # keep Delta positive without softplus
+        p["delta"] = np.abs(p["delta"]) * 0.3 + 0.05
+        if p["delta_bias"] is not None:
+            p["delta_bias"] = np.abs(p["delta_bias"]) * 0.1
+    dout = r.standard_normal(p["u"].shape)
+    dfin = r.standard_normal((2, 3, 4))
+    keys = ["u", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0"]
+
+    def loss(q):
+        out, fin = orc.scan_fwd(q["u"], q["delta"], q["A"], q["B"], q["C"], q["D"], q["z"],
+                                q["delta_bias"], softplus, q["h0"])
+        return float(np.sum(out * dout) + np.sum(fin * dfin))
+
+    g = orc.scan_bwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
+                     softplus, p["h0"], dout, dfin)
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+             "delta_bias": "ddelta_bias", "h0": "dinitial_state"}
+    worst, eps = 0.0, 1e-5
+    for k in keys:
+        if p[k] is None:
+            continue
+        flat = p[k].reshape(-1)
+        for i in r.choice(flat.size, size=min(6, flat.size), replace=False):
+            q = {kk: (None if v is None else v.copy()) for kk, v in p.items()}
+            q[k].reshape(-1)[i] += eps
+            lp = loss(q)
+            q[k].reshape(-1)[i] -= 2 * eps
+            lm = loss(q)
+            fd = (lp - lm) / (2 * eps)
+            an = g[names[k]].reshape(-1)[i]
+            worst = max(worst, abs(an - fd) / max(abs(fd), 1e-2))
+    return worst
+
+
 # (pin function, bound) pairs used by the pin tests and the mutation tests.
 ALL_PINS = [
     (pin_lti_convolution, 1e-11),
@@ -306,4 +349,6 @@ ALL_PINS = [
     (lambda o: pin_solved_form(o, seed=24, zoh=True), 1e-11),
     (lambda o: pin_update_is_one_scan_step(o, seed=25, zoh=True), 1e-12),
     (pin_conv_step_is_causal_convolution, 1e-13),
+    (pin_backward_finite_differences, 1e-5),
+    (lambda o: pin_backward_finite_differences(o, seed=26, softplus=False, full=False), 1e-5),
 ]

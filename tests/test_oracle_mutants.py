@@ -48,6 +48,16 @@ MUTANTS = {
                                 "h[n] = abar * h[n] + f * B[n] * x[r];"),
     "update_bias_ignored": ("double xx = dt[r] + (dt_bias ? dt_bias[d] : 0.0);", "double xx = dt[r];"),
     "update_gate_dropped": ("if (z) y *= silu(z[r]);", ""),
+    "bwd_dDelta_drops_input_term": ("dDelta += dk * u[off + t];", ""),
+    "bwd_g_decays_before_readout": ("g[n] += ds * Cb[n * L + t];", "g[n] = g[n] * exp(dl[t] * A[d * N + n]) + ds * Cb[n * L + t];"),
+    "bwd_no_softplus_derivative": ("const double dx = delta_softplus ? dDelta / (1.0 + exp(-x)) : dDelta;",
+                                   "const double dx = dDelta;"),
+    "bwd_dB_without_delta": ("dB[b * N * L + n * L + t] += g[n] * dl[t] * u[off + t];",
+                             "dB[b * N * L + n * L + t] += g[n] * u[off + t];"),
+    "bwd_dC_uses_previous_state": ("dC[b * N * L + n * L + t] += ds * hs[(t + 1) * N + n];",
+                                   "dC[b * N * L + n * L + t] += ds * hs[t * N + n];"),
+    "bwd_dA_without_delta": ("dA[d * N + n] += dabar * abar * dl[t];", "dA[d * N + n] += dabar * abar;"),
+    "bwd_silu_derivative_wrong": ("(sig * (1.0 + zz * (1.0 - sig)))", "(sig)"),
     "conv_window_not_shifted": ("for (int64_t k = 0; k + 1 < width; ++k) s[k] = s[k + 1];", ""),
     "conv_taps_reversed": ("acc += w[d * width + k] * s[k];", "acc += w[d * width + (width - 1 - k)] * s[k];"),
     "conv_bias_dropped": ("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
