@@ -188,6 +188,45 @@ selscan_status ssm_scan_fwd_no_alloc(const void* u, const void* delta, const flo
                                      selscan_stream_t stream);
 
 /*
+ * ssm_scan_bwd: gradients of the selective scan (Euler), for training. "A Scan on the Chip"
+ * (world.lapla.si) keeps the expanded state out of main memory in the forward pass and computes
+ * it again in the backward pass ("recomputation"); this call does the same: it stores the state
+ * only every 16 tokens (in the workspace), recomputes each 16-token chunk's states on chip and
+ * runs the adjoint recurrence of the scan backwards through them.
+ *
+ * With out, final_state the results of ssm_scan_fwd on the same inputs (Euler, no ZOH), it
+ * returns the gradients of  sum(dout * out) + sum(dfinal_state * final_state)  with respect to
+ * every input:
+ *   du, ddelta, dz        (batch, dim, seqlen)     grad_dtype (like dout)
+ *   dA                    (dim, dstate)            fp32, summed over batch and tokens
+ *   dB, dC                (batch, dstate, seqlen)  fp32, summed over channels
+ *   dD, ddelta_bias       (dim)                    fp32, NULL = not computed
+ *   dinitial_state        (batch, dim, dstate)     fp32, NULL = not computed
+ * Inputs u, delta, A, B, C, D, z, delta_bias, initial_state, delta_softplus: as ssm_scan_fwd
+ * (in_dtype). dout (batch, dim, seqlen) in grad_dtype; dfinal_state (batch, dim, dstate) fp32,
+ * NULL = zeros. dz is required exactly when z is given. Every output is overwritten (nothing is
+ * accumulated into); the sums over channels and batches are taken in a fixed order, so results
+ * are bitwise repeatable. SELSCAN_FLAG_ZOH: SELSCAN_ERR_UNSUPPORTED. Outputs must not overlap
+ * inputs, one another or the workspace (SELSCAN_ERR_INVALID_ARG); every pointer 16-byte aligned.
+ *
+ * workspace: at least ssm_scan_bwd_workspace_size() bytes (always > 0: the state every 16
+ * tokens, 4 bytes per (b, d, token), plus per-block partial sums of dB and dC of
+ * 4*batch*32*seqlen bytes per 32 channels). Its contents on entry do not matter.
+ */
+selscan_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                            const void* C, const float* D, const void* z,
+                            const float* delta_bias, int delta_softplus,
+                            const float* initial_state, const void* dout,
+                            const float* dfinal_state, void* du, void* ddelta, float* dA,
+                            float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+                            float* dinitial_state, int64_t batch, int64_t dim, int64_t dstate,
+                            int64_t seqlen, selscan_dtype in_dtype, selscan_dtype grad_dtype,
+                            void* workspace, size_t workspace_bytes, selscan_stream_t stream);
+
+/* Workspace bytes ssm_scan_bwd needs for this shape (0 for invalid shapes). */
+size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
+
+/*
  * selscan_device_status: errors that kernels of this library detected on the device.
  *
  * Every wait inside a kernel (for a TMA copy of B / C to land in shared memory) is bounded

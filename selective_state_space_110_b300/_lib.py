@@ -29,7 +29,7 @@ STATUS = {
 # Every symbol include/selscan.h declares.
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selscan_status_string",
            "ssm_scan_fwd_no_alloc", "selscan_device_status", "selscan_selftest_wait_timeout",
-           "ssm_conv_state_update")
+           "ssm_conv_state_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size")
 
 # Size of the fixed scratch array behind ssm_scan_fwd_no_alloc (SELSCAN_NO_ALLOC_SCRATCH_BYTES).
 NO_ALLOC_SCRATCH_BYTES = 524288
@@ -65,6 +65,11 @@ def load() -> ctypes.CDLL:
     lib.ssm_conv_state_update.argtypes = ([_VP] * 4 + [ctypes.c_int, _I64] + [_VP] * 9 +
                                           [_VP, ctypes.c_int] + [_I64] * 3 +
                                           [ctypes.c_int, ctypes.c_int, _VP])
+    lib.ssm_scan_bwd.restype = ctypes.c_int
+    lib.ssm_scan_bwd.argtypes = ([_VP] * 8 + [ctypes.c_int] + [_VP] * 12 + [_I64] * 4 +
+                                 [ctypes.c_int, ctypes.c_int, _VP, ctypes.c_size_t, _VP])
+    lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.ssm_scan_bwd_workspace_size.argtypes = [_I64] * 4
     lib.selscan_device_status.restype = ctypes.c_int
     lib.selscan_device_status.argtypes = [ctypes.c_int, _VP]
     lib.selscan_selftest_wait_timeout.restype = ctypes.c_int

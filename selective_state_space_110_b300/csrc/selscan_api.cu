@@ -300,3 +300,95 @@ SELSCAN_EXPORT selscan_status ssm_conv_state_update(
                                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
 }
+
+namespace {
+size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen) {
+    return selscan::scan_bwd_workspace_floats(batch, dim, seqlen, nullptr, nullptr, nullptr,
+                                              nullptr) * sizeof(float);
+}
+}  // namespace
+
+SELSCAN_EXPORT size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
+                                                  int64_t seqlen) {
+    if (!shape_ok(batch, dim, seqlen) || dstate != kStateN) return 0;
+    return bwd_workspace_bytes(batch, dim, seqlen);
+}
+
+SELSCAN_EXPORT selscan_status ssm_scan_bwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const float* initial_state, const void* dout, const float* dfinal_state, void* du,
+    void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+    float* dinitial_state, int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    selscan_dtype in_dtype, selscan_dtype grad_dtype, void* workspace, size_t workspace_bytes,
+    selscan_stream_t stream) {
+    if (dstate != kStateN || !dtype_ok(in_dtype) || !dtype_ok(grad_dtype))
+        return SELSCAN_ERR_UNSUPPORTED;
+    if (delta_softplus & SELSCAN_FLAG_ZOH) return SELSCAN_ERR_UNSUPPORTED;
+    if (!shape_ok(batch, dim, seqlen) || (delta_softplus & ~kKnownFlags)) return SELSCAN_ERR_INVALID_ARG;
+    const bool has_tokens = seqlen > 0;
+    if (!A || !dA) return SELSCAN_ERR_INVALID_ARG;
+    if (has_tokens && (!u || !delta || !B || !C || !dout || !du || !ddelta || !dB || !dC))
+        return SELSCAN_ERR_INVALID_ARG;
+    if (has_tokens && (z != nullptr) != (dz != nullptr)) return SELSCAN_ERR_INVALID_ARG;
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, initial_state, dout,
+                          dfinal_state, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
+                          dinitial_state, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
+
+    const size_t ein = dtype_size(in_dtype), eg = dtype_size(grad_dtype);
+    const size_t act = (size_t)batch * (size_t)dim * (size_t)seqlen;
+    const size_t bc = (size_t)batch * kStateN * (size_t)seqlen;
+    const size_t st = (size_t)batch * (size_t)dim * kStateN * sizeof(float);
+    const size_t dvec = (size_t)dim * 4;
+    const Range in_r[] = {range_of(u, act * ein), range_of(delta, act * ein),
+                          range_of(A, (size_t)dim * kStateN * 4), range_of(B, bc * ein),
+                          range_of(C, bc * ein), range_of(D, D ? dvec : 0),
+                          range_of(z, z ? act * ein : 0),
+                          range_of(delta_bias, delta_bias ? dvec : 0),
+                          range_of(initial_state, initial_state ? st : 0),
+                          range_of(dout, act * eg),
+                          range_of(dfinal_state, dfinal_state ? st : 0)};
+    const size_t ws_need = bwd_workspace_bytes(batch, dim, seqlen);
+    const Range out_r[] = {range_of(du, has_tokens ? act * eg : 0),
+                           range_of(ddelta, has_tokens ? act * eg : 0),
+                           range_of(dz, dz && has_tokens ? act * eg : 0),
+                           range_of(dA, (size_t)dim * kStateN * 4),
+                           range_of(dB, has_tokens ? bc * 4 : 0),
+                           range_of(dC, has_tokens ? bc * 4 : 0),
+                           range_of(dD, dD ? dvec : 0),
+                           range_of(ddelta_bias, ddelta_bias ? dvec : 0),
+                           range_of(dinitial_state, dinitial_state ? st : 0),
+                           range_of(workspace, ws_need)};
+    constexpr size_t kOuts = sizeof(out_r) / sizeof(out_r[0]);
+    for (size_t i = 0; i < kOuts; ++i) {
+        for (const Range& r : in_r)
+            if (overlaps(out_r[i], r)) return SELSCAN_ERR_INVALID_ARG;
+        for (size_t j = i + 1; j < kOuts; ++j)
+            if (overlaps(out_r[i], out_r[j])) return SELSCAN_ERR_INVALID_ARG;
+    }
+    if (ws_need > 0 && (!workspace || workspace_bytes < ws_need)) return SELSCAN_ERR_WORKSPACE;
+
+    int sms = 0;
+    selscan_status s = device_sms(&sms);
+    if (s != SELSCAN_OK) return s;
+
+    int64_t off_part = 0, off_dA = 0, off_dD = 0, off_db = 0;
+    selscan::scan_bwd_workspace_floats(batch, dim, seqlen, &off_part, &off_dA, &off_dD, &off_db);
+    float* ws = static_cast<float*>(workspace);
+    selscan::BwdArgs a{};
+    a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.delta_bias = delta_bias; a.initial_state = initial_state; a.dout = dout;
+    a.dfinal_state = dfinal_state; a.du = du; a.ddelta = ddelta; a.dz = z ? dz : nullptr;
+    a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.ddelta_bias = ddelta_bias;
+    a.dinitial_state = dinitial_state;
+    a.ws_ckpt = ws; a.ws_part = ws + off_part; a.ws_dA = ws + off_dA; a.ws_dD = ws + off_dD;
+    a.ws_db = ws + off_db;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen;
+    a.softplus = (delta_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
+    cudaError_t e = selscan::launch_scan_bwd(a, in_dtype == SELSCAN_BF16,
+                                             grad_dtype == SELSCAN_BF16,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}

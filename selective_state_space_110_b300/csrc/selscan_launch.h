@@ -71,4 +71,42 @@ struct UpdateArgs {
 cudaError_t launch_state_update(const UpdateArgs& a, bool in_bf16, bool out_bf16,
                                 cudaStream_t stream);
 
+struct BwdArgs {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    const float* initial_state;
+    const void* dout;           // gradient dtype
+    const float* dfinal_state;  // NULL = 0
+    void* du;                   // gradient dtype
+    void* ddelta;
+    void* dz;                   // NULL iff z is NULL
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dD;                  // NULL = not written
+    float* ddelta_bias;         // NULL = not written
+    float* dinitial_state;      // NULL = not written
+    float* ws_ckpt;  // (batch*dim, chunks, 16): the state before every chunk
+    float* ws_part;  // (channel blocks, batch, 32, seqlen): per-CTA sums of dB | dC
+    float* ws_dA;    // (batch*dim, 16) per-row sums
+    float* ws_dD;    // (batch*dim)
+    float* ws_db;    // (batch*dim)
+    int64_t batch;
+    int64_t dim;
+    int64_t seqlen;
+    int softplus;
+};
+
+// Workspace of the backward in floats; the offsets of its parts (the checkpoints start at 0).
+size_t scan_bwd_workspace_floats(int64_t batch, int64_t dim, int64_t seqlen, int64_t* off_part,
+                                 int64_t* off_dA, int64_t* off_dD, int64_t* off_db);
+// Launches the backward kernel and the reduction of its partial sums on `stream`.
+cudaError_t launch_scan_bwd(const BwdArgs& a, bool in_bf16, bool grad_bf16, cudaStream_t stream);
+
 }  // namespace selscan

@@ -1,4 +1,4 @@
-"""Torch-facing wrappers of the two libselscan entry points.
+"""Torch-facing wrappers of the libselscan entry points.
 
 torch provides device memory and the current stream; the library does all of the work.
 Shapes and layouts follow include/selscan.h:
@@ -212,3 +212,68 @@ def ssm_conv_state_update(conv_state, x, conv_weight, conv_bias=None, conv_silu=
             _DT[in_dt], odt, _stream_handle(stream))
     _lib.check("ssm_conv_state_update", st)
     return out, conv_out
+
+
+def bwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
+    """Bytes of workspace ssm_scan_bwd needs."""
+    return int(_lib.lib().ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen))
+
+
+def ssm_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 initial_state=None, dout=None, dfinal_state=None, workspace=None, stream=None):
+    """Gradients of sum(dout*out) + sum(dfinal_state*final_state) of ssm_scan_fwd (Euler) with
+    respect to its inputs. dout (batch, dim, seqlen) sets the dtype of du, ddelta and dz; the
+    other gradients are fp32. Returns a dict with keys du, ddelta, dA, dB, dC, dD, dz,
+    ddelta_bias, dinitial_state (None where the matching input is None)."""
+    if u.dim() != 3:
+        raise ValueError("u must be (batch, dim, seqlen)")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise ValueError(f"unsupported input dtype {in_dt}")
+    if dout is None:
+        raise ValueError("dout is required")
+    g_dt = dout.dtype
+    if g_dt not in _DT:
+        raise ValueError(f"unsupported gradient dtype {g_dt}")
+    dev = u.device
+    act = (batch, dim, seqlen)
+    _check_dev("u", u, in_dt, act, dev)
+    _check_dev("delta", delta, in_dt, act, dev)
+    _check_dev("A", A, torch.float32, (dim, dstate), dev)
+    _check_dev("B", B, in_dt, (batch, dstate, seqlen), dev)
+    _check_dev("C", C, in_dt, (batch, dstate, seqlen), dev)
+    _check_dev("D", D, torch.float32, (dim,), dev)
+    _check_dev("z", z, in_dt, act, dev)
+    _check_dev("delta_bias", delta_bias, torch.float32, (dim,), dev)
+    _check_dev("initial_state", initial_state, torch.float32, (batch, dim, dstate), dev)
+    _check_dev("dout", dout, g_dt, act, dev)
+    _check_dev("dfinal_state", dfinal_state, torch.float32, (batch, dim, dstate), dev)
+    f32 = torch.float32
+    g = {
+        "du": torch.empty(act, dtype=g_dt, device=dev),
+        "ddelta": torch.empty(act, dtype=g_dt, device=dev),
+        "dA": torch.empty((dim, dstate), dtype=f32, device=dev),
+        "dB": torch.empty((batch, dstate, seqlen), dtype=f32, device=dev),
+        "dC": torch.empty((batch, dstate, seqlen), dtype=f32, device=dev),
+        "dD": None if D is None else torch.empty(dim, dtype=f32, device=dev),
+        "dz": None if z is None else torch.empty(act, dtype=g_dt, device=dev),
+        "ddelta_bias": None if delta_bias is None else torch.empty(dim, dtype=f32, device=dev),
+        "dinitial_state": (None if initial_state is None
+                           else torch.empty((batch, dim, dstate), dtype=f32, device=dev)),
+    }
+    with torch.cuda.device(dev):
+        need = bwd_workspace_size(batch, dim, dstate, seqlen)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _check_dev("workspace", workspace, None, None, dev)
+        st = _lib.lib().ssm_scan_bwd(
+            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            _flags(delta_softplus, False), _ptr(initial_state), _ptr(dout), _ptr(dfinal_state),
+            _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+            _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dinitial_state"]),
+            batch, dim, dstate, seqlen, _DT[in_dt], _DT[g_dt], _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _lib.check("ssm_scan_bwd", st)
+    return g

@@ -181,3 +181,52 @@ def test_conv_update_valid_args_reach_the_device_check(lib):
         pytest.skip("device present: covered by the GPU tests")
     assert call_conv(lib) == CUDA
     assert call_conv(lib, state=None, dt=None, A=None, B=None, C=None, out=None) == CUDA
+
+
+def call_bwd(lib, **kw):
+    a = dict(u=fake(0), delta=fake(1), A=fake(2), B=fake(3), C=fake(4), D=fake(5), z=fake(6),
+             delta_bias=fake(7), flags=1, h0=fake(8), dout=fake(9), dfinal=fake(10), du=fake(11),
+             ddelta=fake(12), dA=fake(13), dB=fake(14), dC=fake(15), dD=fake(16), dz=fake(17),
+             dbias=fake(18), dh0=fake(19), batch=2, dim=64, dstate=16, seqlen=128,
+             in_dtype=_lib.BF16, g_dtype=_lib.BF16, ws=fake(20), ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.ssm_scan_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                            a["delta_bias"], a["flags"], a["h0"], a["dout"], a["dfinal"], a["du"],
+                            a["ddelta"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["dbias"],
+                            a["dh0"], a["batch"], a["dim"], a["dstate"], a["seqlen"],
+                            a["in_dtype"], a["g_dtype"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dstate=8), UNSUP),
+    (dict(g_dtype=5), UNSUP),
+    (dict(flags=3), UNSUP),                   # zero-order hold has no backward
+    (dict(flags=4), INVALID),
+    (dict(batch=0), INVALID),
+    (dict(dout=None), INVALID),
+    (dict(du=None), INVALID),
+    (dict(dA=None), INVALID),
+    (dict(dB=None), INVALID),
+    (dict(dz=None), INVALID),                 # z given without dz
+    (dict(z=None), INVALID),                  # dz given without z
+    (dict(dC=fake(14) + 64), INVALID),        # dC inside dB
+    (dict(du=fake(0) + 32), INVALID),         # du inside u
+    (dict(ws=fake(13)), INVALID),             # workspace over dA
+    (dict(ws=None, ws_bytes=0), WS),
+    (dict(ws_bytes=1024), WS),
+    (dict(dout=fake(9) + 8), ALIGN),
+])
+def test_bwd_rejects(lib, kw, expect):
+    assert call_bwd(lib, **kw) == expect
+
+
+def test_bwd_valid_args_reach_the_device_check(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("device present: covered by the GPU tests")
+    assert call_bwd(lib) == CUDA
+    assert call_bwd(lib, z=None, dz=None, D=None, dD=None, h0=None, dh0=None, dfinal=None) == CUDA
+    # workspace: the state every 16 tokens plus per-32-channel partial sums of dB | dC
+    need = lib.ssm_scan_bwd_workspace_size(2, 64, 16, 128)
+    assert need >= 4 * (2 * 64 * 8 * 16 + 2 * 2 * 32 * 128)
+    assert lib.ssm_scan_bwd_workspace_size(2, 64, 8, 128) == 0
