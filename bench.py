@@ -36,6 +36,7 @@ from workloads import make_decode_tokens, make_scan_inputs, scan_config  # noqa:
 METRIC = "selective-scan B·D·L elem/s & achieved HBM GB/s (% of peak); decode steps/s"
 SM_PER_GPU_FALLBACK = 148
 ALU_ELEM_PER_CLK_PER_SM = 2.0  # 16 SFU exp2 (32/clk/SM) and 64 FP32 lane-ops (128/clk/SM) per element
+BWD_ELEM_PER_CLK_PER_SM = 32.0 / 48.0  # backward: 48 SFU exp2 per element at 32/clk/SM
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -207,6 +208,35 @@ def time_scan(cfg, steps, warmup, x, flush, stream, soak_s=1.0):
     return times, launches_per_step
 
 
+def time_bwd(cfg, steps, warmup, x, flush, stream):
+    """ssm_scan_bwd on the same workload (gradients of every input for a random bf16 dout),
+    L2 flushed before every step. Returns per-step times (ms) and launches per step."""
+    from selective_state_space_110_b300 import bwd_workspace_size, ssm_scan_bwd
+    gen = torch.Generator("cuda").manual_seed(cfg.seed + 7)
+    dout = torch.randn(cfg.batch, cfg.dim, cfg.seqlen, generator=gen, device="cuda").to(torch.bfloat16)
+    ws = torch.empty(bwd_workspace_size(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen),
+                     dtype=torch.uint8, device="cuda")
+
+    def call():
+        ssm_scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                     x["delta_softplus"], dout=dout, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.fill_(1)
+            call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            flush.fill_(1)
+            ev[s][0].record(stream)
+            call()
+            ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev], 2
+
+
 def time_scan_e2e(cfg, steps, warmup, x, stream):
     """Same scan through the public API from pinned host buffers: every step copies the
     step's inputs host->device, runs the scan and copies y and the final state back."""
@@ -360,6 +390,8 @@ def run_ours(args):
     value = elems / (ms_step * 1e-3)
     clocks = clk.summary()
 
+    bwd_times, bwd_launches = time_bwd(cfg, max(3, min(args.steps, 10)), 3, x, flush, stream)
+    bwd_ms = max_over_ranks(statistics.median(bwd_times), world)
     e2e_ms, h2d, d2h = time_scan_e2e(cfg, max(2, min(args.steps, 10)), 2, x, stream)
     e2e_ms = max_over_ranks(e2e_ms, world)
     dec, dec_conv = {}, {}
@@ -413,6 +445,16 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
+        "backward": {"what": "ssm_scan_bwd: all input gradients, state every 16 tokens, "
+                             "chunks recomputed (scan_bwd_kernel + scan_bwd_reduce_kernel)",
+                     "ms_per_step": round(bwd_ms, 4),
+                     "elem_per_s": round(elems / (bwd_ms * 1e-3), 1),
+                     "vs_forward_time": round(bwd_ms / kern_ms, 2),
+                     "alu_frac": round(elems / (bwd_ms * 1e-3) /
+                                       (BWD_ELEM_PER_CLK_PER_SM * sms * sm_mhz * 1e6), 4),
+                     "alu_note": f"ceiling {BWD_ELEM_PER_CLK_PER_SM:.3f} elem/clk/SM: 48 SFU exp2 "
+                                 "per element (3 passes x 16 states) at 32 per clock per SM",
+                     "launches_per_step": bwd_launches},
         "decode": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim, **dec},
         "decode_conv": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim,
                         "what": "ssm_conv_state_update: width-4 convolution step + state update",
@@ -424,11 +466,22 @@ def run_ours(args):
 
 
 def run_profile(args):
-    """One scan of the workload (plus one decode layer-step at batch 64): a small, bounded
-    program for ncu captures."""
+    """One scan of the workload (plus one decode layer-step at batch 64), or with
+    --profile-op bwd two backward calls: a small, bounded program for ncu captures."""
     from selective_state_space_110_b300 import ssm_scan_fwd, ssm_state_update
     cfg = scan_config(args.workload)
     x = make_scan_inputs(cfg, "cuda")
+    if args.profile_op == "bwd":
+        from selective_state_space_110_b300 import ssm_scan_bwd
+        gen = torch.Generator("cuda").manual_seed(cfg.seed + 7)
+        dout = torch.randn(cfg.batch, cfg.dim, cfg.seqlen, generator=gen, device="cuda").to(torch.bfloat16)
+        for _ in range(2):
+            g = ssm_scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                             x["delta_bias"], x["delta_softplus"], dout=dout)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": cfg.name, "op": "bwd",
+                          "finite": bool(torch.isfinite(g["du"]).all().item())}))
+        return
     out, fin = ssm_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
                             x["delta_bias"], x["delta_softplus"])
     p = make_decode_layer_params(DECODE_CONFIG, "cuda")
@@ -494,6 +547,8 @@ def main():
                     help="untimed back-to-back scans before the timed steps (clock sampling)")
     ap.add_argument("--profile", action="store_true",
                     help="run one scan of the workload and exit (for ncu captures)")
+    ap.add_argument("--profile-op", default="fwd", choices=["fwd", "bwd"],
+                    help="with --profile: the forward scan (default) or the backward")
     args = ap.parse_args()
     if args.profile:
         run_profile(args)

@@ -10,14 +10,19 @@
 //   dk_t = sum_n g_t B_t,   dDelta_t = sum_n g_t h_{t-1} Abar_t A + dk_t u_t
 //   du_t = dk_t Delta_t + ds_t D,   ddelta_t = dDelta_t * sigmoid(delta_t + bias) (softplus)
 //   dA += g h_{t-1} Abar Delta,  dD += ds u,  dbias += ddelta,  dB_t += g k,  dC_t += ds h_t
-// Layout as in the forward: a quad of 4 lanes per channel, lane g holding states 4g..4g+3; a CTA
-// holds 32 channels of one batch. Lane g owns tokens 4g..4g+3 of each 16-token chunk (loads,
-// per-token gradients); per-token values reach the quad by width-4 shuffles.
 //
-// dB and dC are sums over every channel of a batch and dA, dD, dbias over every batch: each
-// CTA writes its partial sums (dB/dC per token after reducing its 32 channels, dA/dD/dbias per
-// channel) to the workspace and a second kernel adds them in a fixed order, so the gradients
-// are deterministic (no atomics).
+// Layout as in the forward: a quad of 4 lanes per channel, lane g holding states 4g..4g+3; a CTA
+// holds 32 channels of one batch. Lane g owns tokens 4g..4g+3 of each 16-token chunk: it loads
+// their inputs, computes their per-token values and writes their gradients; the quad gets
+// per-token values by width-4 shuffles. The inputs of the next chunk are loaded into registers
+// while the current chunk computes. B and C of a chunk are staged in shared memory one row per
+// token (BcStage).
+//
+// dB and dC are sums over every channel of a batch: each warp reduce-scatters its 8 rows' terms
+// in three shuffle rounds (lane (q, g) ends with one of the 32 dB | dC sums of the token), the
+// CTA adds its 4 warps in shared memory and writes one partial per token and value. dA, dD and
+// dbias are kept per (batch, channel). A second kernel adds the partials in a fixed order, so
+// the gradients are deterministic (no atomics).
 #include "selscan_device.cuh"
 #include "selscan_launch.h"
 
@@ -28,12 +33,12 @@ constexpr int kBWarps = 4;
 constexpr int kBThreads = 32 * kBWarps;     // 128: 32 channels
 constexpr int kBRows = 32;                  // channels per CTA
 constexpr int kBSlots = 32;                 // dB[0..15], dC[0..15] per token
+constexpr int kBMinCtas = 5;                // CTAs per SM the kernel is built to fit
 
 struct BwdSmem {
-    float bc[kBChunk][32];                        // fp32 B | C of the chunk per token
-    float4 H[kBWarps][kBChunk][32];               // recomputed states h_t of the chunk
-    float X[kBWarps][8][kBSlots];                 // per-token transpose for the channel sums
-    float P[kBWarps][kBChunk][kBSlots];           // warp sums of dB/dC per token
+    float bc[2][kBChunk][32];                // B | C per token (layout: BcStage)
+    float4 H[kBWarps][kBChunk][32];          // recomputed states h_t of the chunk
+    float P[kBWarps][kBChunk][kBSlots];      // warp sums of dB | dC per token
 };
 
 template <typename Tin>
@@ -44,8 +49,117 @@ __device__ __forceinline__ float sigmoid_f(float x) {
     return kPrecise ? 1.f / (1.f + expf(-x)) : rcp_approx(1.f + ex2_approx(-x * kLog2e));
 }
 
-template <typename Tin, typename Tg, bool kPrecise>
-__global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(const BwdArgs a) {
+// Four consecutive tokens t..t+3 of one row; zeros from token n on. kVec: one 8-byte (bf16)
+// or 16-byte (fp32) load, which needs seqlen % 4 == 0 (t is a multiple of 4).
+template <typename T, bool kVec>
+struct Quad4;
+template <bool kVec>
+struct Quad4<__nv_bfloat16, kVec> {
+    uint2 r;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p, int64_t t, int64_t n) {
+        if (kVec) {
+            r = t < n ? __ldg(reinterpret_cast<const uint2*>(p + t)) : make_uint2(0u, 0u);
+        } else {
+            const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
+            const uint32_t v0 = t < n ? q[t] : 0u, v1 = t + 1 < n ? q[t + 1] : 0u;
+            const uint32_t v2 = t + 2 < n ? q[t + 2] : 0u, v3 = t + 3 < n ? q[t + 3] : 0u;
+            r = make_uint2(v0 | (v1 << 16), v2 | (v3 << 16));
+        }
+    }
+    __device__ __forceinline__ float get(int i) const {
+        return i == 0 ? bf16lo(r.x) : i == 1 ? bf16hi(r.x) : i == 2 ? bf16lo(r.y) : bf16hi(r.y);
+    }
+};
+template <bool kVec>
+struct Quad4<float, kVec> {
+    float4 r;
+    __device__ __forceinline__ void load(const float* p, int64_t t, int64_t n) {
+        if (kVec) {
+            r = t < n ? __ldg(reinterpret_cast<const float4*>(p + t)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            r.x = t < n ? p[t] : 0.f;
+            r.y = t + 1 < n ? p[t + 1] : 0.f;
+            r.z = t + 2 < n ? p[t + 2] : 0.f;
+            r.w = t + 3 < n ? p[t + 3] : 0.f;
+        }
+    }
+    __device__ __forceinline__ float get(int i) const {
+        return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
+    }
+};
+
+// Stores four consecutive values of one row at t..t+3, those before token n only.
+template <typename T, bool kVec>
+__device__ __forceinline__ void store4(T* p, int64_t t, int64_t n, const float (&v)[4]) {
+    if (t >= n) return;
+    if (kVec) {
+        if constexpr (sizeof(T) == 2) {
+            uint2 w;
+            w.x = (uint32_t)__bfloat16_as_ushort(from_f32<T>(v[0])) |
+                  ((uint32_t)__bfloat16_as_ushort(from_f32<T>(v[1])) << 16);
+            w.y = (uint32_t)__bfloat16_as_ushort(from_f32<T>(v[2])) |
+                  ((uint32_t)__bfloat16_as_ushort(from_f32<T>(v[3])) << 16);
+            *reinterpret_cast<uint2*>(p + t) = w;
+        } else {
+            *reinterpret_cast<float4*>(p + t) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (t + i < n) p[t + i] = from_f32<T>(v[i]);
+    }
+}
+
+// B | C of one chunk in shared memory, one row per token.
+// fp32 inputs: 8 granules of 4 floats per row (0..3 = B states 4q.., 4..7 = C), granule index
+// XOR-swizzled by (token & 7). bf16 inputs, kept as bf16 (lossless): 4 granules of 16 bytes per
+// row, granule q = {B 4q..4q+3, C 4q..4q+3}, so a lane gets its B and C values with one 16-byte
+// load; granule index XOR-swizzled by ((token >> 1) & 3). Both swizzles keep the staging stores
+// free of bank conflicts.
+template <typename Tin>
+struct BcStage;
+template <>
+struct BcStage<float> {
+    static __device__ __forceinline__ int off(int tt, int gr) { return tt * 32 + 4 * (gr ^ (tt & 7)); }
+    // Staging thread: 4 values of granule ch (0..3 B, 4..7 C) of token tt.
+    static __device__ __forceinline__ void put(float* base, int tt, int ch, const float (&v)[4]) {
+        *reinterpret_cast<float4*>(base + off(tt, ch)) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    static __device__ __forceinline__ float4 get_b(const float* base, int t, int g) {
+        return *reinterpret_cast<const float4*>(base + off(t, g));
+    }
+    static __device__ __forceinline__ void get_bc(const float* base, int t, int g, float4& b, float4& c) {
+        b = *reinterpret_cast<const float4*>(base + off(t, g));
+        c = *reinterpret_cast<const float4*>(base + off(t, 4 + g));
+    }
+};
+template <>
+struct BcStage<__nv_bfloat16> {
+    static __device__ __forceinline__ int off(int tt, int q) {  // in 32-bit words
+        return tt * 16 + 4 * (q ^ ((tt >> 1) & 3));
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+    }
+    static __device__ __forceinline__ void put(float* base, int tt, int ch, const float (&v)[4]) {
+        // v holds bf16 values widened to fp32: narrowing them back is exact.
+        uint32_t* w = reinterpret_cast<uint32_t*>(base) + off(tt, ch & 3) + 2 * (ch >> 2);
+        *reinterpret_cast<uint2*>(w) = make_uint2(pack(v[0], v[1]), pack(v[2], v[3]));
+    }
+    static __device__ __forceinline__ float4 get_b(const float* base, int t, int g) {
+        const uint2 r = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint32_t*>(base) + off(t, g));
+        return make_float4(bf16lo(r.x), bf16hi(r.x), bf16lo(r.y), bf16hi(r.y));
+    }
+    static __device__ __forceinline__ void get_bc(const float* base, int t, int g, float4& b, float4& c) {
+        const uint4 r = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(base) + off(t, g));
+        b = make_float4(bf16lo(r.x), bf16hi(r.x), bf16lo(r.y), bf16hi(r.y));
+        c = make_float4(bf16lo(r.z), bf16hi(r.z), bf16lo(r.w), bf16hi(r.w));
+    }
+};
+
+template <typename Tin, typename Tg, bool kPrecise, bool kVec>
+__global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const BwdArgs a) {
     __shared__ __align__(16) BwdSmem sm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = lane >> 2, g = lane & 3;
@@ -55,230 +169,261 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(const BwdArgs a) {
     const int64_t d = active ? d_raw : 0;
     const int64_t row = b * a.dim + d;
     const int64_t L = a.seqlen;
+    const int64_t Lr = active ? L : 0;  // tokens of this lane's row (none past dim)
     const int nchunks = (int)((L + kBChunk - 1) / kBChunk);
 
-    // Per-lane constants: A (natural units) and A*log2(e) for the SFU.
-    const float4 An = *reinterpret_cast<const float4*>(a.A + d * kN + 4 * g);
-    const float Av[4] = {An.x, An.y, An.z, An.w};
-    float A2[4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) A2[n] = Av[n] * kLog2e;
+    const float4 A4 = *reinterpret_cast<const float4*>(a.A + d * kN + 4 * g);
+    const float Av[4] = {A4.x, A4.y, A4.z, A4.w};
     const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
     const float Dd = a.D ? a.D[d] : 0.f;
+    // Per-token steps are kept as Delta * kScale: the SFU path takes exp(Delta A) as
+    // 2^(Delta log2(e) A).
+    constexpr float kScale = kPrecise ? 1.f : kLog2e;
 
     const Tin* u_row = static_cast<const Tin*>(a.u) + row * L;
     const Tin* d_row = static_cast<const Tin*>(a.delta) + row * L;
     const Tin* z_row = a.z ? static_cast<const Tin*>(a.z) + row * L : nullptr;
     const Tg* o_row = static_cast<const Tg*>(a.dout) + row * L;
-    const Tin* Bb = static_cast<const Tin*>(a.B) + b * kN * L;
-    const Tin* Cb = static_cast<const Tin*>(a.C) + b * kN * L;
     float* ckpt = a.ws_ckpt + (row * nchunks) * kN + 4 * g;
 
-    // Decay factor of state n over a step with Delta: exp(Delta*A).
-    auto decay = [&](float dt, int n) -> float {
-        return kPrecise ? expf(dt * Av[n]) : ex2_approx(dt * A2[n]);
+    // B | C staging: thread -> token s_tt of the chunk, granule s_ch (0..3 B, 4..7 C).
+    const int s_tt = tid & 15, s_ch = tid >> 4;
+    const Tin* s_src = (s_ch < 4 ? static_cast<const Tin*>(a.B) : static_cast<const Tin*>(a.C)) +
+                       b * kN * L + (int64_t)(4 * (s_ch & 3)) * L;
+    float sb[4];
+    auto fetch_bc = [&](int c, bool withC) {
+        const int64_t t = (int64_t)c * kBChunk + s_tt;
+        const bool ok = t < L && (withC || s_ch < 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sb[j] = ok ? ld1(s_src + j * L + t) : 0.f;
+    };
+    using Stage = BcStage<Tin>;
+    auto put_bc = [&](int buf, bool withC) {
+        if (withC || s_ch < 4) Stage::put(&sm.bc[buf][0][0], s_tt, s_ch, sb);
+    };
+    auto decay = [&](float s, int n) -> float {  // exp(Delta A_n), s = Delta * kScale
+        return kPrecise ? expf(s * Av[n]) : ex2_approx(s * Av[n]);
     };
     auto delta_of = [&](float x) -> float {
         if (!a.softplus) return x;
         return kPrecise ? softplus_f<true>(x) : softplus2(make_float2(x, x)).x;
-    };
-    // Stage B (and C) of chunk c as fp32 rows per token: thread -> (token, 4 states of B|C).
-    auto stage_bc = [&](int c, bool withC) {
-        const int64_t t0 = (int64_t)c * kBChunk;
-        for (int item = tid; item < kBChunk * 8; item += kBThreads) {
-            const int tt = item % kBChunk, ch = item / kBChunk;  // ch 0..3: B quads, 4..7: C quads
-            if (ch >= 4 && !withC) continue;
-            const Tin* src = ch >= 4 ? Cb : Bb;
-            const int q = ch & 3;
-            const int64_t t = t0 + tt;
-            const bool ok = t < L;
-            float4 v;
-            v.x = ok ? ld1(src + (4 * q + 0) * L + t) : 0.f;
-            v.y = ok ? ld1(src + (4 * q + 1) * L + t) : 0.f;
-            v.z = ok ? ld1(src + (4 * q + 2) * L + t) : 0.f;
-            v.w = ok ? ld1(src + (4 * q + 3) * L + t) : 0.f;
-            *reinterpret_cast<float4*>(&sm.bc[tt][4 * ch]) = v;
-        }
     };
 
     // ---- checkpoint pass: the forward state before every chunk ----
     float h[4];
     {
         float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.initial_state) s0 = *reinterpret_cast<const float4*>(a.initial_state + row * kN + 4 * g);
+        if (a.initial_state && active)
+            s0 = *reinterpret_cast<const float4*>(a.initial_state + row * kN + 4 * g);
         h[0] = s0.x; h[1] = s0.y; h[2] = s0.z; h[3] = s0.w;
     }
-    for (int c = 0; c < nchunks; ++c) {
-        if (active) *reinterpret_cast<float4*>(ckpt + (int64_t)c * kN) = make_float4(h[0], h[1], h[2], h[3]);
-        __syncthreads();
-        stage_bc(c, false);
-        const int64_t tl = (int64_t)c * kBChunk + 4 * g;
-        float dl[4], kl[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const bool ok = active && tl + i < L;
-            const float dt = ok ? delta_of(ld1(d_row + tl + i) + bias) : 0.f;
-            dl[i] = dt;
-            kl[i] = ok ? dt * ld1(u_row + tl + i) : 0.f;
+    {
+        Quad4<Tin, kVec> pd, pu;
+        if (nchunks > 0) {
+            pd.load(d_row, 4 * g, Lr);
+            pu.load(u_row, 4 * g, Lr);
+            fetch_bc(0, false);
         }
-        __syncthreads();
+        for (int c = 0; c < nchunks; ++c) {
+            const int64_t tl = (int64_t)c * kBChunk + 4 * g;
+            if (active) *reinterpret_cast<float4*>(ckpt + (int64_t)c * kN) = make_float4(h[0], h[1], h[2], h[3]);
+            put_bc(c & 1, false);
+            float dl[4], kl[4];
 #pragma unroll
-        for (int t = 0; t < kBChunk; ++t) {
-            const float dt = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
-            const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
-            const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[t][4 * g]);
-            const float Bs[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+            for (int i = 0; i < 4; ++i) {  // tokens past the end are the identity step
+                const float dt = tl + i < Lr ? delta_of(pd.get(i) + bias) : 0.f;
+                dl[i] = dt * kScale;
+                kl[i] = dt * pu.get(i);
+            }
+            if (c + 1 < nchunks) {
+                pd.load(d_row, tl + kBChunk, Lr);
+                pu.load(u_row, tl + kBChunk, Lr);
+                fetch_bc(c + 1, false);
+            }
+            __syncthreads();  // B of chunk c staged (buffer c & 1)
+            const float* bcb = &sm.bc[c & 1][0][0];
 #pragma unroll
-            for (int n = 0; n < 4; ++n) h[n] = fmaf(decay(dt, n), h[n], k * Bs[n]);
+            for (int t = 0; t < kBChunk; ++t) {
+                const float s = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
+                const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
+                const float4 Bv = Stage::get_b(bcb, t, g);
+                h[0] = fmaf(decay(s, 0), h[0], k * Bv.x);
+                h[1] = fmaf(decay(s, 1), h[1], k * Bv.y);
+                h[2] = fmaf(decay(s, 2), h[2], k * Bv.z);
+                h[3] = fmaf(decay(s, 3), h[3], k * Bv.w);
+            }
         }
     }
+    __syncthreads();  // the last chunk's readers of the staging buffers are done
 
     // ---- reverse pass ----
-    float gad[4];  // adjoint of the state
-    {
-        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.dfinal_state && active)
-            f = *reinterpret_cast<const float4*>(a.dfinal_state + row * kN + 4 * g);
+    float gad[4] = {0.f, 0.f, 0.f, 0.f};  // adjoint of the state
+    if (a.dfinal_state && active) {
+        const float4 f = *reinterpret_cast<const float4*>(a.dfinal_state + row * kN + 4 * g);
         gad[0] = f.x; gad[1] = f.y; gad[2] = f.z; gad[3] = f.w;
     }
     float dA_acc[4] = {0.f, 0.f, 0.f, 0.f};
     float dD_acc = 0.f, db_acc = 0.f;
     Tg* du_row = static_cast<Tg*>(a.du) + row * L;
     Tg* dd_row = static_cast<Tg*>(a.ddelta) + row * L;
-    Tg* dz_row = a.dz ? static_cast<Tg*>(a.dz) + row * L : nullptr;
-    float* part = a.ws_part + ((int64_t)blockIdx.x * a.batch + b) * kBSlots * L;  // [slot][t]
+    Tg* dz_row = a.z ? static_cast<Tg*>(a.dz) + row * L : nullptr;
+    float* part = a.ws_part + ((int64_t)blockIdx.x * a.batch + b) * L * kBSlots;  // [t][slot]
+    // After the reduce-scatter lane (q, g) holds dB of state 4g+q (q < 4) or dC of 4g+q-4.
+    const int my_slot = (quad >> 2) * 16 + 4 * g + (quad & 3);
+    const bool x16 = (lane >> 4) & 1, x8 = (lane >> 3) & 1, x4 = (lane >> 2) & 1;
 
+    Quad4<Tin, kVec> pd, pu, pz;
+    Quad4<Tg, kVec> po;
+    if (nchunks > 0) {
+        const int64_t tl = (int64_t)(nchunks - 1) * kBChunk + 4 * g;
+        pd.load(d_row, tl, Lr);
+        pu.load(u_row, tl, Lr);
+        if (z_row) pz.load(z_row, tl, Lr);
+        po.load(o_row, tl, Lr);
+        fetch_bc(nchunks - 1, true);
+    }
     for (int c = nchunks - 1; c >= 0; --c) {
-        __syncthreads();  // the previous chunk's readers of bc / P are done
-        stage_bc(c, true);
         const int64_t t0 = (int64_t)c * kBChunk;
         const int64_t tl = t0 + 4 * g;
-        // Owned tokens: inputs and per-token values.
-        float dl[4], kl[4], ul[4], xl[4], zl[4], ol[4];
+        float4 hk4 = make_float4(0.f, 0.f, 0.f, 0.f);  // rows past dim run on zeros
+        if (active) hk4 = *reinterpret_cast<const float4*>(ckpt + (int64_t)c * kN);
+        put_bc(0, true);
+        // Owned tokens: per-token values from the prefetched inputs.
+        float dl[4], kl[4], dsl[4], dzf[4], ul[4], sgx[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const bool ok = active && tl + i < L;
-            xl[i] = ok ? ld1(d_row + tl + i) + bias : 0.f;
-            ul[i] = ok ? ld1(u_row + tl + i) : 0.f;
-            zl[i] = ok && z_row ? ld1(z_row + tl + i) : 0.f;
-            ol[i] = ok ? to_f32(o_row[tl + i]) : 0.f;
-            dl[i] = ok ? delta_of(xl[i]) : 0.f;
-            kl[i] = dl[i] * ul[i];
+            const bool ok = tl + i < Lr;
+            const float x = pd.get(i) + bias;
+            const float dt = ok ? delta_of(x) : 0.f;  // tokens past the end: identity step
+            const float u = pu.get(i), o = po.get(i);
+            dl[i] = dt * kScale;
+            kl[i] = dt * u;
+            ul[i] = u;
+            sgx[i] = a.softplus ? sigmoid_f<kPrecise>(x) : 1.f;
+            if (z_row) {
+                const float zv = pz.get(i), sz = sigmoid_f<kPrecise>(zv);
+                dsl[i] = o * zv * sz;
+                dzf[i] = o * sz * (1.f + zv * (1.f - sz));
+            } else {
+                dsl[i] = o;
+                dzf[i] = 0.f;
+            }
         }
-        float hk[4];
-        {
-            // Rows past dim never wrote a checkpoint: they run on zeros.
-            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (active) s0 = *reinterpret_cast<const float4*>(ckpt + (int64_t)c * kN);
-            hk[0] = s0.x; hk[1] = s0.y; hk[2] = s0.z; hk[3] = s0.w;
+        if (c > 0) {
+            pd.load(d_row, tl - kBChunk, Lr);
+            pu.load(u_row, tl - kBChunk, Lr);
+            if (z_row) pz.load(z_row, tl - kBChunk, Lr);
+            po.load(o_row, tl - kBChunk, Lr);
+            fetch_bc(c - 1, true);
         }
-        __syncthreads();
-        // Recompute the chunk's states (kept in shared memory) and the readouts s_t.
-        float sl[4] = {0.f, 0.f, 0.f, 0.f};
+        __syncthreads();  // B | C of the chunk staged
+        const float* bcb = &sm.bc[0][0][0];
+        float4* Hw = &sm.H[warp][0][0];
+
+        // Recompute the chunk's states (into shared memory) and the readouts s_t - D u_t.
+        float sl[4];
         {
-            float hh[4] = {hk[0], hk[1], hk[2], hk[3]};
+            float hh[4] = {hk4.x, hk4.y, hk4.z, hk4.w};
 #pragma unroll
             for (int t = 0; t < kBChunk; ++t) {
-                const float dt = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
+                const float s = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
                 const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
-                const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[t][4 * g]);
-                const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[t][16 + 4 * g]);
-                const float Bs[4] = {Bv.x, Bv.y, Bv.z, Bv.w}, Cs[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
-                float y = 0.f;
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    hh[n] = fmaf(decay(dt, n), hh[n], k * Bs[n]);
-                    y = fmaf(Cs[n], hh[n], y);
-                }
-                sm.H[warp][t][lane] = make_float4(hh[0], hh[1], hh[2], hh[3]);
+                float4 Bv, Cv;
+                Stage::get_bc(bcb, t, g, Bv, Cv);
+                hh[0] = fmaf(decay(s, 0), hh[0], k * Bv.x);
+                hh[1] = fmaf(decay(s, 1), hh[1], k * Bv.y);
+                hh[2] = fmaf(decay(s, 2), hh[2], k * Bv.z);
+                hh[3] = fmaf(decay(s, 3), hh[3], k * Bv.w);
+                Hw[t * 32 + lane] = make_float4(hh[0], hh[1], hh[2], hh[3]);
+                float y = Cv.x * hh[0];
+                y = fmaf(Cv.y, hh[1], y);
+                y = fmaf(Cv.z, hh[2], y);
+                y = fmaf(Cv.w, hh[3], y);
                 y += __shfl_xor_sync(0xffffffffu, y, 1);
                 y += __shfl_xor_sync(0xffffffffu, y, 2);
-                if (g == (t >> 2)) sl[t & 3] = y;  // the owner keeps s_t - D u_t
+                if (g == (t >> 2)) sl[t & 3] = y;
             }
         }
-        // Owner: ds and dz of its tokens.
-        float dsl[4];
+        if (z_row) {
+            float dzv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float s = sl[i] + Dd * ul[i];
-            if (z_row) {
-                const float sig = sigmoid_f<kPrecise>(zl[i]);
-                dsl[i] = ol[i] * zl[i] * sig;
-                const float dzv = ol[i] * s * sig * (1.f + zl[i] * (1.f - sig));
-                if (active && tl + i < L) dz_row[tl + i] = from_f32<Tg>(dzv);
-            } else {
-                dsl[i] = ol[i];
-            }
+            for (int i = 0; i < 4; ++i) dzv[i] = dzf[i] * fmaf(Dd, ul[i], sl[i]);
+            store4<Tg, kVec>(dz_row, tl, Lr, dzv);
         }
         __syncwarp();
+
         // Adjoint recurrence, last token of the chunk first.
         float dkl[4], dal[4];  // owner: dk_t and the Abar part of dDelta_t
+        float4 ht = Hw[(kBChunk - 1) * 32 + lane];
 #pragma unroll
         for (int t = kBChunk - 1; t >= 0; --t) {
-            const float dt = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
+            const float s = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
             const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
             const float ds = __shfl_sync(0xffffffffu, dsl[t & 3], t >> 2, 4);
-            const float4 Bv = *reinterpret_cast<const float4*>(&sm.bc[t][4 * g]);
-            const float4 Cv = *reinterpret_cast<const float4*>(&sm.bc[t][16 + 4 * g]);
+            float4 Bv, Cv;
+            Stage::get_bc(bcb, t, g, Bv, Cv);
+            const float4 hp = t > 0 ? Hw[(t - 1) * 32 + lane] : hk4;
             const float Bs[4] = {Bv.x, Bv.y, Bv.z, Bv.w}, Cs[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
-            const float4 ht = sm.H[warp][t][lane];
-            float4 hp;
-            if (t > 0) hp = sm.H[warp][t - 1][lane];
-            else hp = make_float4(hk[0], hk[1], hk[2], hk[3]);
             const float hts[4] = {ht.x, ht.y, ht.z, ht.w}, hps[4] = {hp.x, hp.y, hp.z, hp.w};
-            float dk = 0.f, da = 0.f, cdb[4], cdc[4];
+            float dk = 0.f, da = 0.f, v[8];
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
                 gad[n] = fmaf(ds, Cs[n], gad[n]);
-                cdc[n] = ds * hts[n];
-                cdb[n] = gad[n] * k;
+                v[4 + n] = ds * hts[n];   // dC term
+                v[n] = gad[n] * k;        // dB term
                 dk = fmaf(gad[n], Bs[n], dk);
-                const float ab = decay(dt, n);
+                const float ab = decay(s, n);
                 const float w = gad[n] * hps[n] * ab;  // dAbar * Abar
                 da = fmaf(w, Av[n], da);
-                dA_acc[n] = fmaf(w, dt, dA_acc[n]);
+                dA_acc[n] = fmaf(w, s, dA_acc[n]);
                 gad[n] *= ab;
             }
+            ht = hp;
             dk += __shfl_xor_sync(0xffffffffu, dk, 1);
             dk += __shfl_xor_sync(0xffffffffu, dk, 2);
             da += __shfl_xor_sync(0xffffffffu, da, 1);
             da += __shfl_xor_sync(0xffffffffu, da, 2);
             if (g == (t >> 2)) { dkl[t & 3] = dk; dal[t & 3] = da; }
-            // Channel sums of this warp's 8 rows for dB_t, dC_t: transpose through shared memory.
-            *reinterpret_cast<float4*>(&sm.X[warp][quad][4 * g]) = make_float4(cdb[0], cdb[1], cdb[2], cdb[3]);
-            *reinterpret_cast<float4*>(&sm.X[warp][quad][16 + 4 * g]) = make_float4(cdc[0], cdc[1], cdc[2], cdc[3]);
-            __syncwarp();
-            float s = 0.f;
+            // Sums of the 8 rows' dB | dC terms, reduce-scattered over lane bits 4, 3, 2.
+            float w4[4], w2[2];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) s += sm.X[warp][q][lane];
-            sm.P[warp][t][lane] = s;
-            __syncwarp();
+            for (int i = 0; i < 4; ++i) {
+                const float send = x16 ? v[i] : v[i + 4], keep = x16 ? v[i + 4] : v[i];
+                w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float send = x8 ? w4[i] : w4[i + 2], keep = x8 ? w4[i + 2] : w4[i];
+                w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+            const float send = x4 ? w2[0] : w2[1], keep = x4 ? w2[1] : w2[0];
+            sm.P[warp][t][my_slot] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
         }
         // Owner: per-token gradients of its tokens.
+        {
+            float duv[4], ddv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const bool ok = active && tl + i < L;
-            const float du = fmaf(dkl[i], dl[i], dsl[i] * Dd);
-            const float dDelta = fmaf(dkl[i], ul[i], dal[i]);
-            const float ddv = a.softplus ? dDelta * sigmoid_f<kPrecise>(xl[i]) : dDelta;
-            if (ok) {
-                du_row[tl + i] = from_f32<Tg>(du);
-                dd_row[tl + i] = from_f32<Tg>(ddv);
-                dD_acc = fmaf(dsl[i], ul[i], dD_acc);
-                db_acc += ddv;
+            for (int i = 0; i < 4; ++i) {
+                duv[i] = fmaf(dkl[i], dl[i] * (1.f / kScale), dsl[i] * Dd);
+                ddv[i] = fmaf(dkl[i], ul[i], dal[i]) * sgx[i];
+                if (tl + i < Lr) {
+                    dD_acc = fmaf(dsl[i], ul[i], dD_acc);
+                    db_acc += ddv[i];
+                }
             }
+            store4<Tg, kVec>(du_row, tl, Lr, duv);
+            store4<Tg, kVec>(dd_row, tl, Lr, ddv);
         }
-        __syncthreads();
-        // CTA sums of dB_t / dC_t over its 4 warps -> partials [slot][t] of this CTA.
-        for (int item = tid; item < kBSlots * kBChunk; item += kBThreads) {
-            const int slot = item / kBChunk, tt = item % kBChunk;
-            const int64_t t = t0 + tt;
-            if (t < L) {
-                float s = 0.f;
+        __syncthreads();  // every warp's dB | dC sums of the chunk are in P
+        // CTA sums of dB_t / dC_t over the 4 warps -> this CTA's partials [t][slot].
 #pragma unroll
-                for (int w = 0; w < kBWarps; ++w) s += sm.P[w][tt][slot];
-                part[(int64_t)slot * L + t] = s;
-            }
+        for (int r = 0; r < kBSlots * kBChunk / kBThreads; ++r) {
+            const int item = tid + r * kBThreads;
+            const int slot = item & 31, tt = item >> 5;
+            const int64_t t = t0 + tt;
+            if (t < L)
+                part[t * kBSlots + slot] = sm.P[0][tt][slot] + sm.P[1][tt][slot] +
+                                           sm.P[2][tt][slot] + sm.P[3][tt][slot];
         }
     }
 
@@ -287,8 +432,9 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(const BwdArgs a) {
         if (a.dinitial_state)
             *reinterpret_cast<float4*>(a.dinitial_state + row * kN + 4 * g) =
                 make_float4(gad[0], gad[1], gad[2], gad[3]);
+        constexpr float sc = 1.f / kScale;  // the dA terms were taken with Delta * kScale
         *reinterpret_cast<float4*>(a.ws_dA + row * kN + 4 * g) =
-            make_float4(dA_acc[0], dA_acc[1], dA_acc[2], dA_acc[3]);
+            make_float4(dA_acc[0] * sc, dA_acc[1] * sc, dA_acc[2] * sc, dA_acc[3] * sc);
     }
     dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 1);
     dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 2);
@@ -304,15 +450,15 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(const BwdArgs a) {
 // dbias over batches.
 __global__ void scan_bwd_reduce_kernel(const BwdArgs a, int64_t nblk) {
     const int64_t L = a.seqlen;
-    const int64_t nbc = a.batch * kBSlots * L;            // dB and dC entries
+    const int64_t nbc = a.batch * L * kBSlots;            // dB and dC entries
     const int64_t nda = a.dim * kN;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbc + nda + 2 * a.dim;
          i += stride) {
-        if (i < nbc) {
-            const int64_t t = i % L, slot = (i / L) % kBSlots, b = i / (L * kBSlots);
+        if (i < nbc) {  // i = (b * L + t) * 32 + slot
+            const int64_t slot = i % kBSlots, t = (i / kBSlots) % L, b = i / (kBSlots * L);
             float s = 0.f;
-            for (int64_t k = 0; k < nblk; ++k) s += a.ws_part[((k * a.batch + b) * kBSlots + slot) * L + t];
+            for (int64_t k = 0; k < nblk; ++k) s += a.ws_part[k * nbc + i];
             float* dst = slot < kN ? a.dB : a.dC;
             dst[(b * kN + (slot % kN)) * L + t] = s;
         } else if (i < nbc + nda) {
@@ -335,7 +481,11 @@ __global__ void scan_bwd_reduce_kernel(const BwdArgs a, int64_t nblk) {
 template <typename Tin, typename Tg, bool kPrecise>
 static cudaError_t launch_bwd_typed(const BwdArgs& a, cudaStream_t stream) {
     const unsigned gx = (unsigned)((a.dim + kBRows - 1) / kBRows);
-    scan_bwd_kernel<Tin, Tg, kPrecise><<<dim3(gx, (unsigned)a.batch), kBThreads, 0, stream>>>(a);
+    const dim3 grid(gx, (unsigned)a.batch);
+    if (a.seqlen % 4 == 0)
+        scan_bwd_kernel<Tin, Tg, kPrecise, true><<<grid, kBThreads, 0, stream>>>(a);
+    else
+        scan_bwd_kernel<Tin, Tg, kPrecise, false><<<grid, kBThreads, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     scan_bwd_reduce_kernel<<<4 * 148, 256, 0, stream>>>(a, (int64_t)gx);
@@ -359,7 +509,7 @@ size_t scan_bwd_workspace_floats(int64_t batch, int64_t dim, int64_t seqlen, int
     const int64_t nblk = (dim + kBRows - 1) / kBRows;
     auto up = [](int64_t x) { return (x + 63) / 64 * 64; };  // 256-byte alignment
     const int64_t ckpt = up(rows * nchunks * kN);
-    const int64_t part = up(nblk * batch * kBSlots * seqlen);
+    const int64_t part = up(nblk * batch * seqlen * kBSlots);
     const int64_t dA = up(rows * kN);
     const int64_t dD = up(rows), db = up(rows);
     if (off_part) *off_part = ckpt;
