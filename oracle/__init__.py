@@ -59,6 +59,8 @@ class Oracle:
         lib.oracle_scan_bwd.argtypes = [_DP] * 8 + [ctypes.c_int] + [_DP] * 12 + [_I64] * 4
         lib.oracle_conv_step.restype = None
         lib.oracle_conv_step.argtypes = [_DP] * 4 + [ctypes.c_int, _DP] + [_I64] * 3
+        lib.oracle_ssd_fwd.restype = None
+        lib.oracle_ssd_fwd.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP, _DP] + [_I64] * 6
         lib.oracle_max_threads.restype = ctypes.c_int
         self._lib = lib
         self.path = path
@@ -156,6 +158,23 @@ class Oracle:
             _p(g["ddelta_bias"]), _p(g["dinitial_state"]), batch, dim, dstate, seqlen)
         return g
 
+    def ssd_fwd(self, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True,
+                initial_state=None):
+        """Mamba-2 SSD layer by its recurrence. x (batch, seqlen, nheads, headdim), dt
+        (batch, seqlen, nheads), A (nheads), B/C (batch, seqlen, ngroups, dstate). Returns
+        (y like x, final_state (batch, nheads, headdim, dstate)) as float64."""
+        x, dt, A, B, C = map(_f64, (x, dt, A, B, C))
+        D, z, dt_bias, initial_state = map(_f64, (D, z, dt_bias, initial_state))
+        batch, seqlen, nheads, headdim = x.shape
+        ngroups, dstate = B.shape[2], B.shape[3]
+        assert nheads % ngroups == 0 and C.shape == B.shape and dt.shape == x.shape[:3]
+        y = np.empty(x.shape, dtype=np.float64)
+        fin = np.empty((batch, nheads, headdim, dstate), dtype=np.float64)
+        self._lib.oracle_ssd_fwd(_p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(z), _p(dt_bias),
+                                 int(bool(dt_softplus)), _p(initial_state), _p(y), _p(fin),
+                                 batch, seqlen, nheads, headdim, ngroups, dstate)
+        return y, fin
+
     def conv_step(self, conv_state, x, weight, bias=None, silu=True):
         """One step of the short causal convolution. Returns (new_conv_state (batch, dim,
         width), u (batch, dim)); inputs untouched."""
@@ -214,3 +233,7 @@ def scan_bwd(*a, **k):
 
 def conv_state_update(*a, **k):
     return default().conv_state_update(*a, **k)
+
+
+def ssd_fwd(*a, **k):
+    return default().ssd_fwd(*a, **k)

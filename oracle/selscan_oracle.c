@@ -257,3 +257,59 @@ void oracle_scan_bwd(const double* u, const double* delta, const double* A, cons
         free(hs); free(dl); free(sg); free(g);
     }
 }
+
+/* ---- Mamba-2 state space duality layer (SSD) ----
+ *
+ * "Mamba and State Space Models" (world.lapla.si), section "Mamba-2": A is one number per head
+ * times the identity, so a head's whole state (headdim x dstate numbers) decays by the same
+ * factor exp(Delta_t * A_h) each token. Row by row the layer is this recurrence, per (b, h):
+ *   Delta_t  = softplus(dt[b,t,h] + dt_bias[h])   (dt + dt_bias with the flag off)
+ *   H_t[p,n] = exp(Delta_t A_h) H_{t-1}[p,n] + Delta_t x[b,t,h,p] B[b,t,g,n]
+ *   y[b,t,h,p] = sum_n C[b,t,g,n] H_t[p,n] + D_h x[b,t,h,p],  then times silu(z[b,t,h,p])
+ * with g = h / (nheads / ngroups) the group whose B and C head h reads. The page's other form,
+ * one lower-triangular matrix per head (entry i, j = C_i . B_j times the decay in between), is
+ * the same map; the tests check the two against each other. Evaluated in double precision,
+ * sequential in t, the readout summed in increasing n; heads are spread over OpenMP threads.
+ *
+ * Layouts (contiguous, row-major):
+ *   x, z, y          (batch, seqlen, nheads, headdim)
+ *   dt               (batch, seqlen, nheads)
+ *   A, D, dt_bias    (nheads)
+ *   B, C             (batch, seqlen, ngroups, dstate)
+ *   initial_state, final_state  (batch, nheads, headdim, dstate)
+ * D, z, dt_bias, initial_state, final_state may be NULL (zero / no gate / zero / not written).
+ */
+void oracle_ssd_fwd(const double* x, const double* dt, const double* A, const double* B,
+                    const double* C, const double* D, const double* z, const double* dt_bias,
+                    int dt_softplus, const double* initial_state, double* y,
+                    double* final_state, int64_t batch, int64_t seqlen, int64_t nheads,
+                    int64_t headdim, int64_t ngroups, int64_t dstate) {
+    const int64_t P = headdim, N = dstate, heads_per_group = nheads / ngroups;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < batch * nheads; ++bh) {
+        const int64_t b = bh / nheads, h = bh % nheads, g = h / heads_per_group;
+        double* H = (double*)malloc(sizeof(double) * (size_t)(P * N));
+        for (int64_t i = 0; i < P * N; ++i) H[i] = initial_state ? initial_state[bh * P * N + i] : 0.0;
+        for (int64_t t = 0; t < seqlen; ++t) {
+            const double xr = dt[(b * seqlen + t) * nheads + h] + (dt_bias ? dt_bias[h] : 0.0);
+            const double dlt = dt_softplus ? softplus(xr) : xr;
+            const double decay = exp(dlt * A[h]);
+            const double* xt = x + ((b * seqlen + t) * nheads + h) * P;
+            const double* Bt = B + ((b * seqlen + t) * ngroups + g) * N;
+            const double* Ct = C + ((b * seqlen + t) * ngroups + g) * N;
+            for (int64_t p = 0; p < P; ++p) {
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    H[p * N + n] = decay * H[p * N + n] + dlt * xt[p] * Bt[n];
+                    acc += Ct[n] * H[p * N + n];
+                }
+                acc += (D ? D[h] : 0.0) * xt[p];
+                if (z) acc *= silu(z[((b * seqlen + t) * nheads + h) * P + p]);
+                y[((b * seqlen + t) * nheads + h) * P + p] = acc;
+            }
+        }
+        if (final_state)
+            for (int64_t i = 0; i < P * N; ++i) final_state[bh * P * N + i] = H[i];
+        free(H);
+    }
+}

@@ -332,6 +332,108 @@ def pin_backward_finite_differences(orc, seed=19, softplus=True, full=True):
     return worst
 
 
+def _ssd_problem(seed, batch=2, seqlen=23, nheads=4, headdim=3, ngroups=2, dstate=5,
+                 full=True):
+    r = _rng(seed)
+    q = {
+        "x": r.standard_normal((batch, seqlen, nheads, headdim)),
+        "dt": r.standard_normal((batch, seqlen, nheads)) * 0.7,
+        "A": -r.uniform(0.5, 4.0, nheads),
+        "B": r.standard_normal((batch, seqlen, ngroups, dstate)),
+        "C": r.standard_normal((batch, seqlen, ngroups, dstate)),
+        "D": r.standard_normal(nheads) if full else None,
+        "z": r.standard_normal((batch, seqlen, nheads, headdim)) if full else None,
+        "dt_bias": r.standard_normal(nheads) * 0.5 if full else None,
+        "h0": r.standard_normal((batch, nheads, headdim, dstate)) if full else None,
+    }
+    return q
+
+
+def ssd_matrix_form(q, softplus=True):
+    """'Mamba-2' (world.lapla.si): the layer as one lower-triangular matrix per head, entry
+    (i, j) = C_i . B_j times all the decay in between, applied to the Delta-scaled input; plus
+    the initial state carried to every step and read by C_i. The decay from step j to step i
+    is exp(A * (S_i - S_j)) with S the running sum of Delta: closed form, no repeated product."""
+    x, dt, A, B, C = q["x"], q["dt"], q["A"], q["B"], q["C"]
+    batch, L, H, P = x.shape
+    G = B.shape[2]
+    bias = q["dt_bias"] if q["dt_bias"] is not None else np.zeros(H)
+    pre = dt + bias[None, None, :]
+    dl = softplus_ref(pre) if softplus else pre
+    y = np.zeros_like(x)
+    fin = np.zeros((batch, H, P, B.shape[3]))
+    for b in range(batch):
+        for h in range(H):
+            g = h // (H // G)
+            S = np.cumsum(dl[b, :, h])
+            CB = C[b, :, g, :] @ B[b, :, g, :].T                      # (L, L): C_i . B_j
+            dec = np.exp(A[h] * (S[:, None] - S[None, :]))
+            M = np.tril(CB * dec) * dl[b, None, :, h]                  # times Delta_j
+            yy = M @ x[b, :, h, :]                                     # (L, P)
+            w = np.exp(A[h] * (S[-1] - S)) * dl[b, :, h]               # step j to the end
+            fin[b, h] = (x[b, :, h, :] * w[:, None]).T @ B[b, :, g, :]
+            if q["h0"] is not None:
+                carry = np.exp(A[h] * S)                               # from the start to i
+                yy += carry[:, None] * (C[b, :, g, :] @ q["h0"][b, h].T)
+                fin[b, h] += np.exp(A[h] * S[-1]) * q["h0"][b, h]
+            if q["D"] is not None:
+                yy += q["D"][h] * x[b, :, h, :]
+            if q["z"] is not None:
+                yy *= silu_ref(q["z"][b, :, h, :])
+            y[b, :, h, :] = yy
+    return y, fin
+
+
+def pin_ssd_matrix_form(orc, seed=41, full=True, softplus=True):
+    q = _ssd_problem(seed, full=full)
+    y, fin = orc.ssd_fwd(q["x"], q["dt"], q["A"], q["B"], q["C"], q["D"], q["z"], q["dt_bias"],
+                         softplus, q["h0"])
+    ry, rf = ssd_matrix_form(q, softplus)
+    return max(relerr(y, ry), relerr(fin, rf))
+
+
+def pin_ssd_is_s6_with_scalar_A(orc, seed=42):
+    """With A[d, n] = A_h for every state and B, C shared by all heads (one group), each of the
+    headdim channels of a head is one S6 channel: the SSD recurrence must equal the selective
+    scan (itself pinned above) run on dim = nheads * headdim channels."""
+    q = _ssd_problem(seed, batch=2, seqlen=19, nheads=3, headdim=2, ngroups=1, dstate=16)
+    y, fin = orc.ssd_fwd(q["x"], q["dt"], q["A"], q["B"], q["C"], q["D"], q["z"], q["dt_bias"],
+                         True, q["h0"])
+    batch, L, H, P = q["x"].shape
+    to_bdl = lambda a: np.ascontiguousarray(a.reshape(batch, L, H * P).transpose(0, 2, 1))
+    u = to_bdl(q["x"])
+    z = to_bdl(q["z"])
+    delta = np.ascontiguousarray(np.repeat(q["dt"], P, axis=2).transpose(0, 2, 1))
+    A = np.repeat(q["A"], P)[:, None] * np.ones((1, 16))
+    Bs = np.ascontiguousarray(q["B"][:, :, 0, :].transpose(0, 2, 1))
+    Cs = np.ascontiguousarray(q["C"][:, :, 0, :].transpose(0, 2, 1))
+    out, sfin = orc.scan_fwd(u, delta, A, Bs, Cs, np.repeat(q["D"], P), z,
+                             np.repeat(q["dt_bias"], P), True, q["h0"].reshape(batch, H * P, 16))
+    return max(relerr(y, out.transpose(0, 2, 1).reshape(batch, L, H, P)),
+               relerr(fin, sfin.reshape(batch, H, P, 16)))
+
+
+def pin_ssd_no_decay_is_running_sum(orc, seed=43):
+    """A = 0: nothing decays, so the state is the running sum of Delta_j x_j B_j^T and
+    y_i = C_i . H_i (no gate, no skip) -- evaluated with numpy's cumulative sum."""
+    q = _ssd_problem(seed, full=False)
+    q["A"] = np.zeros_like(q["A"])
+    y, fin = orc.ssd_fwd(q["x"], q["dt"], q["A"], q["B"], q["C"], None, None, None, True, None)
+    batch, L, H, P = q["x"].shape
+    G = q["B"].shape[2]
+    dl = softplus_ref(q["dt"])
+    worst = 0.0
+    for b in range(batch):
+        for h in range(H):
+            g = h // (H // G)
+            outer = (dl[b, :, h, None, None] * q["x"][b, :, h, :, None] *
+                     q["B"][b, :, g, None, :])                      # (L, P, N)
+            Hs = np.cumsum(outer, axis=0)
+            ry = np.einsum("tpn,tn->tp", Hs, q["C"][b, :, g, :])
+            worst = max(worst, relerr(y[b, :, h, :], ry), relerr(fin[b, h], Hs[-1]))
+    return worst
+
+
 # (pin function, bound) pairs used by the pin tests and the mutation tests.
 ALL_PINS = [
     (pin_lti_convolution, 1e-11),
@@ -351,4 +453,8 @@ ALL_PINS = [
     (pin_conv_step_is_causal_convolution, 1e-13),
     (pin_backward_finite_differences, 1e-5),
     (lambda o: pin_backward_finite_differences(o, seed=26, softplus=False, full=False), 1e-5),
+    (pin_ssd_matrix_form, 1e-11),
+    (lambda o: pin_ssd_matrix_form(o, seed=44, full=False, softplus=False), 1e-11),
+    (pin_ssd_is_s6_with_scalar_A, 1e-12),
+    (pin_ssd_no_decay_is_running_sum, 1e-12),
 ]

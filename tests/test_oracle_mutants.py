@@ -62,6 +62,22 @@ MUTANTS = {
     "conv_taps_reversed": ("acc += w[d * width + k] * s[k];", "acc += w[d * width + (width - 1 - k)] * s[k];"),
     "conv_bias_dropped": ("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
     "conv_silu_dropped": ("u[r] = silu_on ? silu(acc) : acc;", "u[r] = acc;"),
+    "ssd_decay_sign": ("const double decay = exp(dlt * A[h]);", "const double decay = exp(-dlt * A[h]);"),
+    "ssd_missing_delta": ("H[p * N + n] = decay * H[p * N + n] + dlt * xt[p] * Bt[n];",
+                          "H[p * N + n] = decay * H[p * N + n] + xt[p] * Bt[n];"),
+    "ssd_group_index": ("g = h / heads_per_group;", "g = h % ngroups;"),
+    "ssd_readout_before_update": ("""                    H[p * N + n] = decay * H[p * N + n] + dlt * xt[p] * Bt[n];
+                    acc += Ct[n] * H[p * N + n];""", """                    acc += Ct[n] * H[p * N + n];
+                    H[p * N + n] = decay * H[p * N + n] + dlt * xt[p] * Bt[n];"""),
+    "ssd_C_is_B": ("acc += Ct[n] * H[p * N + n];", "acc += Bt[n] * H[p * N + n];"),
+    "ssd_D_dropped": ("acc += (D ? D[h] : 0.0) * xt[p];", ""),
+    "ssd_gate_dropped": ("if (z) acc *= silu(z[((b * seqlen + t) * nheads + h) * P + p]);", ""),
+    "ssd_bias_ignored": ("const double xr = dt[(b * seqlen + t) * nheads + h] + (dt_bias ? dt_bias[h] : 0.0);",
+                         "const double xr = dt[(b * seqlen + t) * nheads + h];"),
+    "ssd_initial_state_ignored": ("H[i] = initial_state ? initial_state[bh * P * N + i] : 0.0;",
+                                  "H[i] = 0.0;"),
+    "ssd_final_state_transposed": ("for (int64_t i = 0; i < P * N; ++i) final_state[bh * P * N + i] = H[i];",
+                                   "for (int64_t i = 0; i < P * N; ++i) final_state[bh * P * N + i] = H[(i % P) * N + i / P];"),
 }
 
 
