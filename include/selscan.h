@@ -227,6 +227,36 @@ selscan_status ssm_scan_bwd(const void* u, const void* delta, const float* A, co
 size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
 
 /*
+ * ssd_chunk_scan_fwd: the Mamba-2 layer core, state space duality (SSD). "Mamba and State Space
+ * Models" (world.lapla.si), section "Mamba-2": A is one number per head times the identity, so
+ * the layer is one lower-triangular matrix per head (entry i, j = C_i . B_j times the decay
+ * between j and i), computed in chunks: matrix products inside each chunk on the tensor cores,
+ * only the state passed between chunks. Per batch b, head h (group g = h / (nheads/ngroups)):
+ *   Delta_t  = softplus(dt[b,t,h] + dt_bias[h])   (dt + dt_bias without SELSCAN_FLAG_SOFTPLUS)
+ *   H_t[p,n] = exp(Delta_t A[h]) H_{t-1}[p,n] + Delta_t x[b,t,h,p] B[b,t,g,n]
+ *   y[b,t,h,p] = (sum_n C[b,t,g,n] H_t[p,n] + D[h] x[b,t,h,p]) * silu(z[b,t,h,p])
+ * Layouts (contiguous, row-major):
+ *   x, z, y          (batch, seqlen, nheads, headdim)   bf16 (y: out_dtype)
+ *   dt               (batch, seqlen, nheads)            bf16
+ *   B, C             (batch, seqlen, ngroups, dstate)   bf16
+ *   A, D, dt_bias    (nheads)                           fp32; D, dt_bias NULL = 0
+ *   initial_state, final_state  (batch, nheads, headdim, dstate)  fp32, NULL = zeros / not written
+ * z NULL = no gate. headdim must be 64 and dstate 128 (the released Mamba-2 models' sizes),
+ * in_dtype bf16, else SELSCAN_ERR_UNSUPPORTED; nheads % ngroups == 0. dt_softplus takes only
+ * SELSCAN_FLAG_SOFTPLUS. Arithmetic: fp32 accumulation on the tensor cores; the products the
+ * layer derives (the masked decay matrix, the decayed inputs, the state) enter as the sum of two
+ * bf16 parts, which keeps about 16 significand bits. The state of each (b, h) stays on chip for
+ * the whole sequence; nothing but y and the final state is written. No workspace.
+ */
+selscan_status ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A, const void* B,
+                                  const void* C, const float* D, const void* z,
+                                  const float* dt_bias, int dt_softplus, void* y,
+                                  float* final_state, const float* initial_state, int64_t batch,
+                                  int64_t seqlen, int64_t nheads, int64_t headdim,
+                                  int64_t ngroups, int64_t dstate, selscan_dtype in_dtype,
+                                  selscan_dtype out_dtype, selscan_stream_t stream);
+
+/*
  * selscan_device_status: errors that kernels of this library detected on the device.
  *
  * Every wait inside a kernel (for a TMA copy of B / C to land in shared memory) is bounded

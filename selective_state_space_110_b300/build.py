@@ -15,8 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libselscan.so")
 SOURCES = ["selscan_api.cu", "scan_fwd.cu", "state_update.cu", "scan_fwd_no_alloc.cu",
-           "scan_bwd.cu"]
-HEADERS = ["selscan_device.cuh", "selscan_launch.h"]
+           "scan_bwd.cu", "ssd_fwd.cu"]
+HEADERS = ["selscan_device.cuh", "selscan_launch.h", "sm100_async.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
          "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]

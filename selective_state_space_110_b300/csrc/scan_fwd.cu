@@ -44,6 +44,7 @@
 
 #include "selscan_device.cuh"
 #include "selscan_launch.h"
+#include "sm100_async.cuh"
 
 namespace selscan {
 
@@ -62,7 +63,6 @@ struct Geo {
     static constexpr int kBlocks = kChunk / 4;  // 4-token blocks per chunk
     static constexpr int kMinCtas = kR == 1 ? 5 : 6;  // register budget per thread
 };
-constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s: a TMA stage that never lands
 
 // Error bits a kernel can raise; read (and cleared) by read_device_status().
 __device__ unsigned int g_device_status;
@@ -88,54 +88,6 @@ struct __align__(128) ScanSmem {
     float4 red[Geo<kR>::kWarps][kR][Geo<kR>::kBlocks][32];
     unsigned long long full[St::kStages];
 };
-
-// ---- TMA / mbarrier primitives (inline PTX) -------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Waits for phase `parity` of `bar`; false if it has not completed after kWaitLimitCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long start = clock64();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - start > kWaitLimitCycles) return false;
-    }
-}
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
-                                            unsigned long long* bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
 
 // ---- 8-token raw vectors of u / delta / z ---------------------------------------------------
 

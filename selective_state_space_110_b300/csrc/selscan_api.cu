@@ -225,13 +225,14 @@ SELSCAN_EXPORT selscan_status ssm_state_update(float* state, const void* x, cons
 }
 
 SELSCAN_EXPORT selscan_status selscan_device_status(int reset, selscan_stream_t stream) {
-    unsigned int bits = 0;
-    if (selscan::read_device_status(&bits, reset != 0, reinterpret_cast<cudaStream_t>(stream)) !=
-        cudaSuccess) {
+    unsigned int bits = 0, ssd_bits = 0;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (selscan::read_device_status(&bits, reset != 0, s) != cudaSuccess ||
+        selscan::read_ssd_status(&ssd_bits, reset != 0, s) != cudaSuccess) {
         cudaGetLastError();
         return SELSCAN_ERR_CUDA;
     }
-    return bits ? SELSCAN_ERR_DEVICE_TIMEOUT : SELSCAN_OK;
+    return (bits | ssd_bits) ? SELSCAN_ERR_DEVICE_TIMEOUT : SELSCAN_OK;
 }
 
 SELSCAN_EXPORT selscan_status selscan_selftest_wait_timeout(int64_t limit_cycles,
@@ -391,4 +392,54 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
                                              grad_dtype == SELSCAN_BF16,
                                              reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}
+
+SELSCAN_EXPORT selscan_status ssd_chunk_scan_fwd(
+    const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+    const void* z, const float* dt_bias, int dt_softplus, void* y, float* final_state,
+    const float* initial_state, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+    int64_t ngroups, int64_t dstate, selscan_dtype in_dtype, selscan_dtype out_dtype,
+    selscan_stream_t stream) {
+    if (headdim != 64 || dstate != 128 || in_dtype != SELSCAN_BF16 || !dtype_ok(out_dtype))
+        return SELSCAN_ERR_UNSUPPORTED;
+    if (batch < 1 || batch > 65535 || nheads < 1 || nheads > 65535 || ngroups < 1 ||
+        nheads % ngroups != 0 || seqlen < 0 || seqlen > (int64_t(1) << 31) - 256 ||
+        (dt_softplus & ~SELSCAN_FLAG_SOFTPLUS))
+        return SELSCAN_ERR_INVALID_ARG;
+    const bool has_tokens = seqlen > 0;
+    if (!A || (has_tokens && (!x || !dt || !B || !C || !y))) return SELSCAN_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, y, final_state, initial_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
+    const size_t eout = dtype_size(out_dtype);
+    const size_t act = (size_t)batch * (size_t)seqlen * (size_t)nheads * 64;
+    const size_t bc = (size_t)batch * (size_t)seqlen * (size_t)ngroups * 128 * 2;
+    const size_t st = (size_t)batch * (size_t)nheads * 64 * 128 * sizeof(float);
+    const size_t hv = (size_t)nheads * 4;
+    const Range in_r[] = {range_of(x, act * 2), range_of(dt, (size_t)batch * seqlen * nheads * 2),
+                          range_of(A, hv), range_of(B, bc), range_of(C, bc),
+                          range_of(D, D ? hv : 0), range_of(z, z ? act * 2 : 0),
+                          range_of(dt_bias, dt_bias ? hv : 0),
+                          range_of(initial_state, initial_state ? st : 0)};
+    const Range y_r = range_of(y, has_tokens ? act * eout : 0);
+    const Range fin_r = range_of(final_state, final_state ? st : 0);
+    for (const Range& r : in_r)
+        if (overlaps(y_r, r) || overlaps(fin_r, r)) return SELSCAN_ERR_INVALID_ARG;
+    if (overlaps(y_r, fin_r)) return SELSCAN_ERR_INVALID_ARG;
+
+    int sms = 0;
+    selscan_status s = device_sms(&sms);
+    if (s != SELSCAN_OK) return s;
+    selscan::SsdArgs a{};
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
+    a.y = y; a.final_state = final_state; a.initial_state = initial_state;
+    a.batch = batch; a.seqlen = seqlen; a.nheads = nheads; a.ngroups = ngroups;
+    a.softplus = (dt_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
+    cudaError_t e = selscan::launch_ssd_fwd(a, out_dtype == SELSCAN_BF16,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SELSCAN_ERR_CUDA;
+    }
+    return SELSCAN_OK;
 }

@@ -109,4 +109,27 @@ size_t scan_bwd_workspace_floats(int64_t batch, int64_t dim, int64_t seqlen, int
 // Launches the backward kernel and the reduction of its partial sums on `stream`.
 cudaError_t launch_scan_bwd(const BwdArgs& a, bool in_bf16, bool grad_bf16, cudaStream_t stream);
 
+// Mamba-2 SSD layer (bf16 inputs, headdim 64, dstate 128).
+struct SsdArgs {
+    const void* x;        // (batch, seqlen, nheads, 64) bf16
+    const void* dt;       // (batch, seqlen, nheads) bf16
+    const float* A;       // (nheads)
+    const void* B;        // (batch, seqlen, ngroups, 128) bf16
+    const void* C;
+    const float* D;       // (nheads) or NULL
+    const void* z;        // like x, or NULL
+    const float* dt_bias; // (nheads) or NULL
+    void* y;              // like x, output dtype
+    float* final_state;   // (batch, nheads, 64, 128) or NULL
+    const float* initial_state;
+    int64_t batch;
+    int64_t seqlen;
+    int64_t nheads;
+    int64_t ngroups;
+    int softplus;
+};
+cudaError_t launch_ssd_fwd(const SsdArgs& a, bool out_bf16, cudaStream_t stream);
+// Error bits raised by the SSD kernel (timeouts of its bounded waits); see read_device_status.
+cudaError_t read_ssd_status(unsigned int* status, bool reset, cudaStream_t stream);
+
 }  // namespace selscan

@@ -277,3 +277,45 @@ def ssm_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
             workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _lib.check("ssm_scan_bwd", st)
     return g
+
+
+def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True,
+                       initial_state=None, out_dtype=None, y=None, final_state=None,
+                       return_final_state=True, stream=None):
+    """Mamba-2 SSD layer. x (batch, seqlen, nheads, 64) bf16, dt (batch, seqlen, nheads) bf16,
+    A (nheads) fp32, B/C (batch, seqlen, ngroups, 128) bf16. Returns (y, final_state or None)."""
+    if x.dim() != 4:
+        raise ValueError("x must be (batch, seqlen, nheads, headdim)")
+    batch, seqlen, nheads, headdim = x.shape
+    if B.dim() != 4:
+        raise ValueError("B must be (batch, seqlen, ngroups, dstate)")
+    ngroups, dstate = B.shape[2], B.shape[3]
+    in_dt = x.dtype
+    if in_dt not in _DT:
+        raise ValueError(f"unsupported input dtype {in_dt}")
+    dev = x.device
+    _check_dev("x", x, in_dt, (batch, seqlen, nheads, headdim), dev)
+    _check_dev("dt", dt, in_dt, (batch, seqlen, nheads), dev)
+    _check_dev("A", A, torch.float32, (nheads,), dev)
+    _check_dev("B", B, in_dt, (batch, seqlen, ngroups, dstate), dev)
+    _check_dev("C", C, in_dt, (batch, seqlen, ngroups, dstate), dev)
+    _check_dev("D", D, torch.float32, (nheads,), dev)
+    _check_dev("z", z, in_dt, (batch, seqlen, nheads, headdim), dev)
+    _check_dev("dt_bias", dt_bias, torch.float32, (nheads,), dev)
+    _check_dev("initial_state", initial_state, torch.float32, (batch, nheads, headdim, dstate), dev)
+    if y is None:
+        y = torch.empty((batch, seqlen, nheads, headdim), dtype=out_dtype or in_dt, device=dev)
+    if y.dtype not in _DT:
+        raise ValueError(f"unsupported output dtype {y.dtype}")
+    _check_dev("y", y, None, (batch, seqlen, nheads, headdim), dev)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32, device=dev)
+    _check_dev("final_state", final_state, torch.float32, (batch, nheads, headdim, dstate), dev)
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssd_chunk_scan_fwd(
+            _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+            _flags(dt_softplus, False), _ptr(y), _ptr(final_state), _ptr(initial_state), batch,
+            seqlen, nheads, headdim, ngroups, dstate, _DT[in_dt], _DT[y.dtype],
+            _stream_handle(stream))
+    _lib.check("ssd_chunk_scan_fwd", st)
+    return y, final_state

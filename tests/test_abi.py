@@ -230,3 +230,43 @@ def test_bwd_valid_args_reach_the_device_check(lib):
     need = lib.ssm_scan_bwd_workspace_size(2, 64, 16, 128)
     assert need >= 4 * (2 * 64 * 8 * 16 + 2 * 2 * 32 * 128)
     assert lib.ssm_scan_bwd_workspace_size(2, 64, 8, 128) == 0
+
+
+def call_ssd(lib, **kw):
+    a = dict(x=fake(0), dt=fake(1), A=fake(2), B=fake(3), C=fake(4), D=fake(5), z=fake(6),
+             dt_bias=fake(7), flags=1, y=fake(8), fin=fake(9), h0=None, batch=2, seqlen=256,
+             nheads=8, headdim=64, ngroups=1, dstate=128, in_dtype=_lib.BF16, out_dtype=_lib.BF16,
+             stream=None)
+    a.update(kw)
+    return lib.ssd_chunk_scan_fwd(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                  a["dt_bias"], a["flags"], a["y"], a["fin"], a["h0"], a["batch"],
+                                  a["seqlen"], a["nheads"], a["headdim"], a["ngroups"],
+                                  a["dstate"], a["in_dtype"], a["out_dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(headdim=128), UNSUP),
+    (dict(dstate=64), UNSUP),
+    (dict(in_dtype=_lib.F32), UNSUP),
+    (dict(out_dtype=9), UNSUP),
+    (dict(ngroups=3), INVALID),              # 8 heads do not split into 3 groups
+    (dict(flags=2), INVALID),                # zero-order hold is not an SSD option
+    (dict(batch=0), INVALID),
+    (dict(x=None), INVALID),
+    (dict(A=None), INVALID),
+    (dict(y=None), INVALID),
+    (dict(y=fake(0) + 64), INVALID),         # y inside x
+    (dict(fin=fake(8) + 16), INVALID),       # final state inside y
+    (dict(h0=fake(9)), INVALID),             # final state over the initial state
+    (dict(B=fake(3) + 8), ALIGN),
+])
+def test_ssd_rejects(lib, kw, expect):
+    assert call_ssd(lib, **kw) == expect
+
+
+def test_ssd_valid_args_reach_the_device_check(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("device present: covered by the GPU tests")
+    assert call_ssd(lib) == CUDA
+    assert call_ssd(lib, seqlen=0, x=None, dt=None, B=None, C=None, y=None) == CUDA

@@ -7,6 +7,9 @@ same tensors from it without sharing any computation.
 from .configs import (
     ScanConfig,
     DecodeConfig,
+    SsdConfig,
+    SSD_CONFIGS,
+    ssd_config,
     SCAN_CONFIGS,
     DECODE_CONFIG,
     scan_config,
@@ -16,6 +19,7 @@ from .generate import (
     make_decode_layer_params,
     make_decode_tokens,
     make_decode_state,
+    make_ssd_inputs,
 )
 
 __all__ = [
@@ -28,4 +32,8 @@ __all__ = [
     "make_decode_layer_params",
     "make_decode_tokens",
     "make_decode_state",
+    "make_ssd_inputs",
+    "SsdConfig",
+    "SSD_CONFIGS",
+    "ssd_config",
 ]

@@ -71,6 +71,47 @@ SCAN_CONFIGS = {
 DECODE_CONFIG = DecodeConfig("c4_decode_mamba2p8b", 64, (1, 16, 64), 5120, 16, 1024, 8, 1e-3, 1e-1, 1004)
 
 
+@dataclass(frozen=True)
+class SsdConfig:
+    """Mamba-2 SSD layer: x (batch, seqlen, nheads, headdim), B/C (batch, seqlen, ngroups, dstate)."""
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    ngroups: int
+    dstate: int
+    seed: int
+    dt_min: float = 1e-3
+    dt_max: float = 1e-1
+    has_z: bool = True
+    has_D: bool = True
+
+    @property
+    def elements(self) -> int:  # batch * seqlen * nheads * headdim = B*L*d_inner
+        return self.batch * self.seqlen * self.nheads * self.headdim
+
+    def replace(self, **kw) -> "SsdConfig":
+        return dataclasses.replace(self, **kw)
+
+
+SSD_CONFIGS = {
+    # Small case the oracle finishes in well under a second.
+    "ssd0_tiny": SsdConfig("ssd0_tiny", 1, 256, 4, 64, 1, 128, 2000),
+    # Mamba-2 2.7B-like layer: d_model 2560, expand 2 -> d_inner 5120 = 80 heads x 64, a state
+    # of 128 numbers per channel ("Mamba-2": the released models keep 128 where Mamba keeps 16),
+    # one group of B/C; the same batch, sequence length and d_inner as the Mamba-2.8B scan layer.
+    "ssd1_mamba2_2p7b": SsdConfig("ssd1_mamba2_2p7b", 4, 2048, 80, 64, 1, 128, 2001),
+}
+
+
+def ssd_config(name: str) -> SsdConfig:
+    for k, v in SSD_CONFIGS.items():
+        if k == name or k.split("_")[0] == name:
+            return v
+    raise KeyError(f"unknown SSD config {name!r}; known: {sorted(SSD_CONFIGS)}")
+
+
 def scan_config(name: str) -> ScanConfig:
     for k, v in SCAN_CONFIGS.items():
         if k == name or k.split("_")[0] == name:

@@ -18,7 +18,7 @@ import math
 
 import torch
 
-from .configs import ScanConfig, DecodeConfig
+from .configs import ScanConfig, DecodeConfig, SsdConfig
 
 SLAB = 1 << 26
 
@@ -107,3 +107,25 @@ def make_decode_tokens(cfg: DecodeConfig, batch: int, layer: int, slot: int, dev
     B = _normal((batch, cfg.dstate), 1.0, bf, gen, device)
     C = _normal((batch, cfg.dstate), 1.0, bf, gen, device)
     return {"x": x, "dt": dt, "z": z, "B": B, "C": C}
+
+
+def make_ssd_inputs(cfg: SsdConfig, device="cpu") -> dict:
+    """Inputs of one Mamba-2 SSD layer call, in this draw order: dt_bias from dt log-uniform in
+    [dt_min, dt_max] per head (inverse softplus), A = -U(1, 16) per head (fp32), x, dt (raw,
+    N(0, 0.5^2)), z, B, C (N(0, 1), bf16); D = 1 per head."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed)
+    bf = torch.bfloat16
+    bias = _bias_from_dt(cfg.nheads, cfg.dt_min, cfg.dt_max, gen, device)
+    A = -(1.0 + 15.0 * torch.rand(cfg.nheads, generator=gen, device=device, dtype=torch.float32))
+    act = (cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim)
+    x = _normal(act, 1.0, bf, gen, device)
+    dt = _normal((cfg.batch, cfg.seqlen, cfg.nheads), 0.5, bf, gen, device)
+    z = _normal(act, 1.0, bf, gen, device)
+    bc = (cfg.batch, cfg.seqlen, cfg.ngroups, cfg.dstate)
+    B = _normal(bc, 1.0, bf, gen, device)
+    C = _normal(bc, 1.0, bf, gen, device)
+    D = torch.ones(cfg.nheads, dtype=torch.float32, device=device)
+    return {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D if cfg.has_D else None,
+            "z": z if cfg.has_z else None, "dt_bias": bias, "dt_softplus": True}
