@@ -16,17 +16,24 @@
 //
 // One CTA per (b, h) walks the chunks in order; 256 threads, thread (row, half) serving
 // tensor-memory lane `row` (the chunk's token row, or the state row n) and one half of the
-// columns. C, B and X arrive by TMA into 128-byte-swizzled tiles (the layout the MMA
-// descriptors read). The four products run as tcgen05.mma (bf16 operands, fp32 accumulators in
-// tensor memory), issued by one thread and completed through mbarriers; the threads move data
-// between tensor memory, registers and shared memory in between. The operands the kernel
-// derives (M, w * X and the state S) are fp32 values; each is passed to the tensor cores as
-// the sum of two bf16 matrices (hi = bf16(v), lo = bf16(v - hi)), two MMAs accumulating into
-// the same result, so the products keep about 16 significand bits. B, C and x are bf16 inputs
-// and enter exactly.
+// columns. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
+// next chunk's tiles load while this one computes; dt of the next chunk and z of this one are
+// loaded into registers ahead of use. The products run as tcgen05.mma (bf16 operands, fp32
+// accumulators in tensor memory), issued by one thread and completed through mbarriers, and are
+// ordered so that the tensor cores work while the threads do: C B^T and C S run while the
+// threads scale x and decay the state; the state update B^T (w X) runs while they build M; M X
+// runs while they split the new state.
 //
-// Tensor memory (512 columns, one CTA per SM): [0,128) G, [128,192) M X, [192,256) C S,
-// [256,320) the state S (row n, column p), fp32.
+// The operands the kernel derives (M, w * X and the state S) are fp32 values; each enters the
+// tensor cores as the sum of two bf16 matrices (hi = bf16(v), lo = bf16(v - hi)), which keeps
+// about 16 significand bits. For C S and B^T (w X) hi and lo sit side by side as one N = 128
+// operand, giving two accumulators that are added afterwards (the state is kept as such a
+// pair); M is written back into tensor memory over G and read from there as the A operand of
+// M X. B, C and x are bf16 inputs and enter exactly.
+//
+// Tensor memory (512 columns, one CTA per SM): [0,128) G, then M (hi in [0,64), lo in
+// [64,128), bf16 pairs); [128,192) M X; [192,320) C S (hi part | lo part); [320,448) the state
+// as the pair S = Sa + Sb (row n, column p).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,22 +48,19 @@ namespace selscan {
 constexpr int kQ = 128;              // tokens per chunk (the MMA's M)
 constexpr int kHeadDim = 64;         // P
 constexpr int kSsdState = 128;       // N
-constexpr int kSsdThreads = 256;
+constexpr int kWorkers = 256;        // threads that move data (8 warps)
+constexpr int kSsdThreads = kWorkers + 32;  // plus one warp that issues TMA loads and MMAs
 constexpr int kTile = 16384;         // one 128-row x 128-byte swizzled tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0, kColYd = 128, kColYo = 192, kColS = 256;
+constexpr uint32_t kColG = 0, kColMhi = 128, kColMlo = 192, kColS = 256, kColYo = 384;
 
-// Shared-memory tiles, kTile bytes each from a 1024-byte aligned base.
-enum SsdTile : int {
-    kTC0 = 0, kTC1,    // C of the chunk: rows i, states 0..63 | 64..127 (K-major)
-    kTB0, kTB1,        // B: rows j, states 0..63 | 64..127 (K-major for G, MN-major for B^T)
-    kTX,               // x: rows j, headdim 0..63 (MN-major)
-    kTGH0, kTGH1,      // M hi: rows i, columns j 0..63 | 64..127 (K-major)
-    kTGL0, kTGL1,      // M lo
-    kTSH, kTSL,        // state S hi / lo: rows n, headdim 0..63 (MN-major)
-    kTXH, kTXL,        // w * X hi / lo: rows j, headdim (MN-major)
-    kNumTiles
-};
+// Shared-memory tiles, kTile bytes each from a 1024-byte aligned base. Input buffer s holds
+// tiles 5s .. 5s+4: C (rows i, states 0..63 | 64..127; K-major), B (rows j, states 0..63 |
+// 64..127; K-major for G, MN-major for B^T), x (rows j, headdim 0..63; MN-major).
+constexpr int kInC = 0, kInB = 2, kInX = 4, kInTiles = 5;
+constexpr int kTSH = 10, kTSL = 11;  // state hi | lo: rows n, headdim (MN-major), adjacent
+constexpr int kTXH = 12, kTXL = 13;  // w * X hi | lo: rows j, headdim (MN-major), adjacent
+constexpr int kNumTiles = 14;
 constexpr int kSsdSmemBytes = kNumTiles * kTile + 1024;
 
 __device__ unsigned int g_ssd_status;
@@ -66,23 +70,23 @@ __device__ __forceinline__ uint32_t sw128(int r, int ch) {
     return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
-    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+// A pair of fp32 values -> packed bf16 pairs of their hi and lo parts.
+__device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+    const uint32_t hu = *reinterpret_cast<const uint32_t*>(&h);
+    const float2 hf = make_float2(__uint_as_float(hu << 16), __uint_as_float(hu & 0xffff0000u));
+    const float2 r = __ffma2_rn(hf, make_float2(-1.f, -1.f), v);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
+    hi = hu;
+    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Eight fp32 values -> 16-byte chunks of their bf16 hi and lo parts.
 __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * e] - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1));
-        h[e] = pack2(h0, h1);
-        l[e] = pack2(l0, l1);
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
+    split2(make_float2(v[0], v[1]), hi.x, lo.x);
+    split2(make_float2(v[2], v[3]), hi.y, lo.y);
+    split2(make_float2(v[4], v[5]), hi.z, lo.z);
+    split2(make_float2(v[6], v[7]), hi.w, lo.w);
 }
 
 __device__ __forceinline__ void unpack8(const uint4& r, float* v) {
@@ -104,10 +108,21 @@ __device__ __forceinline__ void store32<__nv_bfloat16>(__nv_bfloat16* dst, const
     for (int q = 0; q < 4; ++q) {
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = pack2(__float2bfloat16_rn(v[8 * q + 2 * e]), __float2bfloat16_rn(v[8 * q + 2 * e + 1]));
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&p);
+        }
         reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] (A: 128 rows in tensor-memory lanes, bf16 pairs along columns).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 template <typename Tout>
@@ -115,44 +130,48 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ unsigned long long bar_tma, bar_g1, bar_g2, bar_g4;
+    // Completion of the TMA loads (per input buffer) and of the MMA groups (tcgen05.commit);
+    // hand-offs from the 256 worker threads to the issuing thread.
+    __shared__ unsigned long long bar_tma[2], bar_g1, bar_g2, bar_g4;
+    __shared__ unsigned long long bar_x, bar_m, bar_s, bar_y;
     __shared__ uint32_t tmem_slot;
-    __shared__ float s_cs[kQ];  // running sum of Delta*A*log2(e) in the chunk, inclusive
-    __shared__ float s_dl[kQ];  // Delta
+    __shared__ __align__(16) float s_cs[kQ];  // running sum of Delta*A*log2(e), inclusive
+    __shared__ __align__(16) float s_dl[kQ];  // Delta
     __shared__ float s_wsum[4];
+    __shared__ int s_ok;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     auto tile = [&](int i) { return sm + i * kTile; };
     auto tile_addr = [&](int i) { return smem_u32(sm) + (uint32_t)(i * kTile); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane;  // tensor-memory lane this thread reads and writes
     const int h = blockIdx.x, b = blockIdx.y;
     const int64_t H = a.nheads, L = a.seqlen;
     const int g = (int)(h / (H / a.ngroups));
-    const float A2 = a.A[h] * kLog2e;
-    const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
-    const float Dh = a.D ? a.D[h] : 0.f;
     const int nchunks = (int)((L + kQ - 1) / kQ);
-    const __nv_bfloat16* dt = static_cast<const __nv_bfloat16*>(a.dt);
-    const __nv_bfloat16* zp = static_cast<const __nv_bfloat16*>(a.z);
-    Tout* yp = static_cast<Tout*>(a.y);
+    const bool init_state = a.initial_state != nullptr;
 
     if (warp == 0) tmem_alloc(&tmem_slot, kTmemCols);
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_tma[0], 1);
+        mbar_init(&bar_tma[1], 1);
         mbar_init(&bar_g1, 1);
         mbar_init(&bar_g2, 1);
         mbar_init(&bar_g4, 1);
+        mbar_init(&bar_x, kWorkers);
+        mbar_init(&bar_m, kWorkers);
+        mbar_init(&bar_s, kWorkers);
+        mbar_init(&bar_y, kWorkers);
         fence_mbar_init();
+        s_ok = 1;
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
+    const int row = quarter * 32 + lane;  // tensor-memory lane a worker thread reads and writes
     const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
-
-    // S (hi / lo) for the next C S product: row n = row, headdim columns 32*half..+31.
+    // The state Sa + Sb (row n = row, headdim columns 32*half..+31) -> hi / lo tiles.
     auto put_state_split = [&](const float (&v)[32]) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -162,15 +181,16 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             *reinterpret_cast<uint4*>(tile(kTSL) + sw128(row, 4 * half + q)) = lo;
         }
     };
-
-    bool has_state = a.initial_state != nullptr;
-    bool ok = true;
-    if (has_state) {  // initial state (p, n) -> S[n][p]
-        float v[32];
+    if (init_state && warp < kWorkers / 32) {  // initial state (p, n) -> Sa[n][p], Sb = 0, split
+        float v[32], zero[32];
         const float* src = a.initial_state + ((int64_t)b * H + h) * kHeadDim * kSsdState + row;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = src[(int64_t)(32 * half + i) * kSsdState];
+        for (int i = 0; i < 32; ++i) {
+            v[i] = src[(int64_t)(32 * half + i) * kSsdState];
+            zero[i] = 0.f;
+        }
         tmem_st32(tmem + tlane + kColS + 32 * half, v);
+        tmem_st32(tmem + tlane + kColS + 64 + 32 * half, zero);
         put_state_split(v);
     }
     fence_proxy_async_smem();
@@ -178,221 +198,306 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
 
-    for (int c = 0; c < nchunks; ++c) {
-        const int64_t t0 = (int64_t)c * kQ;
-        const uint32_t par = (uint32_t)(c & 1);
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_tma, 5 * kTile);
-            tma_load_4d(tile(kTC0), &tmC, &bar_tma, 0, g, (int)t0, b);
-            tma_load_4d(tile(kTC1), &tmC, &bar_tma, 64, g, (int)t0, b);
-            tma_load_4d(tile(kTB0), &tmB, &bar_tma, 0, g, (int)t0, b);
-            tma_load_4d(tile(kTB1), &tmB, &bar_tma, 64, g, (int)t0, b);
-            tma_load_4d(tile(kTX), &tmX, &bar_tma, 0, h, (int)t0, b);
-        }
-        // Delta and the running sum of Delta*A over the chunk (one token per thread of warps 0-3).
-        if (tid < kQ) {
-            const int64_t t = t0 + tid;
-            float dl = 0.f;  // tokens past the end: no step, no decay
-            if (t < L) {
-                const float v = __bfloat162float(dt[((int64_t)b * L + t) * H + h]) + bias;
-                dl = a.softplus ? softplus_f<true>(v) : v;
-            }
-            float s = dl * A2;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += n;
-            }
-            if (lane == 31) s_wsum[warp] = s;
-            s_dl[tid] = dl;
-            s_cs[tid] = s;
-        }
-        __syncthreads();
-        if (tid < kQ) {
-            float off = 0.f;
-            for (int w = 0; w < warp; ++w) off += s_wsum[w];
-            s_cs[tid] += off;
-        }
-        ok = mbar_wait_bounded(&bar_tma, par);
-        if (!__syncthreads_and(ok)) { ok = false; break; }
-        tc_fence_after_sync();
-
-        // G = C B^T; with a carried state also C S (hi + lo).
-        if (tid == 0) {
+    if (warp == kWorkers / 32) {
+        // ---------------- issuing thread: TMA loads and tensor-core products ----------------
+        if (lane == 0 && nchunks > 0) {
+            prefetch_tmap(&tmX);
+            prefetch_tmap(&tmB);
+            prefetch_tmap(&tmC);
+            auto issue_tma = [&](int c) {  // chunk c -> input buffer c & 1
+                const int base = kInTiles * (c & 1);
+                unsigned long long* bar = &bar_tma[c & 1];
+                mbar_arrive_expect_tx(bar, kInTiles * kTile);
+                tma_load_4d(tile(base + kInC), &tmC, bar, 0, g, c * kQ, b);
+                tma_load_4d(tile(base + kInC + 1), &tmC, bar, 64, g, c * kQ, b);
+                tma_load_4d(tile(base + kInB), &tmB, bar, 0, g, c * kQ, b);
+                tma_load_4d(tile(base + kInB + 1), &tmB, bar, 64, g, c * kQ, b);
+                tma_load_4d(tile(base + kInX), &tmX, bar, 0, h, c * kQ, b);
+            };
+            issue_tma(0);
+            if (nchunks > 1) issue_tma(1);
             const uint32_t i_g1 = umma_idesc_bf16(128, 128, false, false);
-#pragma unroll 1
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (uint32_t)(k & 3) * 32;
-                umma_bf16(tmem + kColG, umma_desc_sw128(tile_addr(kTC0 + (k >> 2)) + off, 16, 1024),
-                          umma_desc_sw128(tile_addr(kTB0 + (k >> 2)) + off, 16, 1024), i_g1, k > 0);
-            }
-            if (has_state) {
-                const uint32_t i_g3 = umma_idesc_bf16(128, 64, false, true);
-#pragma unroll 1
-                for (int part = 0; part < 2; ++part)
-#pragma unroll 1
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (uint32_t)(k & 3) * 32;
-                        umma_bf16(tmem + kColYo,
-                                  umma_desc_sw128(tile_addr(kTC0 + (k >> 2)) + off, 16, 1024),
-                                  umma_desc_sw128(tile_addr(part ? kTSL : kTSH) + (uint32_t)k * 2048, kTile, 1024),
-                                  i_g3, (part | k) != 0);
-                    }
-            }
-            umma_commit(&bar_g1);
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar_g1, par));
-        tc_fence_after_sync();
-
-        // M = G * exp(cs_i - cs_j) * Delta_j (j <= i) as bf16 hi / lo, row i = row, columns
-        // 64*half..+63 (tile kTGH0 + half).
-        if (ok) {
-            const float cs_i = s_cs[row];
-            const bool live = t0 + row < L;
-#pragma unroll 1
-            for (int part = 0; part < 2; ++part) {
-                float v[32];
-                tmem_ld32(tmem + tlane + kColG + 64 * half + 32 * part, v);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float m[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 64 * half + 32 * part + 8 * q + e;
-                        m[e] = (live && j <= row) ? v[8 * q + e] * ex2_approx(cs_i - s_cs[j]) * s_dl[j] : 0.f;
-                    }
-                    uint4 hi, lo;
-                    split8(m, hi, lo);
-                    *reinterpret_cast<uint4*>(tile(kTGH0 + half) + sw128(row, 4 * part + q)) = hi;
-                    *reinterpret_cast<uint4*>(tile(kTGL0 + half) + sw128(row, 4 * part + q)) = lo;
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        if (!__syncthreads_and(ok)) { ok = false; break; }
-        tc_fence_after_sync();
-
-        // Y_diag = (M hi + M lo) X.
-        if (tid == 0) {
+            const uint32_t i_g3 = umma_idesc_bf16(128, 128, false, true);
+            const uint32_t i_g4 = umma_idesc_bf16(128, 128, true, true);
             const uint32_t i_g2 = umma_idesc_bf16(128, 64, false, true);
-#pragma unroll 1
-            for (int part = 0; part < 2; ++part)
+            bool ok = true;
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int in = kInTiles * (c & 1);
+                const uint32_t par = (uint32_t)(c & 1), prev = par ^ 1u;
+                const bool had_state = c > 0 || init_state;
+                ok = mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
+                if (ok && c > 0) ok = mbar_wait_bounded(&bar_m, prev);  // G of chunk c-1 consumed
+                if (!ok) break;
+                tc_fence_after_sync();
+                // G = C B^T
 #pragma unroll 1
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (uint32_t)(k & 3) * 32;
-                    umma_bf16(tmem + kColYd,
-                              umma_desc_sw128(tile_addr((part ? kTGL0 : kTGH0) + (k >> 2)) + off, 16, 1024),
-                              umma_desc_sw128(tile_addr(kTX) + (uint32_t)k * 2048, kTile, 1024), i_g2,
-                              (part | k) != 0);
+                    umma_bf16(tmem + kColG, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
+                              umma_desc_sw128(tile_addr(in + kInB + (k >> 2)) + off, 16, 1024), i_g1, k > 0);
                 }
-            umma_commit(&bar_g2);
-        }
-        // Meanwhile: w * X (hi / lo) for the state update (warps 0-3, row j = row), and the
-        // decay of the carried state by exp(cs_last) (warps 4-7, state row n = row).
-        const float cs_last = s_cs[kQ - 1];
-        if (half == 0) {
-            const float w = ex2_approx(cs_last - s_cs[row]) * s_dl[row];
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                float v[8];
-                unpack8(*reinterpret_cast<const uint4*>(tile(kTX) + sw128(row, ch)), v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= w;
-                uint4 hi, lo;
-                split8(v, hi, lo);
-                *reinterpret_cast<uint4*>(tile(kTXH) + sw128(row, ch)) = hi;
-                *reinterpret_cast<uint4*>(tile(kTXL) + sw128(row, ch)) = lo;
-            }
-        } else if (has_state) {
-            const float dec = ex2_approx(cs_last);
+                if (had_state) {
+                    if (c > 0) {  // the split state of chunk c-1 is ready and its output is read
+                        ok = mbar_wait_bounded(&bar_s, prev) && mbar_wait_bounded(&bar_y, prev);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                    }
+                    // C [S hi | S lo] (N = 128)
 #pragma unroll 1
-            for (int part = 0; part < 2; ++part) {
-                float v[32];
-                tmem_ld32(tmem + tlane + kColS + 32 * part, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= dec;
-                tmem_st32(tmem + tlane + kColS + 32 * part, v);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        tc_fence_after_sync();
-
-        // S (+)= B^T (w X): A = B^T (MN-major, states in two 64-blocks), B = w X (MN-major).
-        if (tid == 0) {
-            const uint32_t i_g4 = umma_idesc_bf16(128, 64, true, true);
-#pragma unroll 1
-            for (int part = 0; part < 2; ++part)
-#pragma unroll 1
-                for (int k = 0; k < 8; ++k)
-                    umma_bf16(tmem + kColS,
-                              umma_desc_sw128(tile_addr(kTB0) + (uint32_t)k * 2048, kTile, 1024),
-                              umma_desc_sw128(tile_addr(part ? kTXL : kTXH) + (uint32_t)k * 2048, kTile, 1024),
-                              i_g4, (has_state || part || k) ? 1u : 0u);
-            umma_commit(&bar_g4);
-        }
-
-        // y = Y_diag + exp(cs_i) * (C S) + D x, times silu(z): row i = row, headdim
-        // columns 32*half..+31.
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar_g2, par));
-        tc_fence_after_sync();
-        if (ok) {
-            float yd[32], yo[32];
-            tmem_ld32(tmem + tlane + kColYd + 32 * half, yd);
-            if (has_state) tmem_ld32(tmem + tlane + kColYo + 32 * half, yo);
-            const int64_t t = t0 + row;
-            if (t < L) {
-                const float e = has_state ? ex2_approx(s_cs[row]) : 0.f;
-                const int64_t off = (((int64_t)b * L + t) * H + h) * kHeadDim + 32 * half;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float xv[8], zv[8];
-                    unpack8(*reinterpret_cast<const uint4*>(tile(kTX) + sw128(row, 4 * half + q)), xv);
-                    if (zp) unpack8(*reinterpret_cast<const uint4*>(zp + off + 8 * q), zv);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float y = yd[8 * q + i] + Dh * xv[i];
-                        if (has_state) y = fmaf(e, yo[8 * q + i], y);
-                        if (zp) y *= silu_f<false>(zv[i]);
-                        yd[8 * q + i] = y;
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = (uint32_t)(k & 3) * 32;
+                        umma_bf16(tmem + kColYo, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
+                                  umma_desc_sw128(tile_addr(kTSH) + (uint32_t)k * 2048, kTile, 1024), i_g3, k > 0);
                     }
                 }
-                store32<Tout>(yp + off, yd);
+                umma_commit(&bar_g1);
+                // The next chunk's tiles go into the buffer chunk c-1 used, once everything that
+                // read it is done (its products, waited through G2, and its output).
+                if (c > 0 && c + 1 < nchunks) {
+                    ok = mbar_wait_bounded(&bar_g2, prev) && mbar_wait_bounded(&bar_y, prev);
+                    if (!ok) break;
+                    issue_tma(c + 1);
+                }
+                // [Sa | Sb] (+)= B^T [wX hi | wX lo]
+                ok = mbar_wait_bounded(&bar_x, par);
+                if (!ok) break;
+                tc_fence_after_sync();
+#pragma unroll 1
+                for (int k = 0; k < 8; ++k)
+                    umma_bf16(tmem + kColS, umma_desc_sw128(tile_addr(in + kInB) + (uint32_t)k * 2048, kTile, 1024),
+                              umma_desc_sw128(tile_addr(kTXH) + (uint32_t)k * 2048, kTile, 1024), i_g4,
+                              (had_state || k > 0) ? 1u : 0u);
+                umma_commit(&bar_g4);
+                // Y (+)= (M hi + M lo) X, M read from tensor memory
+                ok = mbar_wait_bounded(&bar_m, par);
+                if (!ok) break;
+                tc_fence_after_sync();
+#pragma unroll 1
+                for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+                    for (int k = 0; k < 8; ++k)
+                        umma_bf16_ts(tmem + kColYo, tmem + (part ? kColMlo : kColMhi) + 8 * k,
+                                     umma_desc_sw128(tile_addr(in + kInX) + (uint32_t)k * 2048, kTile, 1024), i_g2,
+                                     (had_state || part || k) ? 1u : 0u);
+                umma_commit(&bar_g2);
             }
+            if (!ok) s_ok = 0;
+        }
+        __syncwarp();
+    } else {
+        // ---------------- 256 worker threads ----------------
+        const float A2 = a.A[h] * kLog2e;
+        const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
+        const float Dh = a.D ? a.D[h] : 0.f;
+        const __nv_bfloat16* dt = static_cast<const __nv_bfloat16*>(a.dt);
+        const __nv_bfloat16* zp = static_cast<const __nv_bfloat16*>(a.z);
+        Tout* yp = static_cast<Tout*>(a.y);
+        auto load_dt = [&](int c) -> float {  // raw dt of token row `tid` of chunk c (tid < 128)
+            const int64_t t = (int64_t)c * kQ + tid;
+            return (c < nchunks && t < L) ? __bfloat162float(dt[((int64_t)b * L + t) * H + h]) : 0.f;
+        };
+        auto worker_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory"); };
+
+        bool ok = true;
+        float dt_raw = tid < kQ ? load_dt(0) : 0.f;  // raw dt of the next chunk to be summed
+        // Delta and the running sum of Delta*A over chunk c for token `tid` (warps 0-3; the
+        // other warps only take part in the barrier), kept in registers until the chunk starts.
+        float nx_dl = 0.f, nx_cs = 0.f;
+        auto chunk_sums = [&](int c) {
+            if (tid < kQ) {
+                const float v = dt_raw + bias;
+                nx_dl = ((int64_t)c * kQ + tid < L) ? (a.softplus ? softplus_f<true>(v) : v) : 0.f;
+                dt_raw = load_dt(c + 1);
+                float s = nx_dl * A2;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float n = __shfl_up_sync(0xffffffffu, s, o);
+                    if (lane >= o) s += n;
+                }
+                if (lane == 31) s_wsum[warp] = s;
+                nx_cs = s;
+            }
+            worker_sync();
+            if (tid < kQ) {
+                float off = 0.f;
+                for (int w = 0; w < warp; ++w) off += s_wsum[w];
+                nx_cs += off;
+            }
+        };
+        if (nchunks > 0) chunk_sums(0);
+        // z of this thread's outputs of the current chunk (row i = row, headdim 32*half..+31).
+        uint4 z0 = make_uint4(0u, 0u, 0u, 0u), z1 = z0, z2 = z0, z3 = z0;
+        if (zp && row < L) {
+            const uint4* zq = reinterpret_cast<const uint4*>(zp + ((int64_t)b * L + row) * H * kHeadDim +
+                                                             (int64_t)h * kHeadDim + 32 * half);
+            z0 = zq[0]; z1 = zq[1]; z2 = zq[2]; z3 = zq[3];
+        }
+        for (int c = 0; c < nchunks; ++c) {
+            const int64_t t0 = (int64_t)c * kQ;
+            const uint32_t par = (uint32_t)(c & 1);
+            const int in = kInTiles * (c & 1);
+            const bool had_state = c > 0 || init_state;
+            if (tid < kQ) {  // publish this chunk's sums (the last reads of the previous ones are done)
+                s_dl[tid] = nx_dl;
+                s_cs[tid] = nx_cs;
+            }
+            worker_sync();
+            const float cs_last = s_cs[kQ - 1];
+
+            // w * X (hi / lo) for the state update (warps 0-3, row j = row), and the decay of the
+            // carried state by exp(cs_last) (warps 4-7, state row n = row).
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1)));
+            if (ok && half == 0) {
+                const float w = ex2_approx(cs_last - s_cs[row]) * s_dl[row];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float v[8];
+                    unpack8(*reinterpret_cast<const uint4*>(tile(in + kInX) + sw128(row, ch)), v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] *= w;
+                    uint4 hi, lo;
+                    split8(v, hi, lo);
+                    *reinterpret_cast<uint4*>(tile(kTXH) + sw128(row, ch)) = hi;
+                    *reinterpret_cast<uint4*>(tile(kTXL) + sw128(row, ch)) = lo;
+                }
+            } else if (ok && had_state) {
+                const float dec = ex2_approx(cs_last);
+#pragma unroll 1
+                for (int part = 0; part < 4; ++part) {
+                    float v[32];
+                    tmem_ld32(tmem + tlane + kColS + 32 * part, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= dec;
+                    tmem_st32(tmem + tlane + kColS + 32 * part, v);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_x);
+
+            // M = G * exp(cs_i - cs_j) * Delta_j (j <= i) as bf16 hi / lo pairs (row i = row,
+            // columns 64*half..+63), and with a carried state Y = exp(cs_i) * (C S hi + C S lo).
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g1, par));
+            tc_fence_after_sync();
+            if (ok) {
+                const float cs_i = s_cs[row];
+                const bool live = t0 + row < L;
+                const bool any = 64 * half <= quarter * 32 + 31;  // a column of this half is on or below the diagonal
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    uint32_t gp[32];
+                    if (any) {
+                        tmem_ld32_async(tmem + tlane + kColG + 64 * half + 32 * part, gp);
+                        tmem_wait_ld();
+                    }
+                    uint32_t mh[16], ml[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = 64 * half + 32 * part + 2 * e;
+                        float2 m = make_float2(0.f, 0.f);
+                        if (any && live && j <= row) {
+                            const float2 cj = *reinterpret_cast<const float2*>(&s_cs[j]);
+                            const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
+                            const float2 dec = make_float2(ex2_approx(cs_i - cj.x),
+                                                           j + 1 <= row ? ex2_approx(cs_i - cj.y) : 0.f);
+                            const float2 gv = make_float2(__uint_as_float(gp[2 * e]), __uint_as_float(gp[2 * e + 1]));
+                            m = __fmul2_rn(__fmul2_rn(gv, dec), dj);
+                        }
+                        split2(m, mh[e], ml[e]);
+                    }
+                    tmem_st16_async(tmem + tlane + kColMhi + 32 * half + 16 * part, mh);
+                    tmem_st16_async(tmem + tlane + kColMlo + 32 * half + 16 * part, ml);
+                }
+                if (had_state) {
+                    uint32_t yh[32], yl[32];
+                    tmem_ld32_async(tmem + tlane + kColYo + 32 * half, yh);
+                    tmem_ld32_async(tmem + tlane + kColYo + 64 + 32 * half, yl);
+                    tmem_wait_ld();
+                    const float e = ex2_approx(cs_i);
+                    float ys[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ys[i] = e * (__uint_as_float(yh[i]) + __uint_as_float(yl[i]));
+                    tmem_st32(tmem + tlane + kColYo + 32 * half, ys);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bar_m);
+
+            const int64_t t_row = t0 + row;
+            const int64_t yoff = ((int64_t)b * L + t_row) * H * kHeadDim + (int64_t)h * kHeadDim + 32 * half;
+
+            // The updated state -> hi / lo for the next chunk's C S.
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g4, par));
+            tc_fence_after_sync();
+            if (ok) {
+                uint32_t ra[32], rb[32];
+                tmem_ld32_async(tmem + tlane + kColS + 32 * half, ra);
+                tmem_ld32_async(tmem + tlane + kColS + 64 + 32 * half, rb);
+                tmem_wait_ld();
+                float sa[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sa[i] = __uint_as_float(ra[i]) + __uint_as_float(rb[i]);
+                put_state_split(sa);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_s);
+            // The next chunk's Delta and running sums, while M X runs.
+            if (c + 1 < nchunks) chunk_sums(c + 1);
+
+            // y = Y + D x, times silu(z): row i = row, headdim columns 32*half..+31.
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g2, par));
+            tc_fence_after_sync();
+            if (ok) {
+                float yd[32];
+                tmem_ld32(tmem + tlane + kColYo + 32 * half, yd);
+                if (t_row < L) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float xv[8], zv[8];
+                        unpack8(*reinterpret_cast<const uint4*>(tile(in + kInX) + sw128(row, 4 * half + q)), xv);
+                        if (zp) unpack8(q == 0 ? z0 : q == 1 ? z1 : q == 2 ? z2 : z3, zv);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            float y = fmaf(Dh, xv[i], yd[8 * q + i]);
+                            if (zp) y *= silu_f<false>(zv[i]);
+                            yd[8 * q + i] = y;
+                        }
+                    }
+                    store32<Tout>(yp + yoff, yd);
+                }
+            }
+            if (zp && c + 1 < nchunks && t_row + kQ < L) {  // z of the next chunk
+                const uint4* zq = reinterpret_cast<const uint4*>(zp + yoff + (int64_t)kQ * H * kHeadDim);
+                z0 = zq[0]; z1 = zq[1]; z2 = zq[2]; z3 = zq[3];
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bar_y);
+            if (!ok) break;
         }
 
-        // The updated state -> hi / lo for the next chunk's C S.
-        ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g4, par));
-        tc_fence_after_sync();
-        if (ok) {
+        if (ok && a.final_state) {  // Sa + Sb [n][p] -> final_state (p, n)
             float v[32];
-            tmem_ld32(tmem + tlane + kColS + 32 * half, v);
-            put_state_split(v);
-        }
-        has_state = true;
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        if (!__syncthreads_and(ok)) { ok = false; break; }
-        tc_fence_after_sync();
-    }
-
-    if (ok && a.final_state) {  // S[n][p] -> final_state (p, n)
-        float v[32];
-        if (has_state) {
-            tmem_ld32(tmem + tlane + kColS + 32 * half, v);
-        } else {
+            if (nchunks > 0 || init_state) {
+                float sb[32];
+                tmem_ld32(tmem + tlane + kColS + 32 * half, v);
+                tmem_ld32(tmem + tlane + kColS + 64 + 32 * half, sb);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        }
-        float* dst = a.final_state + ((int64_t)b * H + h) * kHeadDim * kSsdState + row;
+                for (int i = 0; i < 32; ++i) v[i] += sb[i];
+            } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * half + i) * kSsdState] = v[i];
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
+            float* dst = a.final_state + ((int64_t)b * H + h) * kHeadDim * kSsdState + row;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * half + i) * kSsdState] = v[i];
+        }
+        if (!ok) s_ok = 0;
     }
-    if (!ok && tid == 0) atomicOr(&g_ssd_status, 1u);
     tc_fence_before_sync();
     __syncthreads();
+    if (tid == 0 && !s_ok) atomicOr(&g_ssd_status, 1u);
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
