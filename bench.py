@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 from workloads import DECODE_CONFIG, make_decode_layer_params, make_decode_state  # noqa: E402
-from workloads import make_decode_tokens, make_scan_inputs, scan_config  # noqa: E402
+from workloads import make_decode_tokens, make_scan_inputs, scan_config, ssd_config  # noqa: E402
 
 METRIC = "selective-scan B·D·L elem/s & achieved HBM GB/s (% of peak); decode steps/s"
 SM_PER_GPU_FALLBACK = 148
@@ -237,6 +237,48 @@ def time_bwd(cfg, steps, warmup, x, flush, stream):
     return [a.elapsed_time(b) for a, b in ev], 2
 
 
+def ssd_work(cfg):
+    """Algorithmic tensor FLOPs (the four chunk products once each, no hi/lo split), FLOPs the
+    tensor cores execute (C S, M X and B^T (w X) twice: bf16 hi and lo parts), and compulsory
+    HBM bytes (x, z read and y written once, bf16; B, C, dt read once) of one SSD call."""
+    Q, N, P = 128, cfg.dstate, cfg.headdim
+    chunks = cfg.batch * cfg.nheads * ((cfg.seqlen + Q - 1) // Q)
+    g1, g2, g3, g4 = 2 * Q * Q * N, 2 * Q * Q * P, 2 * Q * N * P, 2 * Q * N * P
+    alg = chunks * (g1 + g2 + g3 + g4)
+    executed = chunks * (g1 + 2 * (g2 + g3 + g4))
+    byts = (cfg.elements * 2 * 3 + cfg.batch * cfg.seqlen * cfg.ngroups * N * 2 * 2 +
+            cfg.batch * cfg.seqlen * cfg.nheads * 2 + cfg.batch * cfg.nheads * P * N * 4)
+    return alg, executed, byts
+
+
+def time_ssd(cfg, steps, warmup, flush, stream):
+    """ssd_chunk_scan_fwd on the Mamba-2 layer workload, L2 flushed before every step."""
+    from selective_state_space_110_b300 import ssd_chunk_scan_fwd
+    from workloads import make_ssd_inputs
+    x = make_ssd_inputs(cfg, "cuda")
+    y = torch.empty(x["x"].shape, dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty(cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate, device="cuda")
+
+    def call():
+        ssd_chunk_scan_fwd(x["x"], x["dt"], x["A"], x["B"], x["C"], x["D"], x["z"], x["dt_bias"],
+                           x["dt_softplus"], y=y, final_state=fin, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.fill_(1)
+            call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            flush.fill_(1)
+            ev[s][0].record(stream)
+            call()
+            ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev], 1
+
+
 def time_scan_e2e(cfg, steps, warmup, x, stream):
     """Same scan through the public API from pinned host buffers: every step copies the
     step's inputs host->device, runs the scan and copies y and the final state back."""
@@ -368,6 +410,40 @@ def cpu_baseline(cfg, x, target_s=12.0):
                       f"({elems} elements, {t:.1f} s)"}
 
 
+def ssd_summary(scfg, ms, launches, world, scan_ms, scan_cfg):
+    alg, executed, byts = ssd_work(scfg)
+    _, _, tflops_peak = read_tensor_peak()
+    hbm_peak, _ = read_peaks()
+    sec = ms * 1e-3
+    out = {"what": "ssd_chunk_scan_fwd: Mamba-2 SSD layer, 128-token chunks on tcgen05, "
+                   "state in tensor memory (ssd_fwd_kernel)",
+           "workload": scfg.name,
+           "shape": {"batch": scfg.batch, "seqlen": scfg.seqlen, "nheads": scfg.nheads,
+                     "headdim": scfg.headdim, "ngroups": scfg.ngroups, "dstate": scfg.dstate},
+           "ms_per_step": round(ms, 4),
+           "elem_per_s": round(world * scfg.elements / sec, 1),
+           "tensor_tflops_algorithmic": round(alg / sec / 1e12, 1),
+           "tensor_tflops_executed": round(executed / sec / 1e12, 1),
+           "tensor_frac": round(executed / sec / 1e12 / tflops_peak, 4),
+           "tensor_peak_tflops": tflops_peak,
+           "achieved_gbs": round(byts / sec / 1e9, 1),
+           "hbm_frac": round(byts / sec / 1e9 / hbm_peak, 4),
+           "launches_per_step": launches}
+    if scfg.elements == scan_cfg.elements:
+        out["vs_s6_scan_same_elements"] = round(scan_ms / ms, 3)
+    return out
+
+
+def read_tensor_peak():
+    """(sustained, source, burst) dense bf16 TFLOP/s: measured, else the fallback figures."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops_sustained"), "measured", float(d["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1400.0, "fallback", 1800.0
+
+
 def run_ours(args):
     world, rank, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -390,6 +466,9 @@ def run_ours(args):
     value = elems / (ms_step * 1e-3)
     clocks = clk.summary()
 
+    ssd_cfg = ssd_config(args.ssd_workload)
+    ssd_times, ssd_launches = time_ssd(ssd_cfg, max(3, min(args.steps, 10)), 3, flush, stream)
+    ssd_ms = max_over_ranks(statistics.median(ssd_times), world)
     bwd_times, bwd_launches = time_bwd(cfg, max(3, min(args.steps, 10)), 3, x, flush, stream)
     bwd_ms = max_over_ranks(statistics.median(bwd_times), world)
     e2e_ms, h2d, d2h = time_scan_e2e(cfg, max(2, min(args.steps, 10)), 2, x, stream)
@@ -455,6 +534,7 @@ def run_ours(args):
                      "alu_note": f"ceiling {BWD_ELEM_PER_CLK_PER_SM:.3f} elem/clk/SM: 48 SFU exp2 "
                                  "per element (3 passes x 16 states) at 32 per clock per SM",
                      "launches_per_step": bwd_launches},
+        "ssd": ssd_summary(ssd_cfg, ssd_ms, ssd_launches, world, kern_ms, cfg),
         "decode": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim, **dec},
         "decode_conv": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim,
                         "what": "ssm_conv_state_update: width-4 convolution step + state update",
@@ -471,6 +551,17 @@ def run_profile(args):
     from selective_state_space_110_b300 import ssm_scan_fwd, ssm_state_update
     cfg = scan_config(args.workload)
     x = make_scan_inputs(cfg, "cuda")
+    if args.profile_op == "ssd":
+        from selective_state_space_110_b300 import ssd_chunk_scan_fwd
+        from workloads import make_ssd_inputs
+        scfg = ssd_config(args.ssd_workload)
+        xs = make_ssd_inputs(scfg, "cuda")
+        for _ in range(2):
+            y, _ = ssd_chunk_scan_fwd(xs["x"], xs["dt"], xs["A"], xs["B"], xs["C"], xs["D"], xs["z"],
+                                      xs["dt_bias"], xs["dt_softplus"])
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": scfg.name, "op": "ssd", "finite": bool(torch.isfinite(y).all().item())}))
+        return
     if args.profile_op == "bwd":
         from selective_state_space_110_b300 import ssm_scan_bwd
         gen = torch.Generator("cuda").manual_seed(cfg.seed + 7)
@@ -547,8 +638,10 @@ def main():
                     help="untimed back-to-back scans before the timed steps (clock sampling)")
     ap.add_argument("--profile", action="store_true",
                     help="run one scan of the workload and exit (for ncu captures)")
-    ap.add_argument("--profile-op", default="fwd", choices=["fwd", "bwd"],
-                    help="with --profile: the forward scan (default) or the backward")
+    ap.add_argument("--profile-op", default="fwd", choices=["fwd", "bwd", "ssd"],
+                    help="with --profile: the forward scan (default), the backward, or the SSD "
+                         "layer (--ssd-workload)")
+    ap.add_argument("--ssd-workload", default="ssd1_mamba2_2p7b")
     args = ap.parse_args()
     if args.profile:
         run_profile(args)
