@@ -38,6 +38,9 @@ SM_PER_GPU_FALLBACK = 148
 ALU_ELEM_PER_CLK_PER_SM = 2.0  # 16 SFU exp2 (32/clk/SM) and 64 FP32 lane-ops (128/clk/SM) per element
 BWD_ELEM_PER_CLK_PER_SM = 32.0 / 48.0  # backward: 48 SFU exp2 per element at 32/clk/SM
 L2_FLUSH_BYTES = 256 << 20
+# dram__bytes_read.sum + dram__bytes_write.sum of one scan_kernel launch, from the ncu capture
+# summarised in profiles/scan_fwd_c2_mamba2p8b.md (same kernel code): 252.8 MB + 50.1 MB.
+SCAN_TRAFFIC_BYTES = {"c2_mamba2p8b": 302_900_000}
 
 
 # ------------------------------------------------------------------------------------------
@@ -514,7 +517,8 @@ def run_ours(args):
         "achieved_gbs": round(achieved, 1),
         "hbm_frac": round(achieved / hbm_peak, 4),
         "roofline": {"bound": "alu", "achieved": round(achieved, 1), "peak": round(alu_peak_gbs, 1),
-                     "unit": "GB/s", "frac": round(achieved / alu_peak_gbs, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / alu_peak_gbs, 4),
+                     "traffic": SCAN_TRAFFIC_BYTES.get(cfg.name),
                      "kernel": "scan_kernel (full pass)",
                      "peak_note": f"ALU ceiling {ALU_ELEM_PER_CLK_PER_SM} elem/clk/SM x {sms} SMs x "
                                   f"{sm_mhz:.0f} MHz, as GB/s of compulsory bytes",
