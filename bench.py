@@ -283,41 +283,33 @@ def time_ssd(cfg, steps, warmup, flush, stream):
 
 
 def time_scan_e2e(cfg, steps, warmup, x, stream):
-    """Same scan through the public API from pinned host buffers: every step copies the
-    step's inputs host->device, runs the scan and copies y and the final state back."""
-    from selective_state_space_110_b300 import ssm_scan_fwd, workspace_size
-    names = ["u", "delta", "z", "B", "C"]
-    host = {k: x[k].cpu().pin_memory() for k in names if x[k] is not None}
-    dev = {k: torch.empty_like(x[k]) for k in host}
+    """The same scan through the host-buffer entry point ssm_scan_fwd_host: every step uploads
+    the step's inputs from pinned host memory, scans, and downloads y and the final state (the
+    library pipelines the copies with the scan, one sequence at a time)."""
+    from selective_state_space_110_b300 import host_workspace_size, ssm_scan_fwd_host
+    names = ["u", "delta", "A", "B", "C", "D", "z", "delta_bias"]
+    host = {k: (x[k].cpu().pin_memory() if x[k] is not None else None) for k in names}
     out_dtype = torch.bfloat16 if cfg.out_dtype == "bf16" else torch.float32
-    out = torch.empty(cfg.batch, cfg.dim, cfg.seqlen, dtype=out_dtype, device="cuda")
-    fin = torch.empty(cfg.batch, cfg.dim, cfg.dstate, dtype=torch.float32, device="cuda")
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
-    ws_n = workspace_size(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen)
-    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda") if ws_n else None
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    out_h = torch.empty(cfg.batch, cfg.dim, cfg.seqlen, dtype=out_dtype).pin_memory()
+    fin_h = torch.empty(cfg.batch, cfg.dim, cfg.dstate, dtype=torch.float32).pin_memory()
+    ws = torch.empty(host_workspace_size(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen,
+                                         x["u"].dtype, out_dtype), dtype=torch.uint8, device="cuda")
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
 
     def step():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        ssm_scan_fwd(dev["u"], dev["delta"], x["A"], dev["B"], dev["C"], x["D"], dev.get("z"),
-                     x["delta_bias"], x["delta_softplus"], out=out, final_state=fin,
-                     workspace=ws, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        fin_h.copy_(fin, non_blocking=True)
+        ssm_scan_fwd_host(host["u"], host["delta"], host["A"], host["B"], host["C"], host["D"],
+                          host["z"], host["delta_bias"], x["delta_softplus"], out=out_h,
+                          final_state=fin_h, workspace=ws, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
+    for _ in range(warmup):
+        step()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        for _ in range(steps):
-            step()
-        b.record(stream)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b) / steps, h2d, d2h
 

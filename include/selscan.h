@@ -188,6 +188,34 @@ selscan_status ssm_scan_fwd_no_alloc(const void* u, const void* delta, const flo
                                      selscan_stream_t stream);
 
 /*
+ * ssm_scan_fwd_host: ssm_scan_fwd on HOST buffers. The paper has no counterpart; it serves
+ * callers whose activations live in host memory. Arguments, layouts and results are those of
+ * ssm_scan_fwd, except that u, delta, A, B, C, D, z, delta_bias, initial_state, out and
+ * final_state are host pointers (pinned memory, e.g. cudaHostAlloc, lets the copies overlap the
+ * scan; pageable memory works but serialises them). The batch is cut into slices of one
+ * sequence: each slice is uploaded, scanned by ssm_scan_fwd on `stream` and downloaded, with the
+ * upload of the next slice and the download of the previous one running during the scan on two
+ * copy streams the library creates once per device. When the call returns the work is queued;
+ * the host outputs are valid once `stream` has completed. Calls on one device must not overlap
+ * (they share those streams and their events).
+ *
+ * workspace: device memory, 256-byte aligned, of at least ssm_scan_fwd_host_workspace_size()
+ * bytes (two slices of inputs and outputs plus A, D, delta_bias); SELSCAN_ERR_WORKSPACE
+ * otherwise. Its contents on entry do not matter.
+ */
+selscan_status ssm_scan_fwd_host(const void* u, const void* delta, const float* A, const void* B,
+                                 const void* C, const float* D, const void* z,
+                                 const float* delta_bias, int delta_softplus, void* out,
+                                 float* final_state, int64_t batch, int64_t dim, int64_t dstate,
+                                 int64_t seqlen, selscan_dtype in_dtype, selscan_dtype out_dtype,
+                                 const float* initial_state, void* workspace,
+                                 size_t workspace_bytes, selscan_stream_t stream);
+
+/* Device workspace bytes ssm_scan_fwd_host needs (0 for invalid arguments). */
+size_t ssm_scan_fwd_host_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                        selscan_dtype in_dtype, selscan_dtype out_dtype);
+
+/*
  * ssm_scan_bwd: gradients of the selective scan (Euler), for training. "A Scan on the Chip"
  * (world.lapla.si) keeps the expanded state out of main memory in the forward pass and computes
  * it again in the backward pass ("recomputation"); this call does the same: it stores the state

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libselscan.so")
 SOURCES = ["selscan_api.cu", "scan_fwd.cu", "state_update.cu", "scan_fwd_no_alloc.cu",
-           "scan_bwd.cu", "ssd_fwd.cu"]
+           "scan_bwd.cu", "ssd_fwd.cu", "scan_host.cu"]
 HEADERS = ["selscan_device.cuh", "selscan_launch.h", "sm100_async.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",

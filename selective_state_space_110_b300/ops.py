@@ -319,3 +319,68 @@ def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus
             _stream_handle(stream))
     _lib.check("ssd_chunk_scan_fwd", st)
     return y, final_state
+
+
+def _check_host(name, t, dtype=None, shape=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def host_workspace_size(batch, dim, dstate, seqlen, in_dtype, out_dtype) -> int:
+    """Device workspace bytes ssm_scan_fwd_host needs."""
+    return int(_lib.lib().ssm_scan_fwd_host_workspace_size(batch, dim, dstate, seqlen,
+                                                           _DT[in_dtype], _DT[out_dtype]))
+
+
+def ssm_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                      out=None, final_state=None, initial_state=None, workspace=None,
+                      out_dtype=None, return_final_state=True, device=None, stream=None):
+    """ssm_scan_fwd on host (CPU) tensors, pinned for overlap: the library uploads, scans and
+    downloads slice by slice. Returns (out, final_state or None) as host tensors; they are valid
+    after the stream (default: the current stream of `device`) has been synchronised."""
+    if u.dim() != 3:
+        raise ValueError("u must be (batch, dim, seqlen)")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    in_dt = u.dtype
+    if in_dt not in _DT:
+        raise ValueError(f"unsupported input dtype {in_dt}")
+    _check_host("u", u, in_dt, (batch, dim, seqlen))
+    _check_host("delta", delta, in_dt, (batch, dim, seqlen))
+    _check_host("A", A, torch.float32, (dim, dstate))
+    _check_host("B", B, in_dt, (batch, dstate, seqlen))
+    _check_host("C", C, in_dt, (batch, dstate, seqlen))
+    _check_host("D", D, torch.float32, (dim,))
+    _check_host("z", z, in_dt, (batch, dim, seqlen))
+    _check_host("delta_bias", delta_bias, torch.float32, (dim,))
+    _check_host("initial_state", initial_state, torch.float32, (batch, dim, dstate))
+    odt = out_dtype or in_dt
+    if out is None:
+        out = torch.empty((batch, dim, seqlen), dtype=odt).pin_memory()
+    _check_host("out", out, None, (batch, dim, seqlen))
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, dim, dstate), dtype=torch.float32).pin_memory()
+    _check_host("final_state", final_state, torch.float32, (batch, dim, dstate))
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        need = host_workspace_size(batch, dim, dstate, seqlen, in_dt, out.dtype)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _check_dev("workspace", workspace, None, None, dev)
+        st = _lib.lib().ssm_scan_fwd_host(
+            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            _flags(delta_softplus, False), _ptr(out), _ptr(final_state), batch, dim, dstate,
+            seqlen, _DT[in_dt], _DT[out.dtype], _ptr(initial_state), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _lib.check("ssm_scan_fwd_host", st)
+    return out, final_state

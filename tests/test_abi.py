@@ -270,3 +270,36 @@ def test_ssd_valid_args_reach_the_device_check(lib):
         pytest.skip("device present: covered by the GPU tests")
     assert call_ssd(lib) == CUDA
     assert call_ssd(lib, seqlen=0, x=None, dt=None, B=None, C=None, y=None) == CUDA
+
+
+def call_host(lib, **kw):
+    a = dict(u=fake(0), delta=fake(1), A=fake(2), B=fake(3), C=fake(4), D=fake(5), z=fake(6),
+             delta_bias=fake(7), flags=1, out=fake(8), fin=fake(9), batch=2, dim=64, dstate=16,
+             seqlen=128, in_dtype=_lib.BF16, out_dtype=_lib.BF16, h0=None, ws=fake(10),
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.ssm_scan_fwd_host(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                 a["delta_bias"], a["flags"], a["out"], a["fin"], a["batch"],
+                                 a["dim"], a["dstate"], a["seqlen"], a["in_dtype"], a["out_dtype"],
+                                 a["h0"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dstate=8), UNSUP),
+    (dict(in_dtype=4), UNSUP),
+    (dict(batch=0), INVALID),
+    (dict(u=None), INVALID),
+    (dict(A=None), INVALID),
+    (dict(ws=None), WS),
+    (dict(ws_bytes=4096), WS),
+    (dict(ws=fake(10) + 16), ALIGN),       # the workspace must be 256-byte aligned
+])
+def test_host_scan_rejects(lib, kw, expect):
+    assert call_host(lib, **kw) == expect
+
+
+def test_host_workspace_size(lib):
+    n = lib.ssm_scan_fwd_host_workspace_size(2, 64, 16, 128, _lib.BF16, _lib.F32)
+    # two slots of (u, delta, z, B, C, y, final and initial state) plus A, D, bias
+    assert n >= 2 * (3 * 64 * 128 * 2 + 2 * 16 * 128 * 2 + 64 * 128 * 4 + 2 * 64 * 16 * 4)
+    assert lib.ssm_scan_fwd_host_workspace_size(2, 64, 8, 128, _lib.BF16, _lib.F32) == 0
