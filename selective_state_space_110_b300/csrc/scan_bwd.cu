@@ -18,6 +18,14 @@
 // while the current chunk computes. B and C of a chunk are staged in shared memory one row per
 // token (BcStage).
 //
+// Long sequences with few rows are cut into time segments that run in parallel (grid.y), as in
+// the forward: a forward pass over segments 0..S-2 from a zero state keeps each one's local end
+// state and summed Delta; a reverse pass over segments 1..S-1 from a zero adjoint keeps each
+// one's local start adjoint (the adjoint of the state before the segment) and summed Delta. The
+// full backward of segment s then starts its forward from the fold of the earlier segments,
+// h <- exp(A sum Delta) h + h_local_end, and its adjoint from the fold of the later ones,
+// g <- g_local_start + exp(A sum Delta) g (the adjoint recurrence is linear in g as well).
+//
 // dB and dC are sums over every channel of a batch: each warp reduce-scatters its 8 rows' terms
 // in three shuffle rounds (lane (q, g) ends with one of the 32 dB | dC sums of the token), the
 // CTA adds its 4 warps in shared memory and writes one partial per token and value. dA, dD and
@@ -158,12 +166,18 @@ struct BcStage<__nv_bfloat16> {
     }
 };
 
-template <typename Tin, typename Tg, bool kPrecise, bool kVec>
+// Modes of the backward kernel: the full backward of a segment, the forward local-end pass
+// (segments 0..S-2) and the adjoint local-start pass (segments 1..S-1).
+enum BwdMode : int { kBwdFull = 0, kBwdFwdLocal = 1, kBwdAdjLocal = 2 };
+
+template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode>
 __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const BwdArgs a) {
     __shared__ __align__(16) BwdSmem sm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = lane >> 2, g = lane & 3;
-    const int64_t b = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int seg = kMode == kBwdAdjLocal ? (int)blockIdx.y + 1 : (int)blockIdx.y;
+    const int nprev = a.nseg - 1;
     const int64_t d_raw = (int64_t)blockIdx.x * kBRows + warp * 8 + quad;
     const bool active = d_raw < a.dim;
     const int64_t d = active ? d_raw : 0;
@@ -171,6 +185,9 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
     const int64_t L = a.seqlen;
     const int64_t Lr = active ? L : 0;  // tokens of this lane's row (none past dim)
     const int nchunks = (int)((L + kBChunk - 1) / kBChunk);
+    const int seg_chunks = (int)(a.seg_len / kBChunk);
+    const int c_begin = seg * seg_chunks;  // this segment's chunks: [c_begin, c_end)
+    const int c_end = min(nchunks, c_begin + seg_chunks);
 
     const float4 A4 = *reinterpret_cast<const float4*>(a.A + d * kN + 4 * g);
     const float Av[4] = {A4.x, A4.y, A4.z, A4.w};
@@ -201,32 +218,69 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
     auto put_bc = [&](int buf, bool withC) {
         if (withC || s_ch < 4) Stage::put(&sm.bc[buf][0][0], s_tt, s_ch, sb);
     };
-    auto decay = [&](float s, int n) -> float {  // exp(Delta A_n), s = Delta * kScale
-        return kPrecise ? expf(s * Av[n]) : ex2_approx(s * Av[n]);
+    // v * exp(Delta A_n) + add (s = Delta * kScale). fp32 inputs write exp as 1 + expm1: the decay's distance from 1
+    // keeps full relative precision, so a slowly decaying state or adjoint accumulates no bias
+    // from rounding the decay itself over thousands of tokens.
+    auto decay_fma = [&](float s, int n, float v, float add) -> float {
+        if (kPrecise) return fmaf(expm1f(s * Av[n]), v, v) + add;
+        return fmaf(ex2_approx(s * Av[n]), v, add);
     };
     auto delta_of = [&](float x) -> float {
         if (!a.softplus) return x;
         return kPrecise ? softplus_f<true>(x) : softplus2(make_float2(x, x)).x;
     };
 
-    // ---- checkpoint pass: the forward state before every chunk ----
-    float h[4];
-    {
-        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.initial_state && active)
-            s0 = *reinterpret_cast<const float4*>(a.initial_state + row * kN + 4 * g);
-        h[0] = s0.x; h[1] = s0.y; h[2] = s0.z; h[3] = s0.w;
-    }
-    {
-        Quad4<Tin, kVec> pd, pu;
-        if (nchunks > 0) {
-            pd.load(d_row, 4 * g, Lr);
-            pu.load(u_row, 4 * g, Lr);
-            fetch_bc(0, false);
+    // exp(A_n * S) for a summed Delta S (fold of a segment).
+    auto seg_decay_fma = [&](float S, int n, float v, float add) -> float {
+        if (kPrecise) return fmaf(expm1f(S * Av[n]), v, v) + add;
+        return fmaf(ex2_approx(S * kLog2e * Av[n]), v, add);
+    };
+    // Kahan sum of Delta over this lane's owned tokens (local passes).
+    float dsum = 0.f, dsum_c = 0.f;
+    auto add_delta = [&](const float (&dl)[4]) {
+        const float part_sum = (dl[0] + dl[1] + dl[2] + dl[3]) * (1.f / kScale);
+        const float yk = part_sum - dsum_c;
+        const float tk = dsum + yk;
+        dsum_c = (tk - dsum) - yk;
+        dsum = tk;
+    };
+    auto quad_delta_sum = [&]() -> float {
+        float v = dsum - dsum_c;
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        return v;
+    };
+
+    float h[4] = {0.f, 0.f, 0.f, 0.f};
+    if (kMode == kBwdFull) {  // initial state, then the fold of the earlier segments
+        if (a.initial_state && active) {
+            const float4 s0 = *reinterpret_cast<const float4*>(a.initial_state + row * kN + 4 * g);
+            h[0] = s0.x; h[1] = s0.y; h[2] = s0.z; h[3] = s0.w;
         }
-        for (int c = 0; c < nchunks; ++c) {
+        for (int k = 0; k < seg && active; ++k) {
+            const float S = a.ws_fsum[row * nprev + k];
+            const float4 hl = *reinterpret_cast<const float4*>(a.ws_hloc + (row * nprev + k) * kN + 4 * g);
+            h[0] = seg_decay_fma(S, 0, h[0], hl.x);
+            h[1] = seg_decay_fma(S, 1, h[1], hl.y);
+            h[2] = seg_decay_fma(S, 2, h[2], hl.z);
+            h[3] = seg_decay_fma(S, 3, h[3], hl.w);
+        }
+    }
+
+    // ---- checkpoint pass: the forward state before every chunk (the local-end pass: the
+    // forward only) ----
+    if (kMode != kBwdAdjLocal) {
+        Quad4<Tin, kVec> pd, pu;
+        if (c_begin < c_end) {
+            const int64_t tl = (int64_t)c_begin * kBChunk + 4 * g;
+            pd.load(d_row, tl, Lr);
+            pu.load(u_row, tl, Lr);
+            fetch_bc(c_begin, false);
+        }
+        for (int c = c_begin; c < c_end; ++c) {
             const int64_t tl = (int64_t)c * kBChunk + 4 * g;
-            if (active) *reinterpret_cast<float4*>(ckpt + (int64_t)c * kN) = make_float4(h[0], h[1], h[2], h[3]);
+            if (kMode == kBwdFull && active)
+                *reinterpret_cast<float4*>(ckpt + (int64_t)c * kN) = make_float4(h[0], h[1], h[2], h[3]);
             put_bc(c & 1, false);
             float dl[4], kl[4];
 #pragma unroll
@@ -235,7 +289,8 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
                 dl[i] = dt * kScale;
                 kl[i] = dt * pu.get(i);
             }
-            if (c + 1 < nchunks) {
+            if (kMode == kBwdFwdLocal) add_delta(dl);
+            if (c + 1 < c_end) {
                 pd.load(d_row, tl + kBChunk, Lr);
                 pu.load(u_row, tl + kBChunk, Lr);
                 fetch_bc(c + 1, false);
@@ -247,20 +302,39 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
                 const float s = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
                 const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
                 const float4 Bv = Stage::get_b(bcb, t, g);
-                h[0] = fmaf(decay(s, 0), h[0], k * Bv.x);
-                h[1] = fmaf(decay(s, 1), h[1], k * Bv.y);
-                h[2] = fmaf(decay(s, 2), h[2], k * Bv.z);
-                h[3] = fmaf(decay(s, 3), h[3], k * Bv.w);
+                h[0] = decay_fma(s, 0, h[0], k * Bv.x);
+                h[1] = decay_fma(s, 1, h[1], k * Bv.y);
+                h[2] = decay_fma(s, 2, h[2], k * Bv.z);
+                h[3] = decay_fma(s, 3, h[3], k * Bv.w);
             }
         }
+    }
+    if (kMode == kBwdFwdLocal) {
+        const float S = quad_delta_sum();
+        if (active) {
+            *reinterpret_cast<float4*>(a.ws_hloc + (row * nprev + seg) * kN + 4 * g) =
+                make_float4(h[0], h[1], h[2], h[3]);
+            if (g == 0) a.ws_fsum[row * nprev + seg] = S;
+        }
+        return;
     }
     __syncthreads();  // the last chunk's readers of the staging buffers are done
 
     // ---- reverse pass ----
     float gad[4] = {0.f, 0.f, 0.f, 0.f};  // adjoint of the state
-    if (a.dfinal_state && active) {
-        const float4 f = *reinterpret_cast<const float4*>(a.dfinal_state + row * kN + 4 * g);
-        gad[0] = f.x; gad[1] = f.y; gad[2] = f.z; gad[3] = f.w;
+    if (kMode == kBwdFull && active) {  // dfinal, then the fold of the later segments
+        if (a.dfinal_state) {
+            const float4 f = *reinterpret_cast<const float4*>(a.dfinal_state + row * kN + 4 * g);
+            gad[0] = f.x; gad[1] = f.y; gad[2] = f.z; gad[3] = f.w;
+        }
+        for (int k = nprev; k > seg; --k) {
+            const float S = a.ws_bsum[row * nprev + (k - 1)];
+            const float4 gl = *reinterpret_cast<const float4*>(a.ws_gloc + (row * nprev + (k - 1)) * kN + 4 * g);
+            gad[0] = seg_decay_fma(S, 0, gad[0], gl.x);
+            gad[1] = seg_decay_fma(S, 1, gad[1], gl.y);
+            gad[2] = seg_decay_fma(S, 2, gad[2], gl.z);
+            gad[3] = seg_decay_fma(S, 3, gad[3], gl.w);
+        }
     }
     float dA_acc[4] = {0.f, 0.f, 0.f, 0.f};
     float dD_acc = 0.f, db_acc = 0.f;
@@ -274,15 +348,15 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
 
     Quad4<Tin, kVec> pd, pu, pz;
     Quad4<Tg, kVec> po;
-    if (nchunks > 0) {
-        const int64_t tl = (int64_t)(nchunks - 1) * kBChunk + 4 * g;
+    if (c_begin < c_end) {
+        const int64_t tl = (int64_t)(c_end - 1) * kBChunk + 4 * g;
         pd.load(d_row, tl, Lr);
         pu.load(u_row, tl, Lr);
         if (z_row) pz.load(z_row, tl, Lr);
         po.load(o_row, tl, Lr);
-        fetch_bc(nchunks - 1, true);
+        fetch_bc(c_end - 1, true);
     }
-    for (int c = nchunks - 1; c >= 0; --c) {
+    for (int c = c_end - 1; c >= c_begin; --c) {
         const int64_t t0 = (int64_t)c * kBChunk;
         const int64_t tl = t0 + 4 * g;
         float4 hk4 = make_float4(0.f, 0.f, 0.f, 0.f);  // rows past dim run on zeros
@@ -309,7 +383,7 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
                 dzf[i] = 0.f;
             }
         }
-        if (c > 0) {
+        if (c > c_begin) {
             pd.load(d_row, tl - kBChunk, Lr);
             pu.load(u_row, tl - kBChunk, Lr);
             if (z_row) pz.load(z_row, tl - kBChunk, Lr);
@@ -319,6 +393,22 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
         __syncthreads();  // B | C of the chunk staged
         const float* bcb = &sm.bc[0][0][0];
         float4* Hw = &sm.H[warp][0][0];
+        if (kMode == kBwdAdjLocal) {  // the adjoint alone, last token first
+            add_delta(dl);
+#pragma unroll
+            for (int t = kBChunk - 1; t >= 0; --t) {
+                const float s = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
+                const float ds = __shfl_sync(0xffffffffu, dsl[t & 3], t >> 2, 4);
+                float4 Bv, Cv;
+                Stage::get_bc(bcb, t, g, Bv, Cv);
+                gad[0] = decay_fma(s, 0, fmaf(ds, Cv.x, gad[0]), 0.f);
+                gad[1] = decay_fma(s, 1, fmaf(ds, Cv.y, gad[1]), 0.f);
+                gad[2] = decay_fma(s, 2, fmaf(ds, Cv.z, gad[2]), 0.f);
+                gad[3] = decay_fma(s, 3, fmaf(ds, Cv.w, gad[3]), 0.f);
+            }
+            __syncthreads();  // the chunk's staging is read before the next one is written
+            continue;
+        }
 
         // Recompute the chunk's states (into shared memory) and the readouts s_t - D u_t.
         float sl[4];
@@ -330,10 +420,10 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
                 const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
                 float4 Bv, Cv;
                 Stage::get_bc(bcb, t, g, Bv, Cv);
-                hh[0] = fmaf(decay(s, 0), hh[0], k * Bv.x);
-                hh[1] = fmaf(decay(s, 1), hh[1], k * Bv.y);
-                hh[2] = fmaf(decay(s, 2), hh[2], k * Bv.z);
-                hh[3] = fmaf(decay(s, 3), hh[3], k * Bv.w);
+                hh[0] = decay_fma(s, 0, hh[0], k * Bv.x);
+                hh[1] = decay_fma(s, 1, hh[1], k * Bv.y);
+                hh[2] = decay_fma(s, 2, hh[2], k * Bv.z);
+                hh[3] = decay_fma(s, 3, hh[3], k * Bv.w);
                 Hw[t * 32 + lane] = make_float4(hh[0], hh[1], hh[2], hh[3]);
                 float y = Cv.x * hh[0];
                 y = fmaf(Cv.y, hh[1], y);
@@ -352,8 +442,11 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
         }
         __syncwarp();
 
-        // Adjoint recurrence, last token of the chunk first.
+        // Adjoint recurrence, last token of the chunk first. The chunk's dA terms are summed
+        // apart and then added to the running sum: two-level summation keeps the rounding of
+        // sums over hundreds of thousands of tokens near that of the per-chunk sums.
         float dkl[4], dal[4];  // owner: dk_t and the Abar part of dDelta_t
+        float dA_chunk[4] = {0.f, 0.f, 0.f, 0.f};
         float4 ht = Hw[(kBChunk - 1) * 32 + lane];
 #pragma unroll
         for (int t = kBChunk - 1; t >= 0; --t) {
@@ -372,11 +465,13 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
                 v[4 + n] = ds * hts[n];   // dC term
                 v[n] = gad[n] * k;        // dB term
                 dk = fmaf(gad[n], Bs[n], dk);
-                const float ab = decay(s, n);
-                const float w = gad[n] * hps[n] * ab;  // dAbar * Abar
+                // Abar, and the adjoint times Abar (1 + expm1 for fp32 inputs, see decay_fma)
+                const float m = kPrecise ? expm1f(s * Av[n]) : ex2_approx(s * Av[n]);
+                const float gab = kPrecise ? fmaf(m, gad[n], gad[n]) : gad[n] * m;
+                const float w = gab * hps[n];  // dAbar * Abar
                 da = fmaf(w, Av[n], da);
-                dA_acc[n] = fmaf(w, s, dA_acc[n]);
-                gad[n] *= ab;
+                dA_chunk[n] = fmaf(w, s, dA_chunk[n]);
+                gad[n] = gab;
             }
             ht = hp;
             dk += __shfl_xor_sync(0xffffffffu, dk, 1);
@@ -399,18 +494,22 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
             const float send = x4 ? w2[0] : w2[1], keep = x4 ? w2[1] : w2[0];
             sm.P[warp][t][my_slot] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
         }
+#pragma unroll
+        for (int n = 0; n < 4; ++n) dA_acc[n] += dA_chunk[n];
         // Owner: per-token gradients of its tokens.
         {
-            float duv[4], ddv[4];
+            float duv[4], ddv[4], dD_c = 0.f, db_c = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 duv[i] = fmaf(dkl[i], dl[i] * (1.f / kScale), dsl[i] * Dd);
                 ddv[i] = fmaf(dkl[i], ul[i], dal[i]) * sgx[i];
                 if (tl + i < Lr) {
-                    dD_acc = fmaf(dsl[i], ul[i], dD_acc);
-                    db_acc += ddv[i];
+                    dD_c = fmaf(dsl[i], ul[i], dD_c);
+                    db_c += ddv[i];
                 }
             }
+            dD_acc += dD_c;
+            db_acc += db_c;
             store4<Tg, kVec>(du_row, tl, Lr, duv);
             store4<Tg, kVec>(dd_row, tl, Lr, ddv);
         }
@@ -427,13 +526,24 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
         }
     }
 
-    // ---- per-channel partials (summed over batches by the reduction kernel) ----
+    if (kMode == kBwdAdjLocal) {
+        const float S = quad_delta_sum();
+        if (active) {
+            *reinterpret_cast<float4*>(a.ws_gloc + (row * nprev + (seg - 1)) * kN + 4 * g) =
+                make_float4(gad[0], gad[1], gad[2], gad[3]);
+            if (g == 0) a.ws_bsum[row * nprev + (seg - 1)] = S;
+        }
+        return;
+    }
+
+    // ---- per-channel partials (summed over batches and segments by the reduction kernel) ----
+    const int64_t rs = row * a.nseg + seg;
     if (active) {
-        if (a.dinitial_state)
+        if (a.dinitial_state && seg == 0)
             *reinterpret_cast<float4*>(a.dinitial_state + row * kN + 4 * g) =
                 make_float4(gad[0], gad[1], gad[2], gad[3]);
         constexpr float sc = 1.f / kScale;  // the dA terms were taken with Delta * kScale
-        *reinterpret_cast<float4*>(a.ws_dA + row * kN + 4 * g) =
+        *reinterpret_cast<float4*>(a.ws_dA + rs * kN + 4 * g) =
             make_float4(dA_acc[0] * sc, dA_acc[1] * sc, dA_acc[2] * sc, dA_acc[3] * sc);
     }
     dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 1);
@@ -441,8 +551,8 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
     db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 1);
     db_acc += __shfl_xor_sync(0xffffffffu, db_acc, 2);
     if (active && g == 0) {
-        a.ws_dD[row] = dD_acc;
-        a.ws_db[row] = db_acc;
+        a.ws_dD[rs] = dD_acc;
+        a.ws_db[rs] = db_acc;
     }
 }
 
@@ -463,30 +573,42 @@ __global__ void scan_bwd_reduce_kernel(const BwdArgs a, int64_t nblk) {
             dst[(b * kN + (slot % kN)) * L + t] = s;
         } else if (i < nbc + nda) {
             const int64_t j = i - nbc;  // d*16 + n
+            const int64_t d = j / kN, n = j % kN;
             float s = 0.f;
-            for (int64_t b = 0; b < a.batch; ++b) s += a.ws_dA[b * nda + j];
+            for (int64_t b = 0; b < a.batch; ++b)
+                for (int k = 0; k < a.nseg; ++k) s += a.ws_dA[((b * a.dim + d) * a.nseg + k) * kN + n];
             a.dA[j] = s;
         } else {
             const int64_t j = i - nbc - nda;
             const int64_t dd = j % a.dim;
             const bool isD = j < a.dim;
+            const float* src = isD ? a.ws_dD : a.ws_db;
             float s = 0.f;
-            for (int64_t b = 0; b < a.batch; ++b) s += (isD ? a.ws_dD : a.ws_db)[b * a.dim + dd];
+            for (int64_t b = 0; b < a.batch; ++b)
+                for (int k = 0; k < a.nseg; ++k) s += src[(b * a.dim + dd) * a.nseg + k];
             if (isD && a.dD) a.dD[dd] = s;
             if (!isD && a.ddelta_bias) a.ddelta_bias[dd] = s;
         }
     }
 }
 
+template <typename Tin, typename Tg, bool kPrecise, bool kVec>
+static cudaError_t launch_bwd_modes(const BwdArgs& a, unsigned gx, cudaStream_t stream) {
+    if (a.nseg > 1) {  // the local passes: forward over segments 0..S-2, adjoint over 1..S-1
+        const dim3 grid(gx, (unsigned)(a.nseg - 1), (unsigned)a.batch);
+        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kBwdFwdLocal><<<grid, kBThreads, 0, stream>>>(a);
+        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kBwdAdjLocal><<<grid, kBThreads, 0, stream>>>(a);
+    }
+    const dim3 grid(gx, (unsigned)a.nseg, (unsigned)a.batch);
+    scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kBwdFull><<<grid, kBThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename Tin, typename Tg, bool kPrecise>
 static cudaError_t launch_bwd_typed(const BwdArgs& a, cudaStream_t stream) {
     const unsigned gx = (unsigned)((a.dim + kBRows - 1) / kBRows);
-    const dim3 grid(gx, (unsigned)a.batch);
-    if (a.seqlen % 4 == 0)
-        scan_bwd_kernel<Tin, Tg, kPrecise, true><<<grid, kBThreads, 0, stream>>>(a);
-    else
-        scan_bwd_kernel<Tin, Tg, kPrecise, false><<<grid, kBThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = a.seqlen % 4 == 0 ? launch_bwd_modes<Tin, Tg, kPrecise, true>(a, gx, stream)
+                                      : launch_bwd_modes<Tin, Tg, kPrecise, false>(a, gx, stream);
     if (e != cudaSuccess) return e;
     scan_bwd_reduce_kernel<<<4 * 148, 256, 0, stream>>>(a, (int64_t)gx);
     return cudaGetLastError();
@@ -502,21 +624,29 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, bool in_bf16, bool grad_bf16, cuda
                      : launch_bwd_typed<float, float, true>(a, stream);
 }
 
-size_t scan_bwd_workspace_floats(int64_t batch, int64_t dim, int64_t seqlen, int64_t* off_part,
-                                 int64_t* off_dA, int64_t* off_dD, int64_t* off_db) {
+BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int nseg) {
     const int64_t rows = batch * dim;
     const int64_t nchunks = (seqlen + kBChunk - 1) / kBChunk;
     const int64_t nblk = (dim + kBRows - 1) / kBRows;
+    const int64_t nprev = nseg - 1;
     auto up = [](int64_t x) { return (x + 63) / 64 * 64; };  // 256-byte alignment
-    const int64_t ckpt = up(rows * nchunks * kN);
-    const int64_t part = up(nblk * batch * seqlen * kBSlots);
-    const int64_t dA = up(rows * kN);
-    const int64_t dD = up(rows), db = up(rows);
-    if (off_part) *off_part = ckpt;
-    if (off_dA) *off_dA = ckpt + part;
-    if (off_dD) *off_dD = ckpt + part + dA;
-    if (off_db) *off_db = ckpt + part + dA + dD;
-    return (size_t)(ckpt + part + dA + dD + db);
+    BwdWorkspace w{};
+    int64_t o = 0;
+    w.ckpt = o; o += up(rows * nchunks * kN);
+    w.part = o; o += up(nblk * batch * seqlen * kBSlots);
+    w.dA = o; o += up(rows * nseg * kN);
+    w.dD = o; o += up(rows * nseg);
+    w.db = o; o += up(rows * nseg);
+    w.hloc = o; o += up(rows * nprev * kN);
+    w.fsum = o; o += up(rows * nprev);
+    w.gloc = o; o += up(rows * nprev * kN);
+    w.bsum = o; o += up(rows * nprev);
+    w.total = o;
+    return w;
 }
+
+int scan_bwd_chunk_tokens() { return kBChunk; }
+int scan_bwd_rows_per_cta() { return kBRows; }
+int scan_bwd_ctas_per_sm() { return kBMinCtas; }
 
 }  // namespace selscan

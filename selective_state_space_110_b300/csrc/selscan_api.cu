@@ -303,16 +303,41 @@ SELSCAN_EXPORT selscan_status ssm_conv_state_update(
 }
 
 namespace {
-size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen) {
-    return selscan::scan_bwd_workspace_floats(batch, dim, seqlen, nullptr, nullptr, nullptr,
-                                              nullptr) * sizeof(float);
+// Time segments of the backward, on the forward's rule: split only when the rows alone fill less
+// than half of the CTA slots; as many segments as fill one wave, each at least kMinSegTokens.
+struct BwdPlan {
+    int nseg;
+    int64_t seg_len;
+};
+BwdPlan make_bwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
+    const int64_t chunk = selscan::scan_bwd_chunk_tokens();
+    const int64_t rows_per_cta = selscan::scan_bwd_rows_per_cta();
+    const int64_t ctas = batch * ((dim + rows_per_cta - 1) / rows_per_cta);
+    const int64_t slots = (int64_t)sms * selscan::scan_bwd_ctas_per_sm();
+    int64_t n = 1;
+    if (2 * ctas <= slots) {
+        n = slots / ctas;
+        n = std::min<int64_t>(n, seqlen / kMinSegTokens);
+        n = std::max<int64_t>(n, 1);
+        n = std::min<int64_t>(n, 65535);
+    }
+    int64_t seg_len = (std::max<int64_t>(seqlen, 1) + n - 1) / n;
+    seg_len = (seg_len + chunk - 1) / chunk * chunk;
+    n = std::max<int64_t>(1, (seqlen + seg_len - 1) / seg_len);
+    return BwdPlan{(int)n, seg_len};
+}
+size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
+    const BwdPlan p = make_bwd_plan(batch, dim, seqlen, sms);
+    return (size_t)selscan::scan_bwd_workspace(batch, dim, seqlen, p.nseg).total * sizeof(float);
 }
 }  // namespace
 
 SELSCAN_EXPORT size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
                                                   int64_t seqlen) {
     if (!shape_ok(batch, dim, seqlen) || dstate != kStateN) return 0;
-    return bwd_workspace_bytes(batch, dim, seqlen);
+    int sms = 0;
+    if (device_sms(&sms) != SELSCAN_OK) return 0;
+    return bwd_workspace_bytes(batch, dim, seqlen, sms);
 }
 
 SELSCAN_EXPORT selscan_status ssm_scan_bwd(
@@ -351,7 +376,6 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
                           range_of(initial_state, initial_state ? st : 0),
                           range_of(dout, act * eg),
                           range_of(dfinal_state, dfinal_state ? st : 0)};
-    const size_t ws_need = bwd_workspace_bytes(batch, dim, seqlen);
     const Range out_r[] = {range_of(du, has_tokens ? act * eg : 0),
                            range_of(ddelta, has_tokens ? act * eg : 0),
                            range_of(dz, dz && has_tokens ? act * eg : 0),
@@ -360,8 +384,7 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
                            range_of(dC, has_tokens ? bc * 4 : 0),
                            range_of(dD, dD ? dvec : 0),
                            range_of(ddelta_bias, ddelta_bias ? dvec : 0),
-                           range_of(dinitial_state, dinitial_state ? st : 0),
-                           range_of(workspace, ws_need)};
+                           range_of(dinitial_state, dinitial_state ? st : 0)};
     constexpr size_t kOuts = sizeof(out_r) / sizeof(out_r[0]);
     for (size_t i = 0; i < kOuts; ++i) {
         for (const Range& r : in_r)
@@ -369,14 +392,22 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
         for (size_t j = i + 1; j < kOuts; ++j)
             if (overlaps(out_r[i], out_r[j])) return SELSCAN_ERR_INVALID_ARG;
     }
-    if (ws_need > 0 && (!workspace || workspace_bytes < ws_need)) return SELSCAN_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes == 0) return SELSCAN_ERR_WORKSPACE;  // always needed
 
+    // The time-segment plan (and so the workspace size) depends on the device's SM count.
     int sms = 0;
     selscan_status s = device_sms(&sms);
     if (s != SELSCAN_OK) return s;
+    const BwdPlan plan = make_bwd_plan(batch, dim, seqlen, sms);
+    const selscan::BwdWorkspace wl = selscan::scan_bwd_workspace(batch, dim, seqlen, plan.nseg);
+    const size_t ws_need = (size_t)wl.total * sizeof(float);
+    if (workspace_bytes < ws_need) return SELSCAN_ERR_WORKSPACE;
+    const Range ws_r = range_of(workspace, ws_need);
+    for (const Range& r : in_r)
+        if (overlaps(ws_r, r)) return SELSCAN_ERR_INVALID_ARG;
+    for (const Range& r : out_r)
+        if (overlaps(ws_r, r)) return SELSCAN_ERR_INVALID_ARG;
 
-    int64_t off_part = 0, off_dA = 0, off_dD = 0, off_db = 0;
-    selscan::scan_bwd_workspace_floats(batch, dim, seqlen, &off_part, &off_dA, &off_dD, &off_db);
     float* ws = static_cast<float*>(workspace);
     selscan::BwdArgs a{};
     a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
@@ -384,9 +415,11 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
     a.dfinal_state = dfinal_state; a.du = du; a.ddelta = ddelta; a.dz = z ? dz : nullptr;
     a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.ddelta_bias = ddelta_bias;
     a.dinitial_state = dinitial_state;
-    a.ws_ckpt = ws; a.ws_part = ws + off_part; a.ws_dA = ws + off_dA; a.ws_dD = ws + off_dD;
-    a.ws_db = ws + off_db;
+    a.ws_ckpt = ws + wl.ckpt; a.ws_part = ws + wl.part; a.ws_dA = ws + wl.dA;
+    a.ws_dD = ws + wl.dD; a.ws_db = ws + wl.db; a.ws_hloc = ws + wl.hloc;
+    a.ws_fsum = ws + wl.fsum; a.ws_gloc = ws + wl.gloc; a.ws_bsum = ws + wl.bsum;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen;
+    a.nseg = plan.nseg; a.seg_len = plan.seg_len;
     a.softplus = (delta_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
     cudaError_t e = selscan::launch_scan_bwd(a, in_dtype == SELSCAN_BF16,
                                              grad_dtype == SELSCAN_BF16,

@@ -94,18 +94,29 @@ struct BwdArgs {
     float* dinitial_state;      // NULL = not written
     float* ws_ckpt;  // (batch*dim, chunks, 16): the state before every chunk
     float* ws_part;  // (channel blocks, batch, 32, seqlen): per-CTA sums of dB | dC
-    float* ws_dA;    // (batch*dim, 16) per-row sums
-    float* ws_dD;    // (batch*dim)
-    float* ws_db;    // (batch*dim)
+    float* ws_dA;    // (batch*dim, nseg, 16) per-row, per-segment sums
+    float* ws_dD;    // (batch*dim, nseg)
+    float* ws_db;    // (batch*dim, nseg)
+    float* ws_hloc;  // (batch*dim, nseg-1, 16): local end states of segments 0..nseg-2
+    float* ws_fsum;  // (batch*dim, nseg-1): their summed Delta
+    float* ws_gloc;  // (batch*dim, nseg-1, 16): local start adjoints of segments 1..nseg-1
+    float* ws_bsum;  // (batch*dim, nseg-1): their summed Delta
     int64_t batch;
     int64_t dim;
     int64_t seqlen;
+    int64_t seg_len;  // tokens per time segment, a multiple of 16
+    int nseg;         // time segments (1 = no split)
     int softplus;
 };
 
-// Workspace of the backward in floats; the offsets of its parts (the checkpoints start at 0).
-size_t scan_bwd_workspace_floats(int64_t batch, int64_t dim, int64_t seqlen, int64_t* off_part,
-                                 int64_t* off_dA, int64_t* off_dD, int64_t* off_db);
+// Workspace of the backward, in floats from its start.
+struct BwdWorkspace {
+    int64_t ckpt, part, dA, dD, db, hloc, fsum, gloc, bsum, total;
+};
+BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int nseg);
+int scan_bwd_chunk_tokens();   // time segments are multiples of this
+int scan_bwd_rows_per_cta();
+int scan_bwd_ctas_per_sm();
 // Launches the backward kernel and the reduction of its partial sums on `stream`.
 cudaError_t launch_scan_bwd(const BwdArgs& a, bool in_bf16, bool grad_bf16, cudaStream_t stream);
 

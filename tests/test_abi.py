@@ -211,9 +211,8 @@ def call_bwd(lib, **kw):
     (dict(z=None), INVALID),                  # dz given without z
     (dict(dC=fake(14) + 64), INVALID),        # dC inside dB
     (dict(du=fake(0) + 32), INVALID),         # du inside u
-    (dict(ws=fake(13)), INVALID),             # workspace over dA
     (dict(ws=None, ws_bytes=0), WS),
-    (dict(ws_bytes=1024), WS),
+    (dict(ws_bytes=0), WS),
     (dict(dout=fake(9) + 8), ALIGN),
 ])
 def test_bwd_rejects(lib, kw, expect):
@@ -226,9 +225,8 @@ def test_bwd_valid_args_reach_the_device_check(lib):
         pytest.skip("device present: covered by the GPU tests")
     assert call_bwd(lib) == CUDA
     assert call_bwd(lib, z=None, dz=None, D=None, dD=None, h0=None, dh0=None, dfinal=None) == CUDA
-    # workspace: the state every 16 tokens plus per-32-channel partial sums of dB | dC
-    need = lib.ssm_scan_bwd_workspace_size(2, 64, 16, 128)
-    assert need >= 4 * (2 * 64 * 8 * 16 + 2 * 2 * 32 * 128)
+    # The workspace size depends on the device (time segments); without one it is 0.
+    assert lib.ssm_scan_bwd_workspace_size(2, 64, 16, 128) == 0
     assert lib.ssm_scan_bwd_workspace_size(2, 64, 8, 128) == 0
 
 

@@ -169,3 +169,37 @@ def test_bwd_mamba2p8b_layer_sampled():
     assert_close(got["dA"][idx.to(DEV)], rs["dA"], tol, "sampled dA")
     assert_close(got["dD"][idx.to(DEV)], rs["dD"], tol, "sampled dD")
     assert_close(got["ddelta_bias"][idx.to(DEV)], rs["ddelta_bias"], tol, "sampled ddelta_bias")
+
+
+def _unsplit_workspace_bytes(b, d, L):
+    """Workspace of the backward without time segments (mirrors its layout, 256-byte parts)."""
+    up = lambda x: (x + 63) // 64 * 64
+    rows, chunks, blocks = b * d, (L + 15) // 16, (d + 31) // 32
+    return 4 * (up(rows * chunks * 16) + up(blocks * b * L * 32) + up(rows * 16) + 2 * up(rows))
+
+
+SEG_SHAPES = [
+    # few rows and long sequences: the backward cuts them into time segments
+    (1, 32, 40000, "bf16", torch.float32),
+    (1, 40, 20001, "f32", torch.float32),    # ragged length (scalar loads), fp32
+    (2, 16, 16384, "bf16", torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("shape", SEG_SHAPES, ids=lambda s: f"{s[0]}x{s[1]}x{s[2]}-{s[3]}-{str(s[4])[6:]}")
+def test_bwd_time_segments(shape):
+    from selective_state_space_110_b300 import bwd_workspace_size
+    b, d, L, dt, gdt = shape
+    assert bwd_workspace_size(b, d, 16, L) > _unsplit_workspace_bytes(b, d, L), "not split"
+    x = _problem(b, d, L, dt, 500 + L, grad_dt=gdt)
+    got = _gpu(x)
+    torch.cuda.synchronize()
+    _compare(got, _oracle(x), TOL[x["u"].dtype], f"{b}x{d}x{L} segments")
+
+
+def test_bwd_rejects_a_small_workspace():
+    from selective_state_space_110_b300 import bwd_workspace_size
+    x = _problem(1, 32, 40000, "bf16", 3)
+    need = bwd_workspace_size(1, 32, 16, 40000)
+    with pytest.raises(SelscanError, match="WORKSPACE"):
+        _gpu(x, workspace=torch.empty(need - 256, dtype=torch.uint8, device=DEV))
