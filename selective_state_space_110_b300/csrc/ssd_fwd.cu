@@ -14,26 +14,28 @@
 // which is the recurrence H_t = exp(a_t) H_{t-1} + Delta_t x_t B_t^T, y_t = C_t . H_t + D x_t
 // evaluated a chunk at a time.
 //
-// One CTA per (b, h) walks the chunks in order; 256 threads, thread (row, half) serving
-// tensor-memory lane `row` (the chunk's token row, or the state row n) and one half of the
-// columns. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
-// next chunk's tiles load while this one computes; dt of the next chunk and z of this one are
-// loaded into registers ahead of use. The products run as tcgen05.mma (bf16 operands, fp32
-// accumulators in tensor memory), issued by one thread and completed through mbarriers, and are
-// ordered so that the tensor cores work while the threads do: C B^T and C S run while the
-// threads scale x and decay the state; the state update B^T (w X) runs while they build M; M X
-// runs while they split the new state.
+// One CTA per (b, h) walks the chunks in order: 288 threads, 8 worker warps and one issuing
+// warp. Worker thread (row, half) serves tensor-memory lane `row` (the chunk's token row, or the
+// state row n) and one half of the columns; lane 0 of the issuing warp starts every TMA load and
+// every MMA. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
+// next chunk's tiles load while this one computes; the next chunk's Delta sums and z are
+// computed and loaded ahead of use. The products run as tcgen05.mma (bf16 operands, fp32
+// accumulators in tensor memory); their completion reaches the workers through mbarriers
+// (tcgen05.commit), and the workers hand finished operands to the issuer through mbarriers they
+// arrive on. The order lets the tensor cores work while the workers do: C B^T and C S run while
+// the workers scale x and decay the state; the state update B^T (w X) runs while they build M;
+// M X runs while they split the new state; the next chunk's C B^T runs during the output.
 //
 // The operands the kernel derives (M, w * X and the state S) are fp32 values; each enters the
 // tensor cores as the sum of two bf16 matrices (hi = bf16(v), lo = bf16(v - hi)), which keeps
 // about 16 significand bits. For C S and B^T (w X) hi and lo sit side by side as one N = 128
 // operand, giving two accumulators that are added afterwards (the state is kept as such a
-// pair); M is written back into tensor memory over G and read from there as the A operand of
-// M X. B, C and x are bf16 inputs and enter exactly.
+// pair); M is written into tensor memory and read from there as the A operand of M X. B, C and
+// x are bf16 inputs and enter exactly.
 //
-// Tensor memory (512 columns, one CTA per SM): [0,128) G, then M (hi in [0,64), lo in
-// [64,128), bf16 pairs); [128,192) M X; [192,320) C S (hi part | lo part); [320,448) the state
-// as the pair S = Sa + Sb (row n, column p).
+// Tensor memory (512 columns, one CTA per SM): [0,128) G; [128,192) M hi and [192,256) M lo
+// (bf16 pairs); [256,384) the state as the pair S = Sa + Sb (row n, column p); [384,512)
+// C S (hi part | lo part), then Y = exp(cs_i) C S in [384,448), into which M X accumulates.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
