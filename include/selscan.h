@@ -103,6 +103,25 @@ selscan_status ssm_scan_fwd(const void* u, const void* delta, const float* A, co
                             selscan_stream_t stream);
 
 /*
+ * ssm_scan_fwd_ckpt: ssm_scan_fwd that also writes the state before every 16th token, for a
+ * backward pass (ssm_scan_bwd) that then does not recompute it. The paper has no counterpart:
+ * "A Scan on the Chip" recomputes the states in the backward pass; this trades 4 bytes per
+ * (b, d, token) of memory for that pass.
+ *   checkpoints  (batch, dim, ceil(seqlen/16), 16) fp32, device: entry [b, d, c, n] is state n
+ *                before token 16*c (entry c = 0 is the initial state).
+ * Everything else as ssm_scan_fwd. The zero-order hold is SELSCAN_ERR_UNSUPPORTED here (the
+ * backward does not cover it); checkpoints must not overlap any other argument.
+ */
+selscan_status ssm_scan_fwd_ckpt(const void* u, const void* delta, const float* A, const void* B,
+                                 const void* C, const float* D, const void* z,
+                                 const float* delta_bias, int delta_softplus, void* out,
+                                 float* final_state, int64_t batch, int64_t dim, int64_t dstate,
+                                 int64_t seqlen, selscan_dtype in_dtype, selscan_dtype out_dtype,
+                                 const float* initial_state, void* workspace,
+                                 size_t workspace_bytes, float* checkpoints,
+                                 selscan_stream_t stream);
+
+/*
  * Workspace bytes ssm_scan_fwd needs for this shape on the CURRENT device (the time split
  * depends on its SM count). 0 means no workspace is needed. Returns 0 for invalid shapes
  * (ssm_scan_fwd then reports the error).
@@ -237,9 +256,14 @@ size_t ssm_scan_fwd_host_workspace_size(int64_t batch, int64_t dim, int64_t dsta
  * are bitwise repeatable. SELSCAN_FLAG_ZOH: SELSCAN_ERR_UNSUPPORTED. Outputs must not overlap
  * inputs, one another or the workspace (SELSCAN_ERR_INVALID_ARG); every pointer 16-byte aligned.
  *
- * workspace: at least ssm_scan_bwd_workspace_size() bytes (always > 0: the state every 16
- * tokens, 4 bytes per (b, d, token), plus per-block partial sums of dB and dC of
- * 4*batch*32*seqlen bytes per 32 channels). Its contents on entry do not matter.
+ * checkpoints: NULL, or the states written by ssm_scan_fwd_ckpt on the same inputs; the backward
+ * then reads them instead of running its own forward pass.
+ *
+ * workspace: at least ssm_scan_bwd_workspace_size(..., checkpoints != NULL) bytes on the CURRENT
+ * device (always > 0: without checkpoints the state every 16 tokens, 4 bytes per (b, d, token);
+ * per-block partial sums of dB and dC, 4*batch*32*seqlen bytes per 32 channels; per-row sums;
+ * and, for long sequences with few rows, which are split into time segments as in the forward,
+ * each segment's local end state and start adjoint). Its contents on entry do not matter.
  */
 selscan_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
                             const void* C, const float* D, const void* z,
@@ -249,10 +273,13 @@ selscan_status ssm_scan_bwd(const void* u, const void* delta, const float* A, co
                             float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
                             float* dinitial_state, int64_t batch, int64_t dim, int64_t dstate,
                             int64_t seqlen, selscan_dtype in_dtype, selscan_dtype grad_dtype,
-                            void* workspace, size_t workspace_bytes, selscan_stream_t stream);
+                            const float* checkpoints, void* workspace, size_t workspace_bytes,
+                            selscan_stream_t stream);
 
-/* Workspace bytes ssm_scan_bwd needs for this shape (0 for invalid shapes). */
-size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
+/* Workspace bytes ssm_scan_bwd needs for this shape on the current device, with or without
+ * checkpoints from ssm_scan_fwd_ckpt (0 for invalid shapes or no device). */
+size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                   int checkpoints_given);
 
 /*
  * ssd_chunk_scan_fwd: the Mamba-2 layer core, state space duality (SSD). "Mamba and State Space

@@ -30,7 +30,8 @@ STATUS = {
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selscan_status_string",
            "ssm_scan_fwd_no_alloc", "selscan_device_status", "selscan_selftest_wait_timeout",
            "ssm_conv_state_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
-           "ssd_chunk_scan_fwd", "ssm_scan_fwd_host", "ssm_scan_fwd_host_workspace_size")
+           "ssd_chunk_scan_fwd", "ssm_scan_fwd_host", "ssm_scan_fwd_host_workspace_size",
+           "ssm_scan_fwd_ckpt")
 
 # Size of the fixed scratch array behind ssm_scan_fwd_no_alloc (SELSCAN_NO_ALLOC_SCRATCH_BYTES).
 NO_ALLOC_SCRATCH_BYTES = 524288
@@ -66,11 +67,14 @@ def load() -> ctypes.CDLL:
     lib.ssm_conv_state_update.argtypes = ([_VP] * 4 + [ctypes.c_int, _I64] + [_VP] * 9 +
                                           [_VP, ctypes.c_int] + [_I64] * 3 +
                                           [ctypes.c_int, ctypes.c_int, _VP])
+    lib.ssm_scan_fwd_ckpt.restype = ctypes.c_int
+    lib.ssm_scan_fwd_ckpt.argtypes = ([_VP] * 8 + [ctypes.c_int, _VP, _VP] + [_I64] * 4 +
+                                      [ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_size_t, _VP, _VP])
     lib.ssm_scan_bwd.restype = ctypes.c_int
     lib.ssm_scan_bwd.argtypes = ([_VP] * 8 + [ctypes.c_int] + [_VP] * 12 + [_I64] * 4 +
-                                 [ctypes.c_int, ctypes.c_int, _VP, ctypes.c_size_t, _VP])
+                                 [ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_size_t, _VP])
     lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
-    lib.ssm_scan_bwd_workspace_size.argtypes = [_I64] * 4
+    lib.ssm_scan_bwd_workspace_size.argtypes = [_I64] * 4 + [ctypes.c_int]
     lib.ssd_chunk_scan_fwd.restype = ctypes.c_int
     lib.ssd_chunk_scan_fwd.argtypes = ([_VP] * 8 + [ctypes.c_int] + [_VP] * 3 + [_I64] * 6 +
                                        [ctypes.c_int, ctypes.c_int, _VP])

@@ -41,7 +41,10 @@ constexpr int kBWarps = 4;
 constexpr int kBThreads = 32 * kBWarps;     // 128: 32 channels
 constexpr int kBRows = 32;                  // channels per CTA
 constexpr int kBSlots = 32;                 // dB[0..15], dC[0..15] per token
-constexpr int kBMinCtas = 5;                // CTAs per SM the kernel is built to fit
+// CTAs per SM the kernel is built to fit: 5 (96 registers) when the grid needs the slots, 4
+// (128 registers, no spills) when it fits one wave at 4 per SM.
+constexpr int kBMinCtas = 5;
+constexpr int kBMinCtasRoomy = 4;
 
 struct BwdSmem {
     float bc[2][kBChunk][32];                // B | C per token (layout: BcStage)
@@ -170,8 +173,8 @@ struct BcStage<__nv_bfloat16> {
 // (segments 0..S-2) and the adjoint local-start pass (segments 1..S-1).
 enum BwdMode : int { kBwdFull = 0, kBwdFwdLocal = 1, kBwdAdjLocal = 2 };
 
-template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode>
-__global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const BwdArgs a) {
+template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode, int kMinCtas>
+__global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const BwdArgs a) {
     __shared__ __align__(16) BwdSmem sm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = lane >> 2, g = lane & 3;
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
     };
 
     float h[4] = {0.f, 0.f, 0.f, 0.f};
-    if (kMode == kBwdFull) {  // initial state, then the fold of the earlier segments
+    if (kMode == kBwdFull && !a.ckpt_given) {  // initial state, then the earlier segments' fold
         if (a.initial_state && active) {
             const float4 s0 = *reinterpret_cast<const float4*>(a.initial_state + row * kN + 4 * g);
             h[0] = s0.x; h[1] = s0.y; h[2] = s0.z; h[3] = s0.w;
@@ -269,7 +272,8 @@ __global__ void __launch_bounds__(kBThreads, kBMinCtas) scan_bwd_kernel(const Bw
 
     // ---- checkpoint pass: the forward state before every chunk (the local-end pass: the
     // forward only) ----
-    if (kMode != kBwdAdjLocal) {
+    // (skipped when the forward pass saved the checkpoints)
+    if (kMode == kBwdFwdLocal || (kMode == kBwdFull && !a.ckpt_given)) {
         Quad4<Tin, kVec> pd, pu;
         if (c_begin < c_end) {
             const int64_t tl = (int64_t)c_begin * kBChunk + 4 * g;
@@ -592,15 +596,22 @@ __global__ void scan_bwd_reduce_kernel(const BwdArgs a, int64_t nblk) {
     }
 }
 
+template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode>
+static void launch_bwd_one(const BwdArgs& a, dim3 grid, cudaStream_t stream) {
+    if ((int64_t)grid.x * grid.y * grid.z <= (int64_t)a.sms * kBMinCtasRoomy)
+        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtasRoomy><<<grid, kBThreads, 0, stream>>>(a);
+    else
+        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtas><<<grid, kBThreads, 0, stream>>>(a);
+}
+
 template <typename Tin, typename Tg, bool kPrecise, bool kVec>
 static cudaError_t launch_bwd_modes(const BwdArgs& a, unsigned gx, cudaStream_t stream) {
     if (a.nseg > 1) {  // the local passes: forward over segments 0..S-2, adjoint over 1..S-1
         const dim3 grid(gx, (unsigned)(a.nseg - 1), (unsigned)a.batch);
-        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kBwdFwdLocal><<<grid, kBThreads, 0, stream>>>(a);
-        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kBwdAdjLocal><<<grid, kBThreads, 0, stream>>>(a);
+        if (!a.ckpt_given) launch_bwd_one<Tin, Tg, kPrecise, kVec, kBwdFwdLocal>(a, grid, stream);
+        launch_bwd_one<Tin, Tg, kPrecise, kVec, kBwdAdjLocal>(a, grid, stream);
     }
-    const dim3 grid(gx, (unsigned)a.nseg, (unsigned)a.batch);
-    scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kBwdFull><<<grid, kBThreads, 0, stream>>>(a);
+    launch_bwd_one<Tin, Tg, kPrecise, kVec, kBwdFull>(a, dim3(gx, (unsigned)a.nseg, (unsigned)a.batch), stream);
     return cudaGetLastError();
 }
 
@@ -624,7 +635,8 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, bool in_bf16, bool grad_bf16, cuda
                      : launch_bwd_typed<float, float, true>(a, stream);
 }
 
-BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int nseg) {
+BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int nseg,
+                                bool with_ckpt) {
     const int64_t rows = batch * dim;
     const int64_t nchunks = (seqlen + kBChunk - 1) / kBChunk;
     const int64_t nblk = (dim + kBRows - 1) / kBRows;
@@ -632,7 +644,7 @@ BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int 
     auto up = [](int64_t x) { return (x + 63) / 64 * 64; };  // 256-byte alignment
     BwdWorkspace w{};
     int64_t o = 0;
-    w.ckpt = o; o += up(rows * nchunks * kN);
+    w.ckpt = o; o += with_ckpt ? up(rows * nchunks * kN) : 0;
     w.part = o; o += up(nblk * batch * seqlen * kBSlots);
     w.dA = o; o += up(rows * nseg * kN);
     w.dD = o; o += up(rows * nseg);

@@ -149,7 +149,8 @@ __device__ __forceinline__ constexpr int red_swz(int j, int q) {
     return kR == 1 ? ((q >> 1) & 3) : ((2 * j + (q >> 1)) & 3);
 }
 
-template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, bool kZoh, Mode kMode>
+template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, bool kZoh, Mode kMode,
+          bool kCkpt = false>
 __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
     scan_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC) {
@@ -395,6 +396,18 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
         const float* const bcb = &sm.bc[buf][0][0];
 #pragma unroll
         for (int q = 0; q < kBlocks; ++q) {
+            // The state before every 16th token, for a backward pass that reuses it.
+            if (kCkpt && kFull && (q & 3) == 0) {
+                const int64_t tq = t0 + 4 * q;
+                if (tq < t_end) {
+                    const int64_t nck = (L + 15) / 16;
+#pragma unroll
+                    for (int j = 0; j < kR; ++j)
+                        if (act[j])
+                            *reinterpret_cast<float4*>(a.ckpt + (row[j] * nck + tq / 16) * kN + 4 * g) =
+                                make_float4(h01[j].x, h01[j].y, h23[j].x, h23[j].y);
+                }
+            }
             // exp2 arguments of tokens (4q, 4q+1) and (4q+2, 4q+3), per row and state
             float2 ea[kR][4], eb[kR][4];
             float dq[kR][4];
@@ -580,6 +593,13 @@ cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) 
         if (e != cudaSuccess) return e;
     }
     dim3 grid(gx, (unsigned)a.nseg, (unsigned)batch);
+    if constexpr (!kZoh) {
+        if (a.ckpt) {  // also keep the state before every 16th token
+            scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kFull, true>
+                <<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
+            return cudaGetLastError();
+        }
+    }
     scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kFull><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
     return cudaGetLastError();
 }

@@ -114,19 +114,21 @@ SELSCAN_EXPORT size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_
     return make_plan(batch, dim, seqlen, sms).ws_bytes;
 }
 
-SELSCAN_EXPORT selscan_status ssm_scan_fwd(
+namespace {
+selscan_status scan_fwd_impl(
     const void* u, const void* delta, const float* A, const void* B, const void* C,
     const float* D, const void* z, const float* delta_bias, int delta_softplus, void* out,
     float* final_state, int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
     selscan_dtype in_dtype, selscan_dtype out_dtype, const float* initial_state,
-    void* workspace, size_t workspace_bytes, selscan_stream_t stream) {
+    void* workspace, size_t workspace_bytes, float* ckpt, selscan_stream_t stream) {
     // ---- checks that need no device ----
     if (dstate != kStateN || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
         return SELSCAN_ERR_UNSUPPORTED;
     if (!shape_ok(batch, dim, seqlen) || (delta_softplus & ~kKnownFlags)) return SELSCAN_ERR_INVALID_ARG;
     const bool has_tokens = seqlen > 0;
     if (!A || (has_tokens && (!u || !delta || !B || !C || !out))) return SELSCAN_ERR_INVALID_ARG;
-    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, out, final_state, initial_state, workspace};
+    if (ckpt && (delta_softplus & SELSCAN_FLAG_ZOH)) return SELSCAN_ERR_UNSUPPORTED;
+    const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, out, final_state, initial_state, workspace, ckpt};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
 
@@ -134,6 +136,7 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
     const size_t act = (size_t)batch * (size_t)dim * (size_t)seqlen;
     const size_t bc = (size_t)batch * kStateN * (size_t)seqlen;
     const size_t st = (size_t)batch * (size_t)dim * kStateN * sizeof(float);
+    const size_t ck = (size_t)batch * (size_t)dim * (size_t)((seqlen + 15) / 16) * kStateN * sizeof(float);
     const Range in_r[] = {range_of(u, act * ein), range_of(delta, act * ein),
                           range_of(A, (size_t)dim * kStateN * 4), range_of(B, bc * ein),
                           range_of(C, bc * ein), range_of(D, D ? (size_t)dim * 4 : 0),
@@ -142,9 +145,10 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
                           range_of(initial_state, initial_state ? st : 0)};
     const Range out_r = range_of(out, has_tokens ? act * eout : 0);
     const Range fin_r = range_of(final_state, final_state ? st : 0);
+    const Range ck_r = range_of(ckpt, ckpt ? ck : 0);
     for (const Range& r : in_r)
-        if (overlaps(out_r, r) || overlaps(fin_r, r)) return SELSCAN_ERR_INVALID_ARG;
-    if (overlaps(out_r, fin_r)) return SELSCAN_ERR_INVALID_ARG;
+        if (overlaps(out_r, r) || overlaps(fin_r, r) || overlaps(ck_r, r)) return SELSCAN_ERR_INVALID_ARG;
+    if (overlaps(out_r, fin_r) || overlaps(ck_r, out_r) || overlaps(ck_r, fin_r)) return SELSCAN_ERR_INVALID_ARG;
 
     // ---- device and plan ----
     int sms = 0;
@@ -156,7 +160,8 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
         const Range ws_r = range_of(workspace, plan.ws_bytes);
         for (const Range& r : in_r)
             if (overlaps(ws_r, r)) return SELSCAN_ERR_INVALID_ARG;
-        if (overlaps(ws_r, out_r) || overlaps(ws_r, fin_r)) return SELSCAN_ERR_INVALID_ARG;
+        if (overlaps(ws_r, out_r) || overlaps(ws_r, fin_r) || overlaps(ws_r, ck_r))
+            return SELSCAN_ERR_INVALID_ARG;
     }
 
     selscan::ScanArgs a{};
@@ -168,6 +173,7 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
     a.dim = dim; a.seqlen = seqlen; a.seg_len = plan.seg_len; a.nseg = plan.nseg;
     a.softplus = (delta_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
     a.zoh = (delta_softplus & SELSCAN_FLAG_ZOH) ? 1 : 0;
+    a.ckpt = ckpt;
     // Two rows per lane halves the shared-memory traffic of B and C but also the warps: worth it
     // once the rows alone give about two warps per scheduler, or when time segments supply
     // the parallelism.
@@ -180,6 +186,30 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd(
                                              out_dtype == SELSCAN_BF16, vec, precise,
                                              reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
+}
+}  // namespace
+
+SELSCAN_EXPORT selscan_status ssm_scan_fwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus, void* out,
+    float* final_state, int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    selscan_dtype in_dtype, selscan_dtype out_dtype, const float* initial_state,
+    void* workspace, size_t workspace_bytes, selscan_stream_t stream) {
+    return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, final_state,
+                         batch, dim, dstate, seqlen, in_dtype, out_dtype, initial_state, workspace,
+                         workspace_bytes, nullptr, stream);
+}
+
+SELSCAN_EXPORT selscan_status ssm_scan_fwd_ckpt(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus, void* out,
+    float* final_state, int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    selscan_dtype in_dtype, selscan_dtype out_dtype, const float* initial_state,
+    void* workspace, size_t workspace_bytes, float* checkpoints, selscan_stream_t stream) {
+    if (!checkpoints && seqlen > 0) return SELSCAN_ERR_INVALID_ARG;
+    return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, final_state,
+                         batch, dim, dstate, seqlen, in_dtype, out_dtype, initial_state, workspace,
+                         workspace_bytes, seqlen > 0 ? checkpoints : nullptr, stream);
 }
 
 SELSCAN_EXPORT selscan_status ssm_state_update(float* state, const void* x, const void* dt,
@@ -326,18 +356,19 @@ BwdPlan make_bwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
     n = std::max<int64_t>(1, (seqlen + seg_len - 1) / seg_len);
     return BwdPlan{(int)n, seg_len};
 }
-size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
+size_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int sms, bool ckpt_given) {
     const BwdPlan p = make_bwd_plan(batch, dim, seqlen, sms);
-    return (size_t)selscan::scan_bwd_workspace(batch, dim, seqlen, p.nseg).total * sizeof(float);
+    return (size_t)selscan::scan_bwd_workspace(batch, dim, seqlen, p.nseg, !ckpt_given).total *
+           sizeof(float);
 }
 }  // namespace
 
 SELSCAN_EXPORT size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate,
-                                                  int64_t seqlen) {
+                                                  int64_t seqlen, int checkpoints_given) {
     if (!shape_ok(batch, dim, seqlen) || dstate != kStateN) return 0;
     int sms = 0;
     if (device_sms(&sms) != SELSCAN_OK) return 0;
-    return bwd_workspace_bytes(batch, dim, seqlen, sms);
+    return bwd_workspace_bytes(batch, dim, seqlen, sms, checkpoints_given != 0);
 }
 
 SELSCAN_EXPORT selscan_status ssm_scan_bwd(
@@ -346,8 +377,8 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
     const float* initial_state, const void* dout, const float* dfinal_state, void* du,
     void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
     float* dinitial_state, int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-    selscan_dtype in_dtype, selscan_dtype grad_dtype, void* workspace, size_t workspace_bytes,
-    selscan_stream_t stream) {
+    selscan_dtype in_dtype, selscan_dtype grad_dtype, const float* checkpoints,
+    void* workspace, size_t workspace_bytes, selscan_stream_t stream) {
     if (dstate != kStateN || !dtype_ok(in_dtype) || !dtype_ok(grad_dtype))
         return SELSCAN_ERR_UNSUPPORTED;
     if (delta_softplus & SELSCAN_FLAG_ZOH) return SELSCAN_ERR_UNSUPPORTED;
@@ -359,7 +390,7 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
     if (has_tokens && (z != nullptr) != (dz != nullptr)) return SELSCAN_ERR_INVALID_ARG;
     const void* ptrs[] = {u, delta, A, B, C, D, z, delta_bias, initial_state, dout,
                           dfinal_state, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
-                          dinitial_state, workspace};
+                          dinitial_state, workspace, checkpoints};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
 
@@ -375,7 +406,8 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
                           range_of(delta_bias, delta_bias ? dvec : 0),
                           range_of(initial_state, initial_state ? st : 0),
                           range_of(dout, act * eg),
-                          range_of(dfinal_state, dfinal_state ? st : 0)};
+                          range_of(dfinal_state, dfinal_state ? st : 0),
+                          range_of(checkpoints, checkpoints ? (size_t)batch * dim * ((seqlen + 15) / 16) * kStateN * 4 : 0)};
     const Range out_r[] = {range_of(du, has_tokens ? act * eg : 0),
                            range_of(ddelta, has_tokens ? act * eg : 0),
                            range_of(dz, dz && has_tokens ? act * eg : 0),
@@ -399,7 +431,8 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
     selscan_status s = device_sms(&sms);
     if (s != SELSCAN_OK) return s;
     const BwdPlan plan = make_bwd_plan(batch, dim, seqlen, sms);
-    const selscan::BwdWorkspace wl = selscan::scan_bwd_workspace(batch, dim, seqlen, plan.nseg);
+    const selscan::BwdWorkspace wl =
+        selscan::scan_bwd_workspace(batch, dim, seqlen, plan.nseg, checkpoints == nullptr);
     const size_t ws_need = (size_t)wl.total * sizeof(float);
     if (workspace_bytes < ws_need) return SELSCAN_ERR_WORKSPACE;
     const Range ws_r = range_of(workspace, ws_need);
@@ -415,11 +448,13 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
     a.dfinal_state = dfinal_state; a.du = du; a.ddelta = ddelta; a.dz = z ? dz : nullptr;
     a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.ddelta_bias = ddelta_bias;
     a.dinitial_state = dinitial_state;
-    a.ws_ckpt = ws + wl.ckpt; a.ws_part = ws + wl.part; a.ws_dA = ws + wl.dA;
+    a.ws_ckpt = checkpoints ? const_cast<float*>(checkpoints) : ws + wl.ckpt;
+    a.ckpt_given = checkpoints ? 1 : 0;
+    a.ws_part = ws + wl.part; a.ws_dA = ws + wl.dA;
     a.ws_dD = ws + wl.dD; a.ws_db = ws + wl.db; a.ws_hloc = ws + wl.hloc;
     a.ws_fsum = ws + wl.fsum; a.ws_gloc = ws + wl.gloc; a.ws_bsum = ws + wl.bsum;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen;
-    a.nseg = plan.nseg; a.seg_len = plan.seg_len;
+    a.nseg = plan.nseg; a.seg_len = plan.seg_len; a.sms = sms;
     a.softplus = (delta_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
     cudaError_t e = selscan::launch_scan_bwd(a, in_dtype == SELSCAN_BF16,
                                              grad_dtype == SELSCAN_BF16,

@@ -28,6 +28,7 @@ struct ScanArgs {
     int softplus;
     int rows_per_lane;  // 1 or 2 (2 only honoured on the bf16 vector path)
     int zoh;            // zero-order-hold discretisation of B instead of Euler
+    float* ckpt;        // (batch*dim, ceil(seqlen/16), 16): the state before every 16th token, or NULL
 };
 
 // Launches the local-end pass (nseg > 1) and the full pass on `stream`.
@@ -93,6 +94,7 @@ struct BwdArgs {
     float* ddelta_bias;         // NULL = not written
     float* dinitial_state;      // NULL = not written
     float* ws_ckpt;  // (batch*dim, chunks, 16): the state before every chunk
+    int ckpt_given;  // ws_ckpt holds the forward's checkpoints (no checkpoint pass)
     float* ws_part;  // (channel blocks, batch, 32, seqlen): per-CTA sums of dB | dC
     float* ws_dA;    // (batch*dim, nseg, 16) per-row, per-segment sums
     float* ws_dD;    // (batch*dim, nseg)
@@ -107,13 +109,15 @@ struct BwdArgs {
     int64_t seg_len;  // tokens per time segment, a multiple of 16
     int nseg;         // time segments (1 = no split)
     int softplus;
+    int sms;          // SMs of the device (launch shape)
 };
 
 // Workspace of the backward, in floats from its start.
 struct BwdWorkspace {
     int64_t ckpt, part, dA, dD, db, hloc, fsum, gloc, bsum, total;
 };
-BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int nseg);
+BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int nseg,
+                                bool with_ckpt);
 int scan_bwd_chunk_tokens();   // time segments are multiples of this
 int scan_bwd_rows_per_cta();
 int scan_bwd_ctas_per_sm();

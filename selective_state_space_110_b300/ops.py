@@ -214,16 +214,55 @@ def ssm_conv_state_update(conv_state, x, conv_weight, conv_bias=None, conv_silu=
     return out, conv_out
 
 
-def bwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
-    """Bytes of workspace ssm_scan_bwd needs."""
-    return int(_lib.lib().ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen))
+def bwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int,
+                       checkpoints_given: bool = False) -> int:
+    """Bytes of workspace ssm_scan_bwd needs on the current device."""
+    return int(_lib.lib().ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen,
+                                                      int(bool(checkpoints_given))))
+
+
+def ssm_scan_fwd_ckpt(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                      out=None, final_state=None, initial_state=None, workspace=None,
+                      out_dtype=None, checkpoints=None, stream=None):
+    """ssm_scan_fwd that also returns the state before every 16th token
+    (batch, dim, ceil(seqlen/16), 16) fp32, for ssm_scan_bwd(..., checkpoints=...).
+    Returns (out, final_state, checkpoints)."""
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[-1]
+    dev = u.device
+    if checkpoints is None:
+        checkpoints = torch.empty((batch, dim, (seqlen + 15) // 16, dstate), dtype=torch.float32,
+                                  device=dev)
+    _check_dev("checkpoints", checkpoints, torch.float32, (batch, dim, (seqlen + 15) // 16, dstate), dev)
+    if out is None:
+        out = torch.empty((batch, dim, seqlen), dtype=out_dtype or u.dtype, device=dev)
+    if final_state is None:
+        final_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
+    for name, t in (("u", u), ("delta", delta), ("A", A), ("B", B), ("C", C), ("D", D), ("z", z),
+                    ("delta_bias", delta_bias), ("initial_state", initial_state), ("out", out),
+                    ("final_state", final_state)):
+        _check_dev(name, t, None, None, dev)
+    with torch.cuda.device(dev):
+        need = workspace_size(batch, dim, dstate, seqlen)
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = _lib.lib().ssm_scan_fwd_ckpt(
+            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            _flags(delta_softplus, False), _ptr(out), _ptr(final_state), batch, dim, dstate, seqlen,
+            _DT[u.dtype], _DT[out.dtype], _ptr(initial_state), _ptr(workspace), ws_bytes,
+            _ptr(checkpoints), _stream_handle(stream))
+    _lib.check("ssm_scan_fwd_ckpt", st)
+    return out, final_state, checkpoints
 
 
 def ssm_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-                 initial_state=None, dout=None, dfinal_state=None, workspace=None, stream=None):
+                 initial_state=None, dout=None, dfinal_state=None, workspace=None, stream=None,
+                 checkpoints=None):
     """Gradients of sum(dout*out) + sum(dfinal_state*final_state) of ssm_scan_fwd (Euler) with
     respect to its inputs. dout (batch, dim, seqlen) sets the dtype of du, ddelta and dz; the
-    other gradients are fp32. Returns a dict with keys du, ddelta, dA, dB, dC, dD, dz,
+    other gradients are fp32. checkpoints: the states ssm_scan_fwd_ckpt saved (skips the
+    backward's own forward pass). Returns a dict with keys du, ddelta, dA, dB, dC, dD, dz,
     ddelta_bias, dinitial_state (None where the matching input is None)."""
     if u.dim() != 3:
         raise ValueError("u must be (batch, dim, seqlen)")
@@ -263,8 +302,9 @@ def ssm_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
         "dinitial_state": (None if initial_state is None
                            else torch.empty((batch, dim, dstate), dtype=f32, device=dev)),
     }
+    _check_dev("checkpoints", checkpoints, torch.float32, (batch, dim, (seqlen + 15) // 16, dstate), dev)
     with torch.cuda.device(dev):
-        need = bwd_workspace_size(batch, dim, dstate, seqlen)
+        need = bwd_workspace_size(batch, dim, dstate, seqlen, checkpoints is not None)
         if workspace is None:
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _check_dev("workspace", workspace, None, None, dev)
@@ -273,7 +313,7 @@ def ssm_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
             _flags(delta_softplus, False), _ptr(initial_state), _ptr(dout), _ptr(dfinal_state),
             _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
             _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dinitial_state"]),
-            batch, dim, dstate, seqlen, _DT[in_dt], _DT[g_dt], _ptr(workspace),
+            batch, dim, dstate, seqlen, _DT[in_dt], _DT[g_dt], _ptr(checkpoints), _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _lib.check("ssm_scan_bwd", st)
     return g

@@ -194,7 +194,8 @@ def call_bwd(lib, **kw):
                             a["delta_bias"], a["flags"], a["h0"], a["dout"], a["dfinal"], a["du"],
                             a["ddelta"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["dbias"],
                             a["dh0"], a["batch"], a["dim"], a["dstate"], a["seqlen"],
-                            a["in_dtype"], a["g_dtype"], a["ws"], a["ws_bytes"], a["stream"])
+                            a["in_dtype"], a["g_dtype"], a.get("ckpt"), a["ws"], a["ws_bytes"],
+                            a["stream"])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -214,6 +215,8 @@ def call_bwd(lib, **kw):
     (dict(ws=None, ws_bytes=0), WS),
     (dict(ws_bytes=0), WS),
     (dict(dout=fake(9) + 8), ALIGN),
+    (dict(ckpt=fake(21) + 4), ALIGN),
+    (dict(ckpt=fake(11) + 64), INVALID),      # checkpoints (an input) inside du (an output)
 ])
 def test_bwd_rejects(lib, kw, expect):
     assert call_bwd(lib, **kw) == expect
@@ -226,8 +229,8 @@ def test_bwd_valid_args_reach_the_device_check(lib):
     assert call_bwd(lib) == CUDA
     assert call_bwd(lib, z=None, dz=None, D=None, dD=None, h0=None, dh0=None, dfinal=None) == CUDA
     # The workspace size depends on the device (time segments); without one it is 0.
-    assert lib.ssm_scan_bwd_workspace_size(2, 64, 16, 128) == 0
-    assert lib.ssm_scan_bwd_workspace_size(2, 64, 8, 128) == 0
+    assert lib.ssm_scan_bwd_workspace_size(2, 64, 16, 128, 0) == 0
+    assert lib.ssm_scan_bwd_workspace_size(2, 64, 8, 128, 1) == 0
 
 
 def call_ssd(lib, **kw):
@@ -301,3 +304,14 @@ def test_host_workspace_size(lib):
     # two slots of (u, delta, z, B, C, y, final and initial state) plus A, D, bias
     assert n >= 2 * (3 * 64 * 128 * 2 + 2 * 16 * 128 * 2 + 64 * 128 * 4 + 2 * 64 * 16 * 4)
     assert lib.ssm_scan_fwd_host_workspace_size(2, 64, 8, 128, _lib.BF16, _lib.F32) == 0
+
+
+def test_fwd_ckpt_rejects(lib):
+    a = scan_args()
+    base = [a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["delta_bias"]]
+    tail = [a["out"], a["final_state"], a["batch"], a["dim"], a["dstate"], a["seqlen"],
+            a["in_dtype"], a["out_dtype"], None, None, 0]
+    assert lib.ssm_scan_fwd_ckpt(*base, 1, *tail, None, None) == INVALID          # no checkpoints
+    assert lib.ssm_scan_fwd_ckpt(*base, 3, *tail, fake(12), None) == UNSUP        # zero-order hold
+    assert lib.ssm_scan_fwd_ckpt(*base, 1, *tail, fake(12) + 8, None) == ALIGN
+    assert lib.ssm_scan_fwd_ckpt(*base, 1, *tail, fake(8) + 16, None) == INVALID  # inside out

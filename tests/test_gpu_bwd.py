@@ -130,7 +130,7 @@ def test_bwd_rejects_zoh_through_the_abi():
         x["C"].data_ptr(), None, None, None, _lib.FLAG_SOFTPLUS | _lib.FLAG_ZOH, None,
         x["dout"].data_ptr(), None, g["du"].data_ptr(), g["ddelta"].data_ptr(),
         g["dA"].data_ptr(), g["dB"].data_ptr(), g["dC"].data_ptr(), None, None, None, None,
-        1, 32, 16, 32, _lib.F32, _lib.F32, ws.data_ptr(), ws.numel(), None)
+        1, 32, 16, 32, _lib.F32, _lib.F32, None, ws.data_ptr(), ws.numel(), None)
     with pytest.raises(SelscanError, match="UNSUPPORTED"):
         _lib.check("ssm_scan_bwd", st)
 
@@ -203,3 +203,28 @@ def test_bwd_rejects_a_small_workspace():
     need = bwd_workspace_size(1, 32, 16, 40000)
     with pytest.raises(SelscanError, match="WORKSPACE"):
         _gpu(x, workspace=torch.empty(need - 256, dtype=torch.uint8, device=DEV))
+
+
+@pytest.mark.parametrize("shape", [(2, 64, 300, "f32"), (3, 40, 1000, "bf16"), (1, 32, 40000, "bf16")],
+                         ids=lambda s: f"{s[0]}x{s[1]}x{s[2]}-{s[3]}")
+def test_bwd_with_forward_checkpoints(shape):
+    """ssm_scan_fwd_ckpt saves the state before every 16th token; ssm_scan_bwd given those
+    checkpoints skips its own forward pass and must give the same gradients."""
+    from selective_state_space_110_b300 import ssm_scan_fwd_ckpt
+    b, d, L, dt = shape
+    x = _problem(b, d, L, dt, 800 + L)
+    _, fin, ck = ssm_scan_fwd_ckpt(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                                   x["delta_bias"], x["delta_softplus"],
+                                   initial_state=x["initial_state"], out_dtype=torch.float32)
+    got = _gpu(x, checkpoints=ck)
+    torch.cuda.synchronize()
+    tol = TOL[x["u"].dtype]
+    assert torch.equal(ck[:, :, 0], x["initial_state"])
+    # checkpoint c is the state after the first 16c tokens: the oracle's final state there
+    for c in (1, (L - 1) // 16):
+        pre = {k: (v[..., :16 * c].contiguous() if k in ("u", "delta", "z", "B", "C") and v is not None else v)
+               for k, v in x.items()}
+        _, rf = oracle.scan_fwd(pre["u"], pre["delta"], pre["A"], pre["B"], pre["C"], pre["D"],
+                                pre["z"], pre["delta_bias"], pre["delta_softplus"], pre["initial_state"])
+        assert_close(ck[:, :, c], rf, tol, f"checkpoint {c}")
+    _compare(got, _oracle(x), tol, f"{b}x{d}x{L} with checkpoints")
