@@ -37,6 +37,7 @@ METRIC = "selective-scan B·D·L elem/s & achieved HBM GB/s (% of peak); decode 
 SM_PER_GPU_FALLBACK = 148
 ALU_ELEM_PER_CLK_PER_SM = 2.0  # 16 SFU exp2 (32/clk/SM) and 64 FP32 lane-ops (128/clk/SM) per element
 BWD_ELEM_PER_CLK_PER_SM = 32.0 / 48.0  # backward: 48 SFU exp2 per element at 32/clk/SM
+BWD_CKPT_ELEM_PER_CLK_PER_SM = 32.0 / 32.0  # backward given the forward's checkpoints: 32 exp2
 L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one scan_kernel launch, from the ncu capture
 # summarised in profiles/scan_fwd_c2_mamba2p8b.md (same kernel code): 252.8 MB + 50.1 MB.
@@ -211,18 +212,31 @@ def time_scan(cfg, steps, warmup, x, flush, stream, soak_s=1.0):
     return times, launches_per_step
 
 
-def time_bwd(cfg, steps, warmup, x, flush, stream):
+def time_bwd(cfg, steps, warmup, x, flush, stream, checkpoints=False):
     """ssm_scan_bwd on the same workload (gradients of every input for a random bf16 dout),
-    L2 flushed before every step. Returns per-step times (ms) and launches per step."""
-    from selective_state_space_110_b300 import bwd_workspace_size, ssm_scan_bwd
+    L2 flushed before every step. Returns per-step times (ms) and launches per step.
+    checkpoints=True times the pair a training step runs when the forward keeps its states:
+    ssm_scan_fwd_ckpt, then ssm_scan_bwd given those checkpoints; it returns the times of
+    the pair and of the backward alone."""
+    from selective_state_space_110_b300 import bwd_workspace_size, ssm_scan_bwd, ssm_scan_fwd_ckpt
     gen = torch.Generator("cuda").manual_seed(cfg.seed + 7)
     dout = torch.randn(cfg.batch, cfg.dim, cfg.seqlen, generator=gen, device="cuda").to(torch.bfloat16)
-    ws = torch.empty(bwd_workspace_size(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen),
+    ws = torch.empty(bwd_workspace_size(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen, checkpoints),
                      dtype=torch.uint8, device="cuda")
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+            x["delta_softplus"])
+    if checkpoints:
+        out = torch.empty(cfg.batch, cfg.dim, cfg.seqlen, dtype=torch.bfloat16, device="cuda")
+        ck = torch.empty(cfg.batch, cfg.dim, (cfg.seqlen + 15) // 16, cfg.dstate, device="cuda")
+        mid = [(torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
 
-    def call():
-        ssm_scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
-                     x["delta_softplus"], dout=dout, workspace=ws, stream=stream)
+    def call(s=None):
+        if checkpoints:
+            ssm_scan_fwd_ckpt(*args, out=out, checkpoints=ck, stream=stream)
+            if s is not None:
+                mid[s].record(stream)
+        ssm_scan_bwd(*args, dout=dout, workspace=ws, stream=stream,
+                     checkpoints=ck if checkpoints else None)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -234,9 +248,11 @@ def time_bwd(cfg, steps, warmup, x, flush, stream):
         for s in range(steps):
             flush.fill_(1)
             ev[s][0].record(stream)
-            call()
+            call(s)
             ev[s][1].record(stream)
     torch.cuda.synchronize()
+    if checkpoints:
+        return [a.elapsed_time(b) for a, b in ev], [m.elapsed_time(b) for m, (_, b) in zip(mid, ev)], 3
     return [a.elapsed_time(b) for a, b in ev], 2
 
 
@@ -466,6 +482,10 @@ def run_ours(args):
     ssd_ms = max_over_ranks(statistics.median(ssd_times), world)
     bwd_times, bwd_launches = time_bwd(cfg, max(3, min(args.steps, 10)), 3, x, flush, stream)
     bwd_ms = max_over_ranks(statistics.median(bwd_times), world)
+    pair_times, bwdc_times, pair_launches = time_bwd(cfg, max(3, min(args.steps, 10)), 3, x, flush,
+                                                     stream, checkpoints=True)
+    pair_ms = max_over_ranks(statistics.median(pair_times), world)
+    bwdc_ms = max_over_ranks(statistics.median(bwdc_times), world)
     e2e_ms, h2d, d2h = time_scan_e2e(cfg, max(2, min(args.steps, 10)), 2, x, stream)
     e2e_ms = max_over_ranks(e2e_ms, world)
     dec, dec_conv = {}, {}
@@ -529,7 +549,19 @@ def run_ours(args):
                                        (BWD_ELEM_PER_CLK_PER_SM * sms * sm_mhz * 1e6), 4),
                      "alu_note": f"ceiling {BWD_ELEM_PER_CLK_PER_SM:.3f} elem/clk/SM: 48 SFU exp2 "
                                  "per element (3 passes x 16 states) at 32 per clock per SM",
-                     "launches_per_step": bwd_launches},
+                     "launches_per_step": bwd_launches,
+                     "with_forward_checkpoints": {
+                         "what": "ssm_scan_fwd_ckpt (the forward keeping the state before every "
+                                 "16th token) then ssm_scan_bwd given them: no recomputing pass",
+                         "fwd_ckpt_ms": round(pair_ms - bwdc_ms, 4),
+                         "bwd_ms": round(bwdc_ms, 4),
+                         "fwd_plus_bwd_ms": round(pair_ms, 4),
+                         "plain_fwd_plus_bwd_ms": round(kern_ms + bwd_ms, 4),
+                         "bwd_alu_frac": round(elems / (bwdc_ms * 1e-3) /
+                                               (BWD_CKPT_ELEM_PER_CLK_PER_SM * sms * sm_mhz * 1e6), 4),
+                         "alu_note": f"ceiling {BWD_CKPT_ELEM_PER_CLK_PER_SM:.3f} elem/clk/SM: 32 "
+                                     "SFU exp2 per element (2 passes x 16 states)",
+                         "launches_per_step": pair_launches}},
         "ssd": ssd_summary(ssd_cfg, ssd_ms, ssd_launches, world, kern_ms, cfg),
         "decode": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim, **dec},
         "decode_conv": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim,

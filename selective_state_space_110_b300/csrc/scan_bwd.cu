@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
 
     const float4 A4 = *reinterpret_cast<const float4*>(a.A + d * kN + 4 * g);
     const float Av[4] = {A4.x, A4.y, A4.z, A4.w};
+    const float2 A01 = make_float2(A4.x, A4.y), A23 = make_float2(A4.z, A4.w);
     const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
     const float Dd = a.D ? a.D[d] : 0.f;
     // Per-token steps are kept as Delta * kScale: the SFU path takes exp(Delta A) as
@@ -227,6 +228,17 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
     auto decay_fma = [&](float s, int n, float v, float add) -> float {
         if (kPrecise) return fmaf(expm1f(s * Av[n]), v, v) + add;
         return fmaf(ex2_approx(s * Av[n]), v, add);
+    };
+    // The SFU path of four states at once as two packed pairs (the same roundings as decay_fma):
+    // v <- 2^(s A) v + k B.
+    auto decay_step2 = [&](float s, float k, const float4& Bv, float (&v)[4]) {
+        const float2 s2 = f2(s), k2 = f2(k);
+        const float2 x01 = __fmul2_rn(s2, A01), x23 = __fmul2_rn(s2, A23);
+        const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+        const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+        const float2 h01 = __ffma2_rn(e01, make_float2(v[0], v[1]), __fmul2_rn(k2, make_float2(Bv.x, Bv.y)));
+        const float2 h23 = __ffma2_rn(e23, make_float2(v[2], v[3]), __fmul2_rn(k2, make_float2(Bv.z, Bv.w)));
+        v[0] = h01.x; v[1] = h01.y; v[2] = h23.x; v[3] = h23.y;
     };
     auto delta_of = [&](float x) -> float {
         if (!a.softplus) return x;
@@ -306,10 +318,14 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
                 const float s = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
                 const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
                 const float4 Bv = Stage::get_b(bcb, t, g);
-                h[0] = decay_fma(s, 0, h[0], k * Bv.x);
-                h[1] = decay_fma(s, 1, h[1], k * Bv.y);
-                h[2] = decay_fma(s, 2, h[2], k * Bv.z);
-                h[3] = decay_fma(s, 3, h[3], k * Bv.w);
+                if constexpr (kPrecise) {
+                    h[0] = decay_fma(s, 0, h[0], k * Bv.x);
+                    h[1] = decay_fma(s, 1, h[1], k * Bv.y);
+                    h[2] = decay_fma(s, 2, h[2], k * Bv.z);
+                    h[3] = decay_fma(s, 3, h[3], k * Bv.w);
+                } else {
+                    decay_step2(s, k, Bv, h);
+                }
             }
         }
     }
@@ -424,15 +440,23 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
                 const float k = __shfl_sync(0xffffffffu, kl[t & 3], t >> 2, 4);
                 float4 Bv, Cv;
                 Stage::get_bc(bcb, t, g, Bv, Cv);
-                hh[0] = decay_fma(s, 0, hh[0], k * Bv.x);
-                hh[1] = decay_fma(s, 1, hh[1], k * Bv.y);
-                hh[2] = decay_fma(s, 2, hh[2], k * Bv.z);
-                hh[3] = decay_fma(s, 3, hh[3], k * Bv.w);
+                float y;
+                if constexpr (kPrecise) {
+                    hh[0] = decay_fma(s, 0, hh[0], k * Bv.x);
+                    hh[1] = decay_fma(s, 1, hh[1], k * Bv.y);
+                    hh[2] = decay_fma(s, 2, hh[2], k * Bv.z);
+                    hh[3] = decay_fma(s, 3, hh[3], k * Bv.w);
+                    y = Cv.x * hh[0];
+                    y = fmaf(Cv.y, hh[1], y);
+                    y = fmaf(Cv.z, hh[2], y);
+                    y = fmaf(Cv.w, hh[3], y);
+                } else {
+                    decay_step2(s, k, Bv, hh);
+                    float2 y2 = __fmul2_rn(make_float2(Cv.x, Cv.y), make_float2(hh[0], hh[1]));
+                    y2 = __ffma2_rn(make_float2(Cv.z, Cv.w), make_float2(hh[2], hh[3]), y2);
+                    y = y2.x + y2.y;
+                }
                 Hw[t * 32 + lane] = make_float4(hh[0], hh[1], hh[2], hh[3]);
-                float y = Cv.x * hh[0];
-                y = fmaf(Cv.y, hh[1], y);
-                y = fmaf(Cv.z, hh[2], y);
-                y = fmaf(Cv.w, hh[3], y);
                 y += __shfl_xor_sync(0xffffffffu, y, 1);
                 y += __shfl_xor_sync(0xffffffffu, y, 2);
                 if (g == (t >> 2)) sl[t & 3] = y;
@@ -463,19 +487,45 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
             const float Bs[4] = {Bv.x, Bv.y, Bv.z, Bv.w}, Cs[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
             const float hts[4] = {ht.x, ht.y, ht.z, ht.w}, hps[4] = {hp.x, hp.y, hp.z, hp.w};
             float dk = 0.f, da = 0.f, v[8];
+            if constexpr (kPrecise) {
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                gad[n] = fmaf(ds, Cs[n], gad[n]);
-                v[4 + n] = ds * hts[n];   // dC term
-                v[n] = gad[n] * k;        // dB term
-                dk = fmaf(gad[n], Bs[n], dk);
-                // Abar, and the adjoint times Abar (1 + expm1 for fp32 inputs, see decay_fma)
-                const float m = kPrecise ? expm1f(s * Av[n]) : ex2_approx(s * Av[n]);
-                const float gab = kPrecise ? fmaf(m, gad[n], gad[n]) : gad[n] * m;
-                const float w = gab * hps[n];  // dAbar * Abar
-                da = fmaf(w, Av[n], da);
-                dA_chunk[n] = fmaf(w, s, dA_chunk[n]);
-                gad[n] = gab;
+                for (int n = 0; n < 4; ++n) {
+                    gad[n] = fmaf(ds, Cs[n], gad[n]);
+                    v[4 + n] = ds * hts[n];   // dC term
+                    v[n] = gad[n] * k;        // dB term
+                    dk = fmaf(gad[n], Bs[n], dk);
+                    // Abar as 1 + expm1 (see decay_fma), and the adjoint times Abar
+                    const float m = expm1f(s * Av[n]);
+                    const float gab = fmaf(m, gad[n], gad[n]);
+                    const float w = gab * hps[n];  // dAbar * Abar
+                    da = fmaf(w, Av[n], da);
+                    dA_chunk[n] = fmaf(w, s, dA_chunk[n]);
+                    gad[n] = gab;
+                }
+            } else {  // the same steps on packed pairs of states (0, 1) and (2, 3)
+                const float2 s2 = f2(s), k2 = f2(k), ds2 = f2(ds);
+                float2 g01 = __ffma2_rn(ds2, make_float2(Cs[0], Cs[1]), make_float2(gad[0], gad[1]));
+                float2 g23 = __ffma2_rn(ds2, make_float2(Cs[2], Cs[3]), make_float2(gad[2], gad[3]));
+                const float2 vc01 = __fmul2_rn(ds2, make_float2(hts[0], hts[1]));
+                const float2 vc23 = __fmul2_rn(ds2, make_float2(hts[2], hts[3]));
+                const float2 vb01 = __fmul2_rn(g01, k2), vb23 = __fmul2_rn(g23, k2);
+                float2 dk2 = __fmul2_rn(g01, make_float2(Bs[0], Bs[1]));
+                dk2 = __ffma2_rn(g23, make_float2(Bs[2], Bs[3]), dk2);
+                const float2 x01 = __fmul2_rn(s2, A01), x23 = __fmul2_rn(s2, A23);
+                g01 = __fmul2_rn(g01, make_float2(ex2_approx(x01.x), ex2_approx(x01.y)));
+                g23 = __fmul2_rn(g23, make_float2(ex2_approx(x23.x), ex2_approx(x23.y)));
+                const float2 w01 = __fmul2_rn(g01, make_float2(hps[0], hps[1]));  // dAbar * Abar
+                const float2 w23 = __fmul2_rn(g23, make_float2(hps[2], hps[3]));
+                float2 da2 = __fmul2_rn(w01, A01);
+                da2 = __ffma2_rn(w23, A23, da2);
+                const float2 c01 = __ffma2_rn(w01, s2, make_float2(dA_chunk[0], dA_chunk[1]));
+                const float2 c23 = __ffma2_rn(w23, s2, make_float2(dA_chunk[2], dA_chunk[3]));
+                dA_chunk[0] = c01.x; dA_chunk[1] = c01.y; dA_chunk[2] = c23.x; dA_chunk[3] = c23.y;
+                gad[0] = g01.x; gad[1] = g01.y; gad[2] = g23.x; gad[3] = g23.y;
+                v[0] = vb01.x; v[1] = vb01.y; v[2] = vb23.x; v[3] = vb23.y;
+                v[4] = vc01.x; v[5] = vc01.y; v[6] = vc23.x; v[7] = vc23.y;
+                dk = dk2.x + dk2.y;
+                da = da2.x + da2.y;
             }
             ht = hp;
             dk += __shfl_xor_sync(0xffffffffu, dk, 1);
