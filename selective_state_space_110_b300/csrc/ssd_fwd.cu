@@ -18,24 +18,30 @@
 // warp. Worker thread (row, half) serves tensor-memory lane `row` (the chunk's token row, or the
 // state row n) and one half of the columns; lane 0 of the issuing warp starts every TMA load and
 // every MMA. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
-// next chunk's tiles load while this one computes; the next chunk's Delta sums and z are
-// computed and loaded ahead of use. The products run as tcgen05.mma (bf16 operands, fp32
-// accumulators in tensor memory); their completion reaches the workers through mbarriers
-// (tcgen05.commit), and the workers hand finished operands to the issuer through mbarriers they
-// arrive on. The order lets the tensor cores work while the workers do: C B^T and C S run while
-// the workers scale x and decay the state; the state update B^T (w X) runs while they build M;
-// M X runs while they split the new state; the next chunk's C B^T runs during the output.
+// next chunk's tiles load while this one computes; the next chunk's Delta sums are computed
+// ahead of use. The products run as tcgen05.mma (bf16 operands, fp32 accumulators in tensor
+// memory); their completion reaches the workers through mbarriers (tcgen05.commit), and the
+// workers hand finished operands to the issuer through mbarriers they arrive on.
+//
+// The workers are the busy side, so the tensor cores get their operands early and the workers
+// never wait on a product in steady state. Per chunk c the workers (1) scale x by w and decay
+// the state, (2) write the output of chunk c-1, (3) build M of chunk c, (4) split the updated
+// state for the next C S and compute the next chunk's sums. Meanwhile C B^T of chunk c (into
+// the G buffer of c's parity, free since the output of c-2) and C S run before (1) ends, the
+// state update during (2) and M X during (4) and the next chunk's (1). Chunk c's output is
+// y = exp(cs_i) (C S) + M X + D x: C S and M X have accumulators of their own, so neither
+// product waits for the other chunk's output to be read.
 //
 // The operands the kernel derives (M, w * X and the state S) are fp32 values; each enters the
 // tensor cores as the sum of two bf16 matrices (hi = bf16(v), lo = bf16(v - hi)), which keeps
-// about 16 significand bits. For C S and B^T (w X) hi and lo sit side by side as one N = 128
-// operand, giving two accumulators that are added afterwards (the state is kept as such a
-// pair); M is written into tensor memory and read from there as the A operand of M X. B, C and
-// x are bf16 inputs and enter exactly.
+// about 16 significand bits: the hi and lo products accumulate into the same fp32 accumulator.
+// M is written over the columns of G it comes from and read from there as the A operand of
+// M X. B, C and x are bf16 inputs and enter exactly.
 //
-// Tensor memory (512 columns, one CTA per SM): [0,128) G; [128,192) M hi and [192,256) M lo
-// (bf16 pairs); [256,384) the state as the pair S = Sa + Sb (row n, column p); [384,512)
-// C S (hi part | lo part), then Y = exp(cs_i) C S in [384,448), into which M X accumulates.
+// Tensor memory (512 columns, one CTA per SM): [0,128) and [128,256) G of even and odd chunks,
+// then M in place (columns [16k, 16k+8) M hi and [16k+8, 16k+16) M lo of j = 16k..16k+15, bf16
+// pairs); [256,320) the state S (row n, column p); [320,384) and [384,448) C S of even and odd
+// chunks; [448,512) M X.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -54,7 +60,7 @@ constexpr int kWorkers = 256;        // threads that move data (8 warps)
 constexpr int kSsdThreads = kWorkers + 32;  // plus one warp that issues TMA loads and MMAs
 constexpr int kTile = 16384;         // one 128-row x 128-byte swizzled tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0, kColMhi = 128, kColMlo = 192, kColS = 256, kColYo = 384;
+constexpr uint32_t kColG0 = 0, kColG1 = 128, kColS = 256, kColCS0 = 320, kColCS1 = 384, kColMX = 448;
 
 // Shared-memory tiles, kTile bytes each from a 1024-byte aligned base. Input buffer s holds
 // tiles 5s .. 5s+4: C (rows i, states 0..63 | 64..127; K-major), B (rows j, states 0..63 |
@@ -97,6 +103,28 @@ __device__ __forceinline__ void unpack8(const uint4& r, float* v) {
 }
 
 template <typename Tout>
+__device__ __forceinline__ void store16(Tout* dst, const float (&v)[16]);
+template <>
+__device__ __forceinline__ void store16<float>(float* dst, const float (&v)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+template <>
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const float (&v)[16]) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <typename Tout>
 __device__ __forceinline__ void store32(Tout* dst, const float (&v)[32]);
 template <>
 __device__ __forceinline__ void store32<float>(float* dst, const float (&v)[32]) {
@@ -132,10 +160,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
     extern __shared__ uint8_t dyn_smem[];
-    // Completion of the TMA loads (per input buffer) and of the MMA groups (tcgen05.commit);
-    // hand-offs from the 256 worker threads to the issuing thread.
-    __shared__ unsigned long long bar_tma[2], bar_g1, bar_g2, bar_g4;
-    __shared__ unsigned long long bar_x, bar_m, bar_s, bar_y;
+    // Completion of the TMA loads (per input buffer) and of the MMA groups (tcgen05.commit: G
+    // per buffer, the state update, M X); hand-offs from the 256 worker threads to the issuer
+    // (x ready, M ready, state split ready, output of a chunk read, per buffer).
+    __shared__ unsigned long long bar_tma[2], bar_gg[2], bar_g4, bar_g2;
+    __shared__ unsigned long long bar_x, bar_m, bar_s, bar_y[2];
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(16) float s_cs[kQ];  // running sum of Delta*A*log2(e), inclusive
     __shared__ __align__(16) float s_dl[kQ];  // Delta
@@ -156,13 +185,15 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     if (tid == 0) {
         mbar_init(&bar_tma[0], 1);
         mbar_init(&bar_tma[1], 1);
-        mbar_init(&bar_g1, 1);
-        mbar_init(&bar_g2, 1);
+        mbar_init(&bar_gg[0], 1);
+        mbar_init(&bar_gg[1], 1);
         mbar_init(&bar_g4, 1);
+        mbar_init(&bar_g2, 1);
         mbar_init(&bar_x, kWorkers);
         mbar_init(&bar_m, kWorkers);
         mbar_init(&bar_s, kWorkers);
-        mbar_init(&bar_y, kWorkers);
+        mbar_init(&bar_y[0], kWorkers);
+        mbar_init(&bar_y[1], kWorkers);
         fence_mbar_init();
         s_ok = 1;
     }
@@ -173,7 +204,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;  // tensor-memory lane a worker thread reads and writes
     const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
-    // The state Sa + Sb (row n = row, headdim columns 32*half..+31) -> hi / lo tiles.
+    // The state (row n = row, headdim columns 32*half..+31) -> hi / lo tiles.
     auto put_state_split = [&](const float (&v)[32]) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -183,16 +214,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             *reinterpret_cast<uint4*>(tile(kTSL) + sw128(row, 4 * half + q)) = lo;
         }
     };
-    if (init_state && warp < kWorkers / 32) {  // initial state (p, n) -> Sa[n][p], Sb = 0, split
-        float v[32], zero[32];
+    if (init_state && warp < kWorkers / 32) {  // initial state (p, n) -> S[n][p], split
+        float v[32];
         const float* src = a.initial_state + ((int64_t)b * H + h) * kHeadDim * kSsdState + row;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            v[i] = src[(int64_t)(32 * half + i) * kSsdState];
-            zero[i] = 0.f;
-        }
+        for (int i = 0; i < 32; ++i) v[i] = src[(int64_t)(32 * half + i) * kSsdState];
         tmem_st32(tmem + tlane + kColS + 32 * half, v);
-        tmem_st32(tmem + tlane + kColS + 64 + 32 * half, zero);
         put_state_split(v);
     }
     fence_proxy_async_smem();
@@ -216,61 +243,72 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 tma_load_4d(tile(base + kInB + 1), &tmB, bar, 64, g, c * kQ, b);
                 tma_load_4d(tile(base + kInX), &tmX, bar, 0, h, c * kQ, b);
             };
+            // Waits for the output of chunk cc to be read (per-buffer barrier, one phase per
+            // two chunks).
+            auto wait_y = [&](int cc) { return mbar_wait_bounded(&bar_y[cc & 1], (uint32_t)((cc >> 1) & 1)); };
             issue_tma(0);
             if (nchunks > 1) issue_tma(1);
-            const uint32_t i_g1 = umma_idesc_bf16(128, 128, false, false);
-            const uint32_t i_g3 = umma_idesc_bf16(128, 128, false, true);
-            const uint32_t i_g4 = umma_idesc_bf16(128, 128, true, true);
-            const uint32_t i_g2 = umma_idesc_bf16(128, 64, false, true);
+            const uint32_t i_g1 = umma_idesc_bf16(128, 128, false, false);  // C B^T
+            const uint32_t i_cs = umma_idesc_bf16(128, 64, false, true);    // C S, M X
+            const uint32_t i_s = umma_idesc_bf16(128, 64, true, true);      // B^T (w X)
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int in = kInTiles * (c & 1);
-                const uint32_t par = (uint32_t)(c & 1), prev = par ^ 1u;
+                const uint32_t par = (uint32_t)(c & 1);
+                const uint32_t gcol = (c & 1) ? kColG1 : kColG0;
                 const bool had_state = c > 0 || init_state;
                 ok = mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
-                if (ok && c > 0) ok = mbar_wait_bounded(&bar_m, prev);  // G of chunk c-1 consumed
+                // G buffer c & 1 (M of chunk c-2) and C S buffer c & 1 are free once the
+                // output of chunk c-2 has been read.
+                if (ok && c >= 2) ok = wait_y(c - 2);
                 if (!ok) break;
                 tc_fence_after_sync();
                 // G = C B^T
 #pragma unroll 1
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (uint32_t)(k & 3) * 32;
-                    umma_bf16(tmem + kColG, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
+                    umma_bf16(tmem + gcol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
                               umma_desc_sw128(tile_addr(in + kInB + (k >> 2)) + off, 16, 1024), i_g1, k > 0);
                 }
+                umma_commit(&bar_gg[c & 1]);
+                // C S = C S_hi + C S_lo, the state as it was before this chunk
                 if (had_state) {
-                    if (c > 0) {  // the split state of chunk c-1 is ready and its output is read
-                        ok = mbar_wait_bounded(&bar_s, prev) && mbar_wait_bounded(&bar_y, prev);
+                    if (c > 0) {
+                        ok = mbar_wait_bounded(&bar_s, par ^ 1u);
                         if (!ok) break;
                         tc_fence_after_sync();
                     }
-                    // C [S hi | S lo] (N = 128)
+                    const uint32_t ccol = (c & 1) ? kColCS1 : kColCS0;
 #pragma unroll 1
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (uint32_t)(k & 3) * 32;
-                        umma_bf16(tmem + kColYo, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
-                                  umma_desc_sw128(tile_addr(kTSH) + (uint32_t)k * 2048, kTile, 1024), i_g3, k > 0);
-                    }
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t off = (uint32_t)(k & 3) * 32;
+                            umma_bf16(tmem + ccol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
+                                      umma_desc_sw128(tile_addr(part ? kTSL : kTSH) + (uint32_t)k * 2048, kTile, 1024),
+                                      i_cs, (part || k) ? 1u : 0u);
+                        }
                 }
-                umma_commit(&bar_g1);
-                // The next chunk's tiles go into the buffer chunk c-1 used, once everything that
-                // read it is done (its products, waited through G2, and its output).
-                if (c > 0 && c + 1 < nchunks) {
-                    ok = mbar_wait_bounded(&bar_g2, prev) && mbar_wait_bounded(&bar_y, prev);
-                    if (!ok) break;
-                    issue_tma(c + 1);
-                }
-                // [Sa | Sb] (+)= B^T [wX hi | wX lo]
+                // S (+)= B^T (wX)_hi + B^T (wX)_lo, after the workers decayed S and wrote w X
                 ok = mbar_wait_bounded(&bar_x, par);
                 if (!ok) break;
                 tc_fence_after_sync();
 #pragma unroll 1
-                for (int k = 0; k < 8; ++k)
-                    umma_bf16(tmem + kColS, umma_desc_sw128(tile_addr(in + kInB) + (uint32_t)k * 2048, kTile, 1024),
-                              umma_desc_sw128(tile_addr(kTXH) + (uint32_t)k * 2048, kTile, 1024), i_g4,
-                              (had_state || k > 0) ? 1u : 0u);
+                for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+                    for (int k = 0; k < 8; ++k)
+                        umma_bf16(tmem + kColS, umma_desc_sw128(tile_addr(in + kInB) + (uint32_t)k * 2048, kTile, 1024),
+                                  umma_desc_sw128(tile_addr(part ? kTXL : kTXH) + (uint32_t)k * 2048, kTile, 1024), i_s,
+                                  (had_state || part || k) ? 1u : 0u);
                 umma_commit(&bar_g4);
-                // Y (+)= (M hi + M lo) X, M read from tensor memory
+                // Once the previous chunk's output is read: its input buffer takes chunk c + 1,
+                // and the M X accumulator is free.
+                if (c > 0) {
+                    ok = wait_y(c - 1);
+                    if (!ok) break;
+                    if (c + 1 < nchunks) issue_tma(c + 1);
+                }
+                // M X = M_hi X + M_lo X, M read from tensor memory (in place of G)
                 ok = mbar_wait_bounded(&bar_m, par);
                 if (!ok) break;
                 tc_fence_after_sync();
@@ -278,9 +316,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 for (int part = 0; part < 2; ++part)
 #pragma unroll 1
                     for (int k = 0; k < 8; ++k)
-                        umma_bf16_ts(tmem + kColYo, tmem + (part ? kColMlo : kColMhi) + 8 * k,
-                                     umma_desc_sw128(tile_addr(in + kInX) + (uint32_t)k * 2048, kTile, 1024), i_g2,
-                                     (had_state || part || k) ? 1u : 0u);
+                        umma_bf16_ts(tmem + kColMX, tmem + gcol + 16 * k + (part ? 8 : 0),
+                                     umma_desc_sw128(tile_addr(in + kInX) + (uint32_t)k * 2048, kTile, 1024), i_cs,
+                                     (part || k) ? 1u : 0u);
                 umma_commit(&bar_g2);
             }
             if (!ok) s_ok = 0;
@@ -327,17 +365,63 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             }
         };
         if (nchunks > 0) chunk_sums(0);
-        // z of this thread's outputs of the current chunk (row i = row, headdim 32*half..+31).
+        // z of this thread's outputs of chunk cc (row i = row, headdim 32*half..+31), loaded
+        // ahead of the output step.
         uint4 z0 = make_uint4(0u, 0u, 0u, 0u), z1 = z0, z2 = z0, z3 = z0;
-        if (zp && row < L) {
-            const uint4* zq = reinterpret_cast<const uint4*>(zp + ((int64_t)b * L + row) * H * kHeadDim +
-                                                             (int64_t)h * kHeadDim + 32 * half);
-            z0 = zq[0]; z1 = zq[1]; z2 = zq[2]; z3 = zq[3];
-        }
+        auto load_z = [&](int cc) {
+            const int64_t t_row = (int64_t)cc * kQ + row;
+            if (zp && t_row < L) {
+                const uint4* zq = reinterpret_cast<const uint4*>(
+                    zp + ((int64_t)b * L + t_row) * H * kHeadDim + (int64_t)h * kHeadDim + 32 * half);
+                z0 = zq[0]; z1 = zq[1]; z2 = zq[2]; z3 = zq[3];
+            }
+        };
+        // y of chunk cc = exp(cs_i) C S + M X + D x, times silu(z); e = exp(cs_i) of its row.
+        auto output = [&](int cc, float e, bool with_state) {
+            const int64_t t_row = (int64_t)cc * kQ + row;
+            const int64_t yoff = ((int64_t)b * L + t_row) * H * kHeadDim + (int64_t)h * kHeadDim + 32 * half;
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g2, (uint32_t)(cc & 1)));
+            tc_fence_after_sync();
+            if (ok) {
+                const int in = kInTiles * (cc & 1);
+                const uint32_t ccol = (cc & 1) ? kColCS1 : kColCS0;
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {  // 16 columns at a time
+                    uint32_t mx[16], cs[16];
+                    tmem_ld16_async(tmem + tlane + kColMX + 32 * half + 16 * hq, mx);
+                    if (with_state) tmem_ld16_async(tmem + tlane + ccol + 32 * half + 16 * hq, cs);
+                    tmem_wait_ld();
+                    if (t_row < L) {
+                        float yd[16];
+#pragma unroll
+                        for (int qq = 0; qq < 2; ++qq) {
+                            const int q = 2 * hq + qq;
+                            float xv[8], zv[8];
+                            unpack8(*reinterpret_cast<const uint4*>(tile(in + kInX) + sw128(row, 4 * half + q)), xv);
+                            if (zp) unpack8(q == 0 ? z0 : q == 1 ? z1 : q == 2 ? z2 : z3, zv);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                float y = fmaf(Dh, xv[i], __uint_as_float(mx[8 * qq + i]));
+                                if (with_state) y = fmaf(e, __uint_as_float(cs[8 * qq + i]), y);
+                                if (zp) y *= silu_f<false>(zv[i]);
+                                yd[8 * qq + i] = y;
+                            }
+                        }
+                        store16<Tout>(yp + yoff + 16 * hq, yd);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bar_y[cc & 1]);
+        };
+
+        float e_prev = 0.f;      // exp(cs_i) of the previous chunk (its output is pending)
+        bool prev_state = false;
         for (int c = 0; c < nchunks; ++c) {
             const int64_t t0 = (int64_t)c * kQ;
             const uint32_t par = (uint32_t)(c & 1);
             const int in = kInTiles * (c & 1);
+            const uint32_t gcol = (c & 1) ? kColG1 : kColG0;
             const bool had_state = c > 0 || init_state;
             if (tid < kQ) {  // publish this chunk's sums (the last reads of the previous ones are done)
                 s_dl[tid] = nx_dl;
@@ -345,10 +429,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             }
             worker_sync();
             const float cs_last = s_cs[kQ - 1];
+            if (c > 0) load_z(c - 1);  // used by the previous chunk's output below
 
             // w * X (hi / lo) for the state update (warps 0-3, row j = row), and the decay of the
             // carried state by exp(cs_last) (warps 4-7, state row n = row).
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1)));
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1)));
             if (ok && half == 0) {
                 const float w = ex2_approx(cs_last - s_cs[row]) * s_dl[row];
 #pragma unroll
@@ -365,39 +450,47 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             } else if (ok && had_state) {
                 const float dec = ex2_approx(cs_last);
 #pragma unroll 1
-                for (int part = 0; part < 4; ++part) {
+                for (int part = 0; part < 2; ++part) {
                     float v[32];
                     tmem_ld32(tmem + tlane + kColS + 32 * part, v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= dec;
                     tmem_st32(tmem + tlane + kColS + 32 * part, v);
                 }
+                tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bar_x);
 
+            // The previous chunk's output, while this chunk's C B^T and C S run.
+            if (c > 0) output(c - 1, e_prev, prev_state);
+
             // M = G * exp(cs_i - cs_j) * Delta_j (j <= i) as bf16 hi / lo pairs (row i = row,
-            // columns 64*half..+63), and with a carried state Y = exp(cs_i) * (C S hi + C S lo).
-            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g1, par));
+            // columns 64*half..+63), written over the 16 columns of G they came from: columns
+            // [16k, 16k+8) hold M hi of j = 16k..16k+15 (bf16 pairs), [16k+8, 16k+16) M lo.
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_gg[c & 1], (uint32_t)((c >> 1) & 1)));
             tc_fence_after_sync();
+            const float cs_i = s_cs[row];
             if (ok) {
-                const float cs_i = s_cs[row];
                 const bool live = t0 + row < L;
                 const bool any = 64 * half <= quarter * 32 + 31;  // a column of this half is on or below the diagonal
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    uint32_t gp[32];
-                    if (any) {
-                        tmem_ld32_async(tmem + tlane + kColG + 64 * half + 32 * part, gp);
+                for (int piece = 0; piece < 4; ++piece) {  // 16 columns of G: j = 16k .. 16k+15
+                    const int k = 4 * half + piece;
+                    const uint32_t col = gcol + 16 * k;
+                    const bool need = any && 16 * k <= quarter * 32 + 31;  // warp-uniform
+                    uint32_t gp[16];
+                    if (need) {
+                        tmem_ld16_async(tmem + tlane + col, gp);
                         tmem_wait_ld();
                     }
-                    uint32_t mh[16], ml[16];
+                    uint32_t mh[8], ml[8];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = 64 * half + 32 * part + 2 * e;
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 16 * k + 2 * e;
                         float2 m = make_float2(0.f, 0.f);
-                        if (any && live && j <= row) {
+                        if (need && live && j <= row) {
                             const float2 cj = *reinterpret_cast<const float2*>(&s_cs[j]);
                             const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
                             const float2 dec = make_float2(ex2_approx(cs_i - cj.x),
@@ -407,86 +500,41 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                         }
                         split2(m, mh[e], ml[e]);
                     }
-                    tmem_st16_async(tmem + tlane + kColMhi + 32 * half + 16 * part, mh);
-                    tmem_st16_async(tmem + tlane + kColMlo + 32 * half + 16 * part, ml);
-                }
-                if (had_state) {
-                    uint32_t yh[32], yl[32];
-                    tmem_ld32_async(tmem + tlane + kColYo + 32 * half, yh);
-                    tmem_ld32_async(tmem + tlane + kColYo + 64 + 32 * half, yl);
-                    tmem_wait_ld();
-                    const float e = ex2_approx(cs_i);
-                    float ys[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ys[i] = e * (__uint_as_float(yh[i]) + __uint_as_float(yl[i]));
-                    tmem_st32(tmem + tlane + kColYo + 32 * half, ys);
+                    tmem_st8_async(tmem + tlane + col, mh);
+                    tmem_st8_async(tmem + tlane + col + 8, ml);
                 }
                 tmem_wait_st();
             }
             tc_fence_before_sync();
             mbar_arrive(&bar_m);
+            e_prev = ex2_approx(cs_i);
+            prev_state = had_state;
 
-            const int64_t t_row = t0 + row;
-            const int64_t yoff = ((int64_t)b * L + t_row) * H * kHeadDim + (int64_t)h * kHeadDim + 32 * half;
-
-            // The updated state -> hi / lo for the next chunk's C S.
+            // The updated state -> hi / lo for the next chunk's C S (the wait on the state
+            // update also covers this chunk's C S, issued before it).
             ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g4, par));
             tc_fence_after_sync();
             if (ok) {
-                uint32_t ra[32], rb[32];
-                tmem_ld32_async(tmem + tlane + kColS + 32 * half, ra);
-                tmem_ld32_async(tmem + tlane + kColS + 64 + 32 * half, rb);
-                tmem_wait_ld();
-                float sa[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sa[i] = __uint_as_float(ra[i]) + __uint_as_float(rb[i]);
-                put_state_split(sa);
+                float sv[32];
+                tmem_ld32(tmem + tlane + kColS + 32 * half, sv);
+                put_state_split(sv);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bar_s);
             // The next chunk's Delta and running sums, while M X runs.
             if (c + 1 < nchunks) chunk_sums(c + 1);
-
-            // y = Y + D x, times silu(z): row i = row, headdim columns 32*half..+31.
-            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g2, par));
-            tc_fence_after_sync();
-            if (ok) {
-                float yd[32];
-                tmem_ld32(tmem + tlane + kColYo + 32 * half, yd);
-                if (t_row < L) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float xv[8], zv[8];
-                        unpack8(*reinterpret_cast<const uint4*>(tile(in + kInX) + sw128(row, 4 * half + q)), xv);
-                        if (zp) unpack8(q == 0 ? z0 : q == 1 ? z1 : q == 2 ? z2 : z3, zv);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            float y = fmaf(Dh, xv[i], yd[8 * q + i]);
-                            if (zp) y *= silu_f<false>(zv[i]);
-                            yd[8 * q + i] = y;
-                        }
-                    }
-                    store32<Tout>(yp + yoff, yd);
-                }
-            }
-            if (zp && c + 1 < nchunks && t_row + kQ < L) {  // z of the next chunk
-                const uint4* zq = reinterpret_cast<const uint4*>(zp + yoff + (int64_t)kQ * H * kHeadDim);
-                z0 = zq[0]; z1 = zq[1]; z2 = zq[2]; z3 = zq[3];
-            }
-            tc_fence_before_sync();
-            mbar_arrive(&bar_y);
             if (!ok) break;
         }
+        if (ok && nchunks > 0) {
+            load_z(nchunks - 1);
+            output(nchunks - 1, e_prev, prev_state);
+        }
 
-        if (ok && a.final_state) {  // Sa + Sb [n][p] -> final_state (p, n)
+        if (ok && a.final_state) {  // S[n][p] -> final_state (p, n)
             float v[32];
             if (nchunks > 0 || init_state) {
-                float sb[32];
                 tmem_ld32(tmem + tlane + kColS + 32 * half, v);
-                tmem_ld32(tmem + tlane + kColS + 64 + 32 * half, sb);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] += sb[i];
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
