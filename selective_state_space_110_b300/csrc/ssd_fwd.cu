@@ -429,7 +429,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             }
             worker_sync();
             const float cs_last = s_cs[kQ - 1];
-            if (c > 0) load_z(c - 1);  // used by the previous chunk's output below
 
             // w * X (hi / lo) for the state update (warps 0-3, row j = row), and the decay of the
             // carried state by exp(cs_last) (warps 4-7, state row n = row).
@@ -522,14 +521,14 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&bar_s);
-            // The next chunk's Delta and running sums, while M X runs.
+            // z of this chunk's output (written in the next iteration; loaded here so that it
+            // lands before the next proxy fence), and the next chunk's Delta and running sums,
+            // while M X runs.
+            load_z(c);
             if (c + 1 < nchunks) chunk_sums(c + 1);
             if (!ok) break;
         }
-        if (ok && nchunks > 0) {
-            load_z(nchunks - 1);
-            output(nchunks - 1, e_prev, prev_state);
-        }
+        if (ok && nchunks > 0) output(nchunks - 1, e_prev, prev_state);
 
         if (ok && a.final_state) {  // S[n][p] -> final_state (p, n)
             float v[32];
