@@ -138,3 +138,17 @@ def test_split_sequence_equals_one_call():
     torch.cuda.synchronize()
     assert_close(torch.cat([y1, y2], dim=1), y.double(), TOL_BF16, "split y")
     assert_close(f2, fin.double(), TOL_BF16, "split final state")
+
+
+@pytest.mark.parametrize("dt_range", [(0.2, 0.5), (5.0, 8.0)], ids=["mixed", "strong"])
+def test_strong_decay(dt_range):
+    """Steps large enough that the decay over 16 tokens exceeds 2^64 in many heads, so that both
+    ways of forming M's decays are taken: the product of a row and a column factor within such a
+    16-token piece, and the per-element exponential where a piece decays further."""
+    cfg = SsdConfig("decay", 2, 500, 8, 64, 1, 128, 77, dt_min=dt_range[0], dt_max=dt_range[1])
+    x = make_ssd_inputs(cfg, DEV)
+    y, fin = _gpu(x, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ry, rf = _oracle(x)
+    assert_close(y, ry, TOL_BF16, "y")
+    assert_close(fin, rf, TOL_BF16, "final state")
