@@ -142,7 +142,7 @@ def test_split_sequence_equals_one_call():
 
 @pytest.mark.parametrize("dt_range", [(0.2, 0.5), (5.0, 8.0)], ids=["mixed", "strong"])
 def test_strong_decay(dt_range):
-    """Steps large enough that the decay over 16 tokens exceeds 2^-64 in many heads (and, for
+    """Steps large enough that the decay factor over 16 tokens falls below 2^-64 in many heads (and, for
     steps of 5-8, that the state is all but forgotten from one token to the next): M's decays
     underflow for distant tokens and the carried state's contribution vanishes, with no
     overflow or NaN on the way."""
