@@ -651,6 +651,58 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_oracle_timings(args):
+    """The fp64 oracle as it stands, on the host cores, over whole workloads (a baseline only):
+    C0-C3 in full (rows in batches; only the oracle calls are timed) and decode at batch 64 on
+    8 of the 64 layers for 8 steps, scaled to a 64-layer step. One JSON line per workload."""
+    import numpy as np
+    import oracle
+    from workloads import (DECODE_CONFIG, make_decode_layer_params, make_decode_state,
+                           make_decode_tokens)
+    cores = oracle.max_threads()
+    f64 = oracle._f64
+    for name in ("c0_tiny_f32", "c1_mamba130m", "c2_mamba2p8b", "c3_long_1m"):
+        cfg = scan_config(name)
+        x = make_scan_inputs(cfg, "cpu")
+        R = cfg.batch * cfg.dim
+        per_call = max(1, min(R, (1 << 26) // cfg.seqlen))  # about 64 M elements a call
+        A, B, C = f64(x["A"]), f64(x["B"]), f64(x["C"])
+        D = None if x["D"] is None else f64(x["D"])
+        bias = None if x["delta_bias"] is None else f64(x["delta_bias"])
+        total = 0.0
+        for r0 in range(0, R, per_call):
+            rows = np.arange(r0, min(R, r0 + per_call), dtype=np.int64)
+            sl = lambda t: None if t is None else f64(t.reshape(R, -1)[r0:r0 + len(rows)])
+            u, dl, z = sl(x["u"]), sl(x["delta"]), sl(x["z"])
+            t0 = time.perf_counter()
+            oracle.scan_fwd_rows(rows, u, dl, A, B, C, D, z, bias, x["delta_softplus"])
+            total += time.perf_counter() - t0
+        elems = R * cfg.seqlen
+        print(json.dumps({"oracle_timing": name, "value": round(elems / total, 1), "unit": "elem/s",
+                          "seconds": round(total, 3), "elements": elems, "cores": cores,
+                          "kind": "oracle", "sample": "all rows and tokens"}), flush=True)
+        del x
+    dc = DECODE_CONFIG
+    batch, layers, steps = 64, 8, 8
+    p = {k: f64(v) for k, v in make_decode_layer_params(dc, "cpu").items()}
+    total = 0.0
+    for layer in range(layers):
+        state = f64(make_decode_state(dc, batch, layer, "cpu"))
+        for step in range(steps):
+            t = {k: f64(v) for k, v in make_decode_tokens(dc, batch, layer, step % dc.ring, "cpu").items()}
+            t0 = time.perf_counter()
+            state, _ = oracle.state_update(state, t["x"], t["dt"], p["A"], t["B"], t["C"], p["D"],
+                                           t["z"], p["dt_bias"], True)
+            total += time.perf_counter() - t0
+    per_call = total / (layers * steps)
+    print(json.dumps({"oracle_timing": f"{dc.name}_batch{batch}",
+                      "value": round(1.0 / (per_call * dc.layers), 2), "unit": "steps/s",
+                      "seconds_per_layer_call": round(per_call, 6), "cores": cores,
+                      "kind": "oracle",
+                      "sample": f"{layers} of {dc.layers} layers x {steps} steps, scaled to "
+                                f"{dc.layers} layers"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -670,7 +722,12 @@ def main():
                     help="with --profile: the forward scan (default), the backward, or the SSD "
                          "layer (--ssd-workload)")
     ap.add_argument("--ssd-workload", default="ssd1_mamba2_2p7b")
+    ap.add_argument("--oracle-timings", action="store_true",
+                    help="time the fp64 oracle on the host cores over C0-C3 and decode, and exit")
     args = ap.parse_args()
+    if args.oracle_timings:
+        run_oracle_timings(args)
+        return
     if args.profile:
         run_profile(args)
         return
