@@ -39,9 +39,9 @@ ALU_ELEM_PER_CLK_PER_SM = 2.0  # 16 SFU exp2 (32/clk/SM) and 64 FP32 lane-ops (1
 BWD_ELEM_PER_CLK_PER_SM = 32.0 / 48.0  # backward: 48 SFU exp2 per element at 32/clk/SM
 BWD_CKPT_ELEM_PER_CLK_PER_SM = 32.0 / 32.0  # backward given the forward's checkpoints: 32 exp2
 L2_FLUSH_BYTES = 256 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum of one scan_kernel launch, from the ncu capture
-# summarised in profiles/scan_fwd_c2_mamba2p8b.md (same kernel code): 252.8 MB + 50.1 MB.
-SCAN_TRAFFIC_BYTES = {"c2_mamba2p8b": 302_900_000}
+# dram__bytes_read.sum + dram__bytes_write.sum of one scan_kernel launch on this workload, from
+# one ncu capture of the same kernel code (summarised under profiles/): 252.8 MB + 50.3 MB.
+SCAN_TRAFFIC_BYTES = {"c2_mamba2p8b": 303_045_888}
 
 
 # ------------------------------------------------------------------------------------------
