@@ -92,3 +92,21 @@ def test_update_bf16_output_and_no_gate():
     assert out.dtype == torch.bfloat16
     assert_close(out, ref, TOL[torch.bfloat16], "y")
     assert_close(st, ref_state, TOL[torch.bfloat16], "state")
+
+
+def test_ragged_channels_larger_batch():
+    """1,000 channels (the last block of 64 part-empty) at batch 40: every row checked over
+    three steps."""
+    cfg = DECODE_CONFIG.replace(dim=1000)
+    batch = 40
+    p = make_decode_layer_params(cfg, DEV)
+    st = make_decode_state(cfg, batch, 0, DEV)
+    ref_state = st.clone()
+    for step in range(3):
+        tok = make_decode_tokens(cfg, batch, 0, step, DEV)
+        out = ssm_state_update(st, tok["x"], tok["dt"], p["A"], tok["B"], tok["C"], p["D"],
+                               tok["z"], dt_bias=p["dt_bias"], out_dtype=torch.float32)
+        ref_state, ref = oracle.state_update(ref_state, tok["x"], tok["dt"], p["A"], tok["B"],
+                                             tok["C"], p["D"], tok["z"], p["dt_bias"], True)
+        assert_close(out, ref, TOL[torch.bfloat16], f"step {step} y")
+        assert_close(st, ref_state, TOL[torch.bfloat16], f"step {step} state")
