@@ -14,19 +14,20 @@
 // which is the recurrence H_t = exp(a_t) H_{t-1} + Delta_t x_t B_t^T, y_t = C_t . H_t + D x_t
 // evaluated a chunk at a time.
 //
-// One CTA per (b, h) walks the chunks in order: 288 threads, 8 worker warps and one issuing
-// warp. Worker thread (row, half) serves tensor-memory lane `row` (the chunk's token row, or the
-// state row n) and one half of the columns; lane 0 of the issuing warp starts every TMA load and
-// every MMA. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
-// next chunk's tiles load while this one computes; the next chunk's Delta sums are computed
-// ahead of use. The products run as tcgen05.mma (bf16 operands, fp32 accumulators in tensor
+// One CTA per (b, h) walks the chunks in order: 320 threads, 8 worker warps, one issuing warp
+// and one sums warp. Worker thread (row, half) serves tensor-memory lane `row` (the chunk's
+// token row, or the state row n) and one half of the columns; lane 0 of the issuing warp starts
+// every TMA load and every MMA; the sums warp computes each chunk's Delta and running sums (lane
+// l: tokens 4l..4l+3) ahead of use and publishes them once the workers have built the previous
+// chunk's M. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
+// next chunk's tiles load while this one computes. The products run as tcgen05.mma (bf16 operands, fp32 accumulators in tensor
 // memory); their completion reaches the workers through mbarriers (tcgen05.commit), and the
 // workers hand finished operands to the issuer through mbarriers they arrive on.
 //
 // The workers are the busy side, so the tensor cores get their operands early and the workers
 // never wait on a product in steady state. Per chunk c the workers (1) scale x by w and decay
 // the state, (2) write the output of chunk c-1, (3) build M of chunk c, (4) split the updated
-// state for the next C S and compute the next chunk's sums. Meanwhile C B^T of chunk c (into
+// state for the next C S. Meanwhile C B^T of chunk c (into
 // the G buffer of c's parity, free since the output of c-2) and C S run before (1) ends, the
 // state update during (2) and M X during (4) and the next chunk's (1). Chunk c's output is
 // y = exp(cs_i) (C S) + M X + D x: C S and M X have accumulators of their own, so neither
@@ -57,7 +58,8 @@ constexpr int kQ = 128;              // tokens per chunk (the MMA's M)
 constexpr int kHeadDim = 64;         // P
 constexpr int kSsdState = 128;       // N
 constexpr int kWorkers = 256;        // threads that move data (8 warps)
-constexpr int kSsdThreads = kWorkers + 32;  // plus one warp that issues TMA loads and MMAs
+constexpr int kSsdThreads = kWorkers + 64;  // plus a warp that issues TMA loads and MMAs and one
+                                            // that computes each chunk's Delta sums
 constexpr int kTile = 16384;         // one 128-row x 128-byte swizzled tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG0 = 0, kColG1 = 128, kColS = 256, kColCS0 = 320, kColCS1 = 384, kColMX = 448;
@@ -165,10 +167,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     // (x ready, M ready, state split ready, output of a chunk read, per buffer).
     __shared__ unsigned long long bar_tma[2], bar_gg[2], bar_g4, bar_g2;
     __shared__ unsigned long long bar_x, bar_m, bar_s, bar_y[2];
+    // The sums warp and the workers: a chunk's Delta and running sums are published (bar_sums),
+    // and the workers' last reads of them are done (bar_free).
+    __shared__ unsigned long long bar_sums, bar_free;
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(16) float s_cs[kQ];  // running sum of Delta*A*log2(e), inclusive
     __shared__ __align__(16) float s_dl[kQ];  // Delta
-    __shared__ float s_wsum[4];
     __shared__ int s_ok;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     auto tile = [&](int i) { return sm + i * kTile; };
@@ -194,6 +198,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         mbar_init(&bar_s, kWorkers);
         mbar_init(&bar_y[0], kWorkers);
         mbar_init(&bar_y[1], kWorkers);
+        mbar_init(&bar_sums, 32);
+        mbar_init(&bar_free, kWorkers);
         fence_mbar_init();
         s_ok = 1;
     }
@@ -324,47 +330,58 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             if (!ok) s_ok = 0;
         }
         __syncwarp();
-    } else {
-        // ---------------- 256 worker threads ----------------
+    } else if (warp == kWorkers / 32 + 1) {
+        // ---------------- sums warp: Delta and running sums of each chunk ----------------
+        // Lane l takes tokens 4l .. 4l+3 of the chunk: softplus, a running sum over its four
+        // tokens, then an inclusive scan of the lane totals across the warp.
         const float A2 = a.A[h] * kLog2e;
         const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
-        const float Dh = a.D ? a.D[h] : 0.f;
         const __nv_bfloat16* dt = static_cast<const __nv_bfloat16*>(a.dt);
+        float raw[4];
+        auto load_dt = [&](int c) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t t = (int64_t)c * kQ + 4 * lane + i;
+                raw[i] = (c < nchunks && t < L) ? __bfloat162float(dt[((int64_t)b * L + t) * H + h]) : 0.f;
+            }
+        };
+        load_dt(0);
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            float dl[4], cs[4];
+            float run = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t t = (int64_t)c * kQ + 4 * lane + i;
+                const float v = raw[i] + bias;
+                dl[i] = t < L ? (a.softplus ? softplus_f<true>(v) : v) : 0.f;
+                run += dl[i] * A2;
+                cs[i] = run;
+            }
+            load_dt(c + 1);
+            float incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const float excl = incl - run;
+            // The buffer held chunk c - 1: wait until the workers have read it (they have then
+            // built that chunk's M; the next chunk's sums are ready by then).
+            if (c >= 1) ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_free, (uint32_t)((c - 1) & 1)));
+            if (!ok) break;
+            *reinterpret_cast<float4*>(&s_dl[4 * lane]) = make_float4(dl[0], dl[1], dl[2], dl[3]);
+            *reinterpret_cast<float4*>(&s_cs[4 * lane]) =
+                make_float4(excl + cs[0], excl + cs[1], excl + cs[2], excl + cs[3]);
+            mbar_arrive(&bar_sums);
+        }
+        if (!ok) s_ok = 0;
+    } else {
+        // ---------------- 256 worker threads ----------------
+        const float Dh = a.D ? a.D[h] : 0.f;
         const __nv_bfloat16* zp = static_cast<const __nv_bfloat16*>(a.z);
         Tout* yp = static_cast<Tout*>(a.y);
-        auto load_dt = [&](int c) -> float {  // raw dt of token row `tid` of chunk c (tid < 128)
-            const int64_t t = (int64_t)c * kQ + tid;
-            return (c < nchunks && t < L) ? __bfloat162float(dt[((int64_t)b * L + t) * H + h]) : 0.f;
-        };
-        auto worker_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory"); };
-
         bool ok = true;
-        float dt_raw = tid < kQ ? load_dt(0) : 0.f;  // raw dt of the next chunk to be summed
-        // Delta and the running sum of Delta*A over chunk c for token `tid` (warps 0-3; the
-        // other warps only take part in the barrier), kept in registers until the chunk starts.
-        float nx_dl = 0.f, nx_cs = 0.f;
-        auto chunk_sums = [&](int c) {
-            if (tid < kQ) {
-                const float v = dt_raw + bias;
-                nx_dl = ((int64_t)c * kQ + tid < L) ? (a.softplus ? softplus_f<true>(v) : v) : 0.f;
-                dt_raw = load_dt(c + 1);
-                float s = nx_dl * A2;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float n = __shfl_up_sync(0xffffffffu, s, o);
-                    if (lane >= o) s += n;
-                }
-                if (lane == 31) s_wsum[warp] = s;
-                nx_cs = s;
-            }
-            worker_sync();
-            if (tid < kQ) {
-                float off = 0.f;
-                for (int w = 0; w < warp; ++w) off += s_wsum[w];
-                nx_cs += off;
-            }
-        };
-        if (nchunks > 0) chunk_sums(0);
         // z of this thread's outputs of chunk cc (row i = row, headdim 32*half..+31), loaded
         // ahead of the output step.
         uint4 z0 = make_uint4(0u, 0u, 0u, 0u), z1 = z0, z2 = z0, z3 = z0;
@@ -423,18 +440,16 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             const int in = kInTiles * (c & 1);
             const uint32_t gcol = (c & 1) ? kColG1 : kColG0;
             const bool had_state = c > 0 || init_state;
-            if (tid < kQ) {  // publish this chunk's sums (the last reads of the previous ones are done)
-                s_dl[tid] = nx_dl;
-                s_cs[tid] = nx_cs;
-            }
-            worker_sync();
-            const float cs_last = s_cs[kQ - 1];
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_sums, par));
+            const float* const scs = s_cs;
+            const float* const sdl = s_dl;
+            const float cs_last = scs[kQ - 1];
 
             // w * X (hi / lo) for the state update (warps 0-3, row j = row), and the decay of the
             // carried state by exp(cs_last) (warps 4-7, state row n = row).
             ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1)));
             if (ok && half == 0) {
-                const float w = ex2_approx(cs_last - s_cs[row]) * s_dl[row];
+                const float w = ex2_approx(cs_last - scs[row]) * sdl[row];
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     float v[8];
@@ -470,7 +485,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             // [16k, 16k+8) hold M hi of j = 16k..16k+15 (bf16 pairs), [16k+8, 16k+16) M lo.
             ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_gg[c & 1], (uint32_t)((c >> 1) & 1)));
             tc_fence_after_sync();
-            const float cs_i = s_cs[row];
+            const float cs_i = scs[row];
             if (ok) {
                 const bool live = t0 + row < L;
                 const bool any = 64 * half <= quarter * 32 + 31;  // a column of this half is on or below the diagonal
@@ -490,8 +505,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                         const int j = 16 * k + 2 * e;
                         float2 m = make_float2(0.f, 0.f);
                         if (need && live && j <= row) {
-                            const float2 cj = *reinterpret_cast<const float2*>(&s_cs[j]);
-                            const float2 dj = *reinterpret_cast<const float2*>(&s_dl[j]);
+                            const float2 cj = *reinterpret_cast<const float2*>(&scs[j]);
+                            const float2 dj = *reinterpret_cast<const float2*>(&sdl[j]);
                             const float2 dec = make_float2(ex2_approx(cs_i - cj.x),
                                                            j + 1 <= row ? ex2_approx(cs_i - cj.y) : 0.f);
                             const float2 gv = make_float2(__uint_as_float(gp[2 * e]), __uint_as_float(gp[2 * e + 1]));
@@ -506,6 +521,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             }
             tc_fence_before_sync();
             mbar_arrive(&bar_m);
+            mbar_arrive(&bar_free);  // this chunk's sums are no longer read
             e_prev = ex2_approx(cs_i);
             prev_state = had_state;
 
@@ -522,10 +538,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             tc_fence_before_sync();
             mbar_arrive(&bar_s);
             // z of this chunk's output (written in the next iteration; loaded here so that it
-            // lands before the next proxy fence), and the next chunk's Delta and running sums,
-            // while M X runs.
+            // lands before the next proxy fence).
             load_z(c);
-            if (c + 1 < nchunks) chunk_sums(c + 1);
             if (!ok) break;
         }
         if (ok && nchunks > 0) output(nchunks - 1, e_prev, prev_state);
