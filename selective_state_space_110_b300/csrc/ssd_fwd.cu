@@ -417,11 +417,15 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                             unpack8(*reinterpret_cast<const uint4*>(tile(in + kInX) + sw128(row, 4 * half + q)), xv);
                             if (zp) unpack8(q == 0 ? z0 : q == 1 ? z1 : q == 2 ? z2 : z3, zv);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                float y = fmaf(Dh, xv[i], __uint_as_float(mx[8 * qq + i]));
-                                if (with_state) y = fmaf(e, __uint_as_float(cs[8 * qq + i]), y);
-                                if (zp) y *= silu_f<false>(zv[i]);
-                                yd[8 * qq + i] = y;
+                            for (int i = 0; i < 8; i += 2) {  // pairs, packed
+                                const int o = 8 * qq + i;
+                                float2 y = __ffma2_rn(f2(Dh), make_float2(xv[i], xv[i + 1]),
+                                                      make_float2(__uint_as_float(mx[o]), __uint_as_float(mx[o + 1])));
+                                if (with_state)
+                                    y = __ffma2_rn(f2(e), make_float2(__uint_as_float(cs[o]), __uint_as_float(cs[o + 1])), y);
+                                if (zp) y = __fmul2_rn(y, silu2(make_float2(zv[i], zv[i + 1])));
+                                yd[o] = y.x;
+                                yd[o + 1] = y.y;
                             }
                         }
                         store16<Tout>(yp + yoff + 16 * hq, yd);
