@@ -459,7 +459,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                     float v[8];
                     unpack8(*reinterpret_cast<const uint4*>(tile(in + kInX) + sw128(row, ch)), v);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] *= w;
+                    for (int e = 0; e < 8; e += 2) {
+                        const float2 p2 = __fmul2_rn(make_float2(v[e], v[e + 1]), f2(w));
+                        v[e] = p2.x;
+                        v[e + 1] = p2.y;
+                    }
                     uint4 hi, lo;
                     split8(v, hi, lo);
                     *reinterpret_cast<uint4*>(tile(kTXH) + sw128(row, ch)) = hi;
@@ -472,7 +476,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                     float v[32];
                     tmem_ld32(tmem + tlane + kColS + 32 * part, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= dec;
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 d2 = __fmul2_rn(make_float2(v[i], v[i + 1]), f2(dec));
+                        v[i] = d2.x;
+                        v[i + 1] = d2.y;
+                    }
                     tmem_st32(tmem + tlane + kColS + 32 * part, v);
                 }
                 tmem_wait_st();
