@@ -71,6 +71,9 @@ constexpr int kInC = 0, kInB = 2, kInX = 4, kInTiles = 5;
 constexpr int kTSH = 10, kTSL = 11;  // state hi | lo: rows n, headdim (MN-major), adjacent
 constexpr int kTXH = 12, kTXL = 13;  // w * X hi | lo: rows j, headdim (MN-major), adjacent
 constexpr int kNumTiles = 14;
+// Largest decay (log2 units) over a 16-token piece for which M's decay is taken as a row factor
+// times a column factor: 2^64 times Delta stays far inside the fp32 range.
+constexpr float kFactorSpan = 64.f;
 constexpr int kSsdSmemBytes = kNumTiles * kTile + 1024;
 
 __device__ unsigned int g_ssd_status;
@@ -173,6 +176,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(16) float s_cs[kQ];  // running sum of Delta*A*log2(e), inclusive
     __shared__ __align__(16) float s_dl[kQ];  // Delta
+    // M's decay within 16-token piece k as a product: the column factor
+    // 2^(cs_16k - cs_j) * Delta_j, and the piece's span cs_16k - cs_16k+15 (log2 units).
+    __shared__ __align__(16) float s_cf[kQ];
+    __shared__ float s_span[kQ / 16];
     __shared__ int s_ok;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     auto tile = [&](int i) { return sm + i * kTile; };
@@ -370,9 +377,19 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             // built that chunk's M; the next chunk's sums are ready by then).
             if (c >= 1) ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_free, (uint32_t)((c - 1) & 1)));
             if (!ok) break;
+            float csv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) csv[i] = excl + cs[i];
+            // piece k = lanes 4k..4k+3: its first token's sum sits in lane 4k, its last in 4k+3
+            const float ref = __shfl_sync(0xffffffffu, csv[0], lane & ~3);
+            const float span = ref - __shfl_sync(0xffffffffu, csv[3], lane | 3);
+            float cf[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cf[i] = fabsf(span) < kFactorSpan ? ex2_approx(ref - csv[i]) * dl[i] : 0.f;
             *reinterpret_cast<float4*>(&s_dl[4 * lane]) = make_float4(dl[0], dl[1], dl[2], dl[3]);
-            *reinterpret_cast<float4*>(&s_cs[4 * lane]) =
-                make_float4(excl + cs[0], excl + cs[1], excl + cs[2], excl + cs[3]);
+            *reinterpret_cast<float4*>(&s_cs[4 * lane]) = make_float4(csv[0], csv[1], csv[2], csv[3]);
+            *reinterpret_cast<float4*>(&s_cf[4 * lane]) = make_float4(cf[0], cf[1], cf[2], cf[3]);
+            if ((lane & 3) == 0) s_span[lane >> 2] = span;
             mbar_arrive(&bar_sums);
         }
         if (!ok) s_ok = 0;
@@ -512,19 +529,40 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                         tmem_wait_ld();
                     }
                     uint32_t mh[8], ml[8];
+                    // exp(cs_i - cs_j) Delta_j = 2^(cs_i - cs_16k) [2^(cs_16k - cs_j) Delta_j]: one
+                    // exp per row and piece where the piece's decay span keeps both factors in
+                    // range (rows decaying further make the first factor underflow to a
+                    // negligible term); other pieces take the exp per element.
+                    const bool factored = fabsf(s_span[k]) < kFactorSpan;  // warp-uniform
+                    if (factored) {
+                        const float rf = ex2_approx(cs_i - scs[16 * k]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 16 * k + 2 * e;
-                        float2 m = make_float2(0.f, 0.f);
-                        if (need && live && j <= row) {
-                            const float2 cj = *reinterpret_cast<const float2*>(&scs[j]);
-                            const float2 dj = *reinterpret_cast<const float2*>(&sdl[j]);
-                            const float2 dec = make_float2(ex2_approx(cs_i - cj.x),
-                                                           j + 1 <= row ? ex2_approx(cs_i - cj.y) : 0.f);
-                            const float2 gv = make_float2(__uint_as_float(gp[2 * e]), __uint_as_float(gp[2 * e + 1]));
-                            m = __fmul2_rn(__fmul2_rn(gv, dec), dj);
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 16 * k + 2 * e;
+                            float2 m = make_float2(0.f, 0.f);
+                            if (need && live && j <= row) {
+                                const float2 gv = make_float2(__uint_as_float(gp[2 * e]), __uint_as_float(gp[2 * e + 1]));
+                                const float2 cf = *reinterpret_cast<const float2*>(&s_cf[j]);
+                                m = __fmul2_rn(__fmul2_rn(gv, cf), f2(rf));
+                                if (j + 1 > row) m.y = 0.f;
+                            }
+                            split2(m, mh[e], ml[e]);
                         }
-                        split2(m, mh[e], ml[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 16 * k + 2 * e;
+                            float2 m = make_float2(0.f, 0.f);
+                            if (need && live && j <= row) {
+                                const float2 cj = *reinterpret_cast<const float2*>(&scs[j]);
+                                const float2 dj = *reinterpret_cast<const float2*>(&sdl[j]);
+                                const float2 dec = make_float2(ex2_approx(cs_i - cj.x),
+                                                               j + 1 <= row ? ex2_approx(cs_i - cj.y) : 0.f);
+                                const float2 gv = make_float2(__uint_as_float(gp[2 * e]), __uint_as_float(gp[2 * e + 1]));
+                                m = __fmul2_rn(__fmul2_rn(gv, dec), dj);
+                            }
+                            split2(m, mh[e], ml[e]);
+                        }
                     }
                     tmem_st8_async(tmem + tlane + col, mh);
                     tmem_st8_async(tmem + tlane + col + 8, ml);

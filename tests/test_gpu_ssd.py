@@ -142,10 +142,11 @@ def test_split_sequence_equals_one_call():
 
 @pytest.mark.parametrize("dt_range", [(0.2, 0.5), (5.0, 8.0)], ids=["mixed", "strong"])
 def test_strong_decay(dt_range):
-    """Steps large enough that the decay factor over 16 tokens falls below 2^-64 in many heads (and, for
-    steps of 5-8, that the state is all but forgotten from one token to the next): M's decays
-    underflow for distant tokens and the carried state's contribution vanishes, with no
-    overflow or NaN on the way."""
+    """Steps large enough that the decay factor over 16 tokens falls below 2^-64 in many heads
+    (steps of 0.2-0.5: some 16-token pieces of a head on each side of that line; steps of 5-8:
+    the state all but forgotten from one token to the next). M's decays are then taken both
+    ways, as a row factor times a column factor within a piece and per element where a piece
+    decays further; they underflow for distant tokens with no overflow or NaN on the way."""
     cfg = SsdConfig("decay", 2, 500, 8, 64, 1, 128, 77, dt_min=dt_range[0], dt_max=dt_range[1])
     x = make_ssd_inputs(cfg, DEV)
     y, fin = _gpu(x, out_dtype=torch.float32)
