@@ -18,8 +18,10 @@
 // and one sums warp. Worker thread (row, half) serves tensor-memory lane `row` (the chunk's
 // token row, or the state row n) and one half of the columns; lane 0 of the issuing warp starts
 // every TMA load and every MMA; the sums warp computes each chunk's Delta and running sums (lane
-// l: tokens 4l..4l+3) ahead of use and publishes them once the workers have built the previous
-// chunk's M. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
+// l: tokens 4l..4l+3) and the column factors of M's decay ahead of use, and publishes them once
+// the workers have built the previous chunk's M. Within a 16-token piece k of columns,
+// exp(cs_i - cs_j) Delta_j = 2^(cs_i - cs_16k) * [2^(cs_16k - cs_j) Delta_j]: the workers take
+// one exp per row and piece; a piece whose decay exceeds 2^64 keeps one exp per element. C, B and x arrive by TMA into 128-byte-swizzled tiles, double-buffered so that the
 // next chunk's tiles load while this one computes. The products run as tcgen05.mma (bf16 operands, fp32 accumulators in tensor
 // memory); their completion reaches the workers through mbarriers (tcgen05.commit), and the
 // workers hand finished operands to the issuer through mbarriers they arrive on.
