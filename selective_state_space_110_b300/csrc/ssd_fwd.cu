@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 if (!ok) break;
                 tc_fence_after_sync();
                 // G = C B^T
-#pragma unroll 1
+#pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t off = (uint32_t)(k & 3) * 32;
                     umma_bf16(tmem + gcol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
@@ -294,9 +294,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                         tc_fence_after_sync();
                     }
                     const uint32_t ccol = (c & 1) ? kColCS1 : kColCS0;
-#pragma unroll 1
+#pragma unroll
                     for (int part = 0; part < 2; ++part)
-#pragma unroll 1
+#pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const uint32_t off = (uint32_t)(k & 3) * 32;
                             umma_bf16(tmem + ccol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
@@ -308,9 +308,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 ok = mbar_wait_bounded(&bar_x, par);
                 if (!ok) break;
                 tc_fence_after_sync();
-#pragma unroll 1
+#pragma unroll
                 for (int part = 0; part < 2; ++part)
-#pragma unroll 1
+#pragma unroll
                     for (int k = 0; k < 8; ++k)
                         umma_bf16(tmem + kColS, umma_desc_sw128(tile_addr(in + kInB) + (uint32_t)k * 2048, kTile, 1024),
                                   umma_desc_sw128(tile_addr(part ? kTXL : kTXH) + (uint32_t)k * 2048, kTile, 1024), i_s,
@@ -327,9 +327,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 ok = mbar_wait_bounded(&bar_m, par);
                 if (!ok) break;
                 tc_fence_after_sync();
-#pragma unroll 1
+#pragma unroll
                 for (int part = 0; part < 2; ++part)
-#pragma unroll 1
+#pragma unroll
                     for (int k = 0; k < 8; ++k)
                         umma_bf16_ts(tmem + kColMX, tmem + gcol + 16 * k + (part ? 8 : 0),
                                      umma_desc_sw128(tile_addr(in + kInX) + (uint32_t)k * 2048, kTile, 1024), i_cs,
