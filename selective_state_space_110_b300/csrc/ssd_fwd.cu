@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     // The sums warp and the workers: a chunk's Delta and running sums are published (bar_sums),
     // and the workers' last reads of them are done (bar_free).
     __shared__ unsigned long long bar_sums, bar_free;
+    __shared__ unsigned long long bar_drain;  // failure path: the issuer's MMAs in flight
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(16) float s_cs[kQ];  // running sum of Delta*A*log2(e), inclusive
     __shared__ __align__(16) float s_dl[kQ];  // Delta
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         mbar_init(&bar_y[0], kWorkers);
         mbar_init(&bar_y[1], kWorkers);
         mbar_init(&bar_sums, 32);
+        mbar_init(&bar_drain, 1);
         mbar_init(&bar_free, kWorkers);
         fence_mbar_init();
         s_ok = 1;
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             auto wait_y = [&](int cc) { return mbar_wait_bounded(&bar_y[cc & 1], (uint32_t)((cc >> 1) & 1)); };
             issue_tma(0);
             if (nchunks > 1) issue_tma(1);
+            int tma_issued = nchunks > 1 ? 2 : 1, tma_landed = 0;  // chunks
             const uint32_t i_g1 = umma_idesc_bf16(128, 128, false, false);  // C B^T
             const uint32_t i_cs = umma_idesc_bf16(128, 64, false, true);    // C S, M X
             const uint32_t i_s = umma_idesc_bf16(128, 64, true, true);      // B^T (w X)
@@ -273,6 +276,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 const uint32_t gcol = (c & 1) ? kColG1 : kColG0;
                 const bool had_state = c > 0 || init_state;
                 ok = mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
+                if (ok) tma_landed = c + 1;
                 // G buffer c & 1 (M of chunk c-2) and C S buffer c & 1 are free once the
                 // output of chunk c-2 has been read.
                 if (ok && c >= 2) ok = wait_y(c - 2);
@@ -321,7 +325,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 if (c > 0) {
                     ok = wait_y(c - 1);
                     if (!ok) break;
-                    if (c + 1 < nchunks) issue_tma(c + 1);
+                    if (c + 1 < nchunks) {
+                        issue_tma(c + 1);
+                        tma_issued = c + 2;
+                    }
                 }
                 // M X = M_hi X + M_lo X, M read from tensor memory (in place of G)
                 ok = mbar_wait_bounded(&bar_m, par);
@@ -336,7 +343,16 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                                      (part || k) ? 1u : 0u);
                 umma_commit(&bar_g2);
             }
-            if (!ok) s_ok = 0;
+            if (!ok) {
+                // A wait gave up: record it, then give the copies and products this CTA still
+                // has in flight a bounded chance to finish before the CTA leaves and frees its
+                // tensor memory.
+                s_ok = 0;
+                for (int cc = tma_landed; cc < tma_issued; ++cc)
+                    mbar_wait_bounded(&bar_tma[cc & 1], (uint32_t)((cc >> 1) & 1));
+                umma_commit(&bar_drain);
+                mbar_wait_bounded(&bar_drain, 0);
+            }
         }
         __syncwarp();
     } else if (warp == kWorkers / 32 + 1) {
