@@ -178,9 +178,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __shared__ unsigned long long bar_drain;  // failure path: the issuer's MMAs in flight
     __shared__ uint32_t tmem_slot;
     __shared__ __align__(16) float s_cs[kQ];  // running sum of Delta*A*log2(e), inclusive
-    __shared__ __align__(16) float s_dl[kQ];  // Delta
+    __shared__ __align__(16) float s_w[kQ];   // w_j = 2^(cs_last - cs_j) * Delta_j
     // M's decay within 16-token piece k as a product: the column factor
-    // 2^(cs_16k - cs_j) * Delta_j, and the piece's span cs_16k - cs_16k+15 (log2 units).
+    // 2^(cs_16k - cs_j) * Delta_j (Delta_j itself in pieces that are not factored), and the
+    // piece's span cs_16k - cs_16k+15 (log2 units).
     __shared__ __align__(16) float s_cf[kQ];
     __shared__ float s_span[kQ / 16];
     __shared__ int s_ok;
@@ -373,38 +374,61 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         load_dt(0);
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
-            float dl[4], cs[4];
+            float dl[4], al[4], cs[4];
             float run = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int64_t t = (int64_t)c * kQ + 4 * lane + i;
                 const float v = raw[i] + bias;
                 dl[i] = t < L ? (a.softplus ? softplus_f<true>(v) : v) : 0.f;
-                run += dl[i] * A2;
+                al[i] = dl[i] * A2;
+                run += al[i];
                 cs[i] = run;
             }
             load_dt(c + 1);
-            float incl = run;
+            // Sums of the lane totals before this lane (the chunk), before it within its piece
+            // of 4 lanes, and after it (the chunk): scans that add, never subtract, so that a
+            // decay between nearby tokens keeps its precision however far the chunk decays.
+            float incl = run, pincl = run, rincl = run;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float n = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += n;
+                const float r = __shfl_down_sync(0xffffffffu, rincl, o);
+                if (lane + o < 32) rincl += r;
             }
-            const float excl = incl - run;
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, pincl, o, 4);
+                if ((lane & 3) >= o) pincl += n;
+            }
+            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            float pexcl = __shfl_up_sync(0xffffffffu, pincl, 1, 4);
+            float after = __shfl_down_sync(0xffffffffu, rincl, 1);
+            if (lane == 0) excl = 0.f;
+            if ((lane & 3) == 0) pexcl = 0.f;
+            if (lane == 31) after = 0.f;
             // The buffer held chunk c - 1: wait until the workers have read it (they have then
             // built that chunk's M; the next chunk's sums are ready by then).
             if (c >= 1) ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_free, (uint32_t)((c - 1) & 1)));
             if (!ok) break;
-            float csv[4];
+            float csv[4], pl[4], wv[4];
+            float suf = 0.f;  // the tokens after token i within this lane
 #pragma unroll
-            for (int i = 0; i < 4; ++i) csv[i] = excl + cs[i];
+            for (int i = 3; i >= 0; --i) {
+                csv[i] = excl + cs[i];
+                pl[i] = pexcl + cs[i];  // running sum from the piece's first token
+                wv[i] = ex2_approx(suf + after) * dl[i];
+                suf += al[i];
+            }
             // piece k = lanes 4k..4k+3: its first token's sum sits in lane 4k, its last in 4k+3
-            const float ref = __shfl_sync(0xffffffffu, csv[0], lane & ~3);
-            const float span = ref - __shfl_sync(0xffffffffu, csv[3], lane | 3);
+            const float ref = __shfl_sync(0xffffffffu, pl[0], lane & ~3);
+            const float span = ref - __shfl_sync(0xffffffffu, pl[3], lane | 3);
+            const bool factored = fabsf(span) < kFactorSpan;
             float cf[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) cf[i] = fabsf(span) < kFactorSpan ? ex2_approx(ref - csv[i]) * dl[i] : 0.f;
-            *reinterpret_cast<float4*>(&s_dl[4 * lane]) = make_float4(dl[0], dl[1], dl[2], dl[3]);
+            for (int i = 0; i < 4; ++i) cf[i] = factored ? ex2_approx(ref - pl[i]) * dl[i] : dl[i];
+            *reinterpret_cast<float4*>(&s_w[4 * lane]) = make_float4(wv[0], wv[1], wv[2], wv[3]);
             *reinterpret_cast<float4*>(&s_cs[4 * lane]) = make_float4(csv[0], csv[1], csv[2], csv[3]);
             *reinterpret_cast<float4*>(&s_cf[4 * lane]) = make_float4(cf[0], cf[1], cf[2], cf[3]);
             if ((lane & 3) == 0) s_span[lane >> 2] = span;
@@ -481,14 +505,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             const bool had_state = c > 0 || init_state;
             ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_sums, par));
             const float* const scs = s_cs;
-            const float* const sdl = s_dl;
             const float cs_last = scs[kQ - 1];
 
             // w * X (hi / lo) for the state update (warps 0-3, row j = row), and the decay of the
             // carried state by exp(cs_last) (warps 4-7, state row n = row).
             ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1)));
             if (ok && half == 0) {
-                const float w = ex2_approx(cs_last - scs[row]) * sdl[row];
+                const float w = s_w[row];
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     float v[8];
@@ -573,7 +596,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                             float2 m = make_float2(0.f, 0.f);
                             if (need && live && j <= row) {
                                 const float2 cj = *reinterpret_cast<const float2*>(&scs[j]);
-                                const float2 dj = *reinterpret_cast<const float2*>(&sdl[j]);
+                                const float2 dj = *reinterpret_cast<const float2*>(&s_cf[j]);  // Delta here
                                 const float2 dec = make_float2(ex2_approx(cs_i - cj.x),
                                                                j + 1 <= row ? ex2_approx(cs_i - cj.y) : 0.f);
                                 const float2 gv = make_float2(__uint_as_float(gp[2 * e]), __uint_as_float(gp[2 * e + 1]));
