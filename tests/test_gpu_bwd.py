@@ -228,3 +228,20 @@ def test_bwd_with_forward_checkpoints(shape):
                                 pre["z"], pre["delta_bias"], pre["delta_softplus"], pre["initial_state"])
         assert_close(ck[:, :, c], rf, tol, f"checkpoint {c}")
     _compare(got, _oracle(x), tol, f"{b}x{d}x{L} with checkpoints")
+
+
+@pytest.mark.parametrize("shape", [(2, 64, 300, "f32"), (3, 40, 1000, "bf16"), (4, 5120, 256, "bf16"),
+                                   (1, 32, 40000, "bf16")],
+                         ids=lambda s: f"{s[0]}x{s[1]}x{s[2]}-{s[3]}")
+def test_forward_with_checkpoints_gives_the_same_outputs(shape):
+    """The checkpoint-storing forward only adds stores: y and the final state are the plain
+    forward's, bit for bit (one and two rows per lane, and time segments)."""
+    from selective_state_space_110_b300 import ssm_scan_fwd, ssm_scan_fwd_ckpt
+    b, d, L, dt = shape
+    x = _problem(b, d, L, dt, 900 + L)
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+            x["delta_softplus"])
+    y0, f0 = ssm_scan_fwd(*args, initial_state=x["initial_state"], out_dtype=torch.float32)
+    y1, f1, _ = ssm_scan_fwd_ckpt(*args, initial_state=x["initial_state"], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)
