@@ -39,9 +39,12 @@ ALU_ELEM_PER_CLK_PER_SM = 2.0  # 16 SFU exp2 (32/clk/SM) and 64 FP32 lane-ops (1
 BWD_ELEM_PER_CLK_PER_SM = 32.0 / 48.0  # backward: 48 SFU exp2 per element at 32/clk/SM
 BWD_CKPT_ELEM_PER_CLK_PER_SM = 32.0 / 32.0  # backward given the forward's checkpoints: 32 exp2
 L2_FLUSH_BYTES = 256 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum of one scan_kernel launch on this workload, from
-# one ncu capture of the same kernel code (summarised under profiles/): 252.8 MB + 50.3 MB.
-SCAN_TRAFFIC_BYTES = {"c2_mamba2p8b": 303_045_888}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the scan kernel on this workload,
+# from one ncu capture of the same kernel code (summarised under profiles/, the file named in
+# SCAN_TRAFFIC_SOURCE); re-taken whenever the kernel changes.
+SCAN_KERNEL_NAME = "scan_kernel (full pass)"
+SCAN_TRAFFIC_BYTES = {}
+SCAN_TRAFFIC_SOURCE = {}
 
 
 # ------------------------------------------------------------------------------------------
@@ -208,8 +211,63 @@ def time_scan(cfg, steps, warmup, x, flush, stream, soak_s=1.0):
             ev[s][1].record(stream)
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) for a, b in ev]
-    launches_per_step = 2 if ws_n else 1
-    return times, launches_per_step
+    return times, scan_launches(cfg)
+
+
+def scan_launches(cfg) -> int:
+    """Kernel launches of one ssm_scan_fwd of this workload: one for whole blocks, plus a
+    local-end pass when blocks are cut into segments, plus the segments' own launch when whole
+    and cut blocks are mixed (the balanced plan)."""
+    from selective_state_space_110_b300 import scan_plan
+    p = scan_plan(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen,
+                  in_dtype=torch.bfloat16 if cfg.in_dtype == "bf16" else torch.float32)
+    if p["split_blocks"] == 0 or p["segments"] == 1:
+        return 1
+    return 3 if p["whole_blocks"] > 0 else 2
+
+
+def time_segments(cfg) -> int:
+    """Time segments per cut block of the library's launch plan on this device (1 = none)."""
+    from selective_state_space_110_b300 import scan_plan
+    return scan_plan(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen)["segments"]
+
+
+def plan_summary(cfg) -> dict:
+    """The launch plan of the scan on this device, and the exps it runs per element: every cut
+    block's first segments-1 segments are scanned twice (the local-end pass, then the full pass
+    after the fold)."""
+    from selective_state_space_110_b300 import scan_plan
+    p = scan_plan(cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen,
+                  in_dtype=torch.bfloat16 if cfg.in_dtype == "bf16" else torch.float32)
+    blocks = p["whole_blocks"] + p["split_blocks"]
+    seg, L = p["segments"], max(cfg.seqlen, 1)
+    twice = p["split_blocks"] * min(L, (seg - 1) * p["segment_tokens"]) / (blocks * L) if seg > 1 else 0.0
+    return {"plan": {"whole_blocks": p["whole_blocks"], "split_blocks": p["split_blocks"],
+                     "time_segments": seg, "segment_tokens": p["segment_tokens"],
+                     "channels_per_block": p["channels_per_block"], "rows_per_lane": p["rows_per_lane"]},
+            "exp_passes": round(1 + twice, 3)}
+
+
+def other_scan_summary(name, args, flush, stream, sms, sm_mhz, hbm_peak):
+    """Another scan workload timed like the main one (L2 flushed, CUDA events per step):
+    median ms, elements/s, compulsory GB/s against the HBM and arithmetic ceilings, and the
+    time split the plan takes (each extra segment runs its exps a second time)."""
+    cfg = scan_config(name)
+    x = make_scan_inputs(cfg, "cuda")
+    steps = 3 if cfg.elements > (1 << 30) else max(3, min(args.steps, 10))
+    times, launches = time_scan(cfg, steps, 3, x, flush, stream, soak_s=0.2)
+    del x
+    ms = statistics.median(times)
+    alg = scan_algorithmic_bytes(cfg)
+    elem_s = cfg.elements / (ms * 1e-3)
+    alu_elem_s = ALU_ELEM_PER_CLK_PER_SM * sms * sm_mhz * 1e6
+    return {"shape": {"batch": cfg.batch, "dim": cfg.dim, "dstate": cfg.dstate, "seqlen": cfg.seqlen},
+            "steps": steps, "ms_per_step": round(ms, 4), "elem_per_s": round(elem_s, 1),
+            "achieved_gbs": round(alg / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(alg / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "alu_frac": round(elem_s / alu_elem_s, 4),
+            **plan_summary(cfg),
+            "launches_per_step": launches}
 
 
 def time_bwd(cfg, steps, warmup, x, flush, stream, checkpoints=False):
@@ -501,12 +559,18 @@ def run_ours(args):
                                  "hbm_frac": round(dbytes / (dms * 1e-3) / 1e9 / hbm_peak, 3),
                                  "launches_per_step": nl}
 
+    sm_mhz = clocks["sm_mhz"] or 1900.0
+    others = {}
+    for name in args.other_workloads:
+        o = other_scan_summary(name, args, flush, stream, sms, sm_mhz, hbm_peak)
+        o["ms_per_step"] = round(max_over_ranks(o["ms_per_step"], world), 4)
+        others[scan_config(name).name] = o
+
     if rank != 0:
         return
     alg = scan_algorithmic_bytes(cfg)
     kern_ms = statistics.mean(times)
     achieved = alg / (kern_ms * 1e-3) / 1e9
-    sm_mhz = clocks["sm_mhz"] or 1900.0
     alu_peak_elem = ALU_ELEM_PER_CLK_PER_SM * sms * sm_mhz * 1e6
     alu_peak_gbs = alu_peak_elem * alg / cfg.elements / 1e9
     line = {
@@ -531,11 +595,15 @@ def run_ours(args):
         "roofline": {"bound": "alu", "achieved": round(achieved, 1), "peak": round(alu_peak_gbs, 1),
                      "unit": "GB/s", "frac": round(achieved / alu_peak_gbs, 4),
                      "traffic": SCAN_TRAFFIC_BYTES.get(cfg.name),
-                     "kernel": "scan_kernel (full pass)",
+                     "traffic_source": SCAN_TRAFFIC_SOURCE.get(cfg.name),
+                     "kernel": SCAN_KERNEL_NAME,
                      "peak_note": f"ALU ceiling {ALU_ELEM_PER_CLK_PER_SM} elem/clk/SM x {sms} SMs x "
-                                  f"{sm_mhz:.0f} MHz, as GB/s of compulsory bytes",
+                                  f"{sm_mhz:.0f} MHz, as GB/s of compulsory bytes; the rates behind "
+                                  "it (ex2 32/clk/SM, fp32 FMA 128 lanes/clk/SM) are measured by "
+                                  "bench.py --pipe-rates, profiles/pipe_rates_b300.md",
                      "hbm_peak": hbm_peak, "hbm_peak_source": peak_src,
                      "hbm_frac": round(achieved / hbm_peak, 4)},
+        "plan": plan_summary(cfg),
         "e2e": {"value": round(elems / (e2e_ms * 1e-3), 1), "unit": "elem/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
@@ -562,6 +630,7 @@ def run_ours(args):
                          "alu_note": f"ceiling {BWD_CKPT_ELEM_PER_CLK_PER_SM:.3f} elem/clk/SM: 32 "
                                      "SFU exp2 per element (2 passes x 16 states)",
                          "launches_per_step": pair_launches}},
+        "other_workloads": others,
         "ssd": ssd_summary(ssd_cfg, ssd_ms, ssd_launches, world, kern_ms, cfg),
         "decode": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim, **dec},
         "decode_conv": {"layers": DECODE_CONFIG.layers, "dim": DECODE_CONFIG.dim,
@@ -651,6 +720,41 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_pipe_rates(args):
+    """Pipe rates of this GPU that the scan's arithmetic ceiling rests on (one CTA of 1,024
+    threads per SM, clock64 around a fixed loop; see csrc/pipe_probe.cu), one JSON line."""
+    import ctypes
+    from selective_state_space_110_b300 import build as b
+    lib = ctypes.CDLL(b.build_probe())
+    lib.selscan_probe_rate.restype = ctypes.c_double
+    lib.selscan_probe_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                       ctypes.c_void_p]
+    torch.cuda.set_device(0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(sms * 1024, dtype=torch.float32, device="cuda")
+    names = ["ex2_per_clk_per_sm", "ffma_lanes_per_clk_per_sm", "lg2_per_clk_per_sm",
+             "rcp_per_clk_per_sm", "ffma2_lanes_per_clk_per_sm", "shfl_per_clk_per_sm",
+             "lds32_words_per_clk_per_sm", "lds128_words_per_clk_per_sm"]
+    iters = {0: 4096, 1: 16384, 2: 4096, 3: 4096, 4: 16384, 5: 4096, 6: 4096, 7: 2048}
+    out = {"pipe_rates": torch.cuda.get_device_name(0), "sms": sms,
+           "method": "1 CTA x 1024 threads per SM, 16 independent chains (8 loads) per thread, "
+                     "clock64 around the loop; best of 3 runs"}
+    for which, name in enumerate(names):
+        best = 0.0
+        for _ in range(3):
+            r = lib.selscan_probe_rate(which, sms, iters[which], cycles.data_ptr(), sink.data_ptr())
+            if r < 0:
+                raise RuntimeError(f"probe {name} failed ({r})")
+            best = max(best, r)
+        out[name] = round(best, 2)
+    with ClockSampler(0) as clk:
+        for _ in range(20):
+            lib.selscan_probe_rate(0, sms, 16384, cycles.data_ptr(), sink.data_ptr())
+    out["clocks"] = clk.summary()
+    print(json.dumps(out), flush=True)
+
+
 def run_oracle_timings(args):
     """The fp64 oracle as it stands, on the host cores, over whole workloads (a baseline only):
     C0-C3 in full (rows in batches; only the oracle calls are timed) and decode at batch 64 on
@@ -724,7 +828,14 @@ def main():
     ap.add_argument("--ssd-workload", default="ssd1_mamba2_2p7b")
     ap.add_argument("--oracle-timings", action="store_true",
                     help="time the fp64 oracle on the host cores over C0-C3 and decode, and exit")
+    ap.add_argument("--pipe-rates", action="store_true",
+                    help="measure the SFU / FMA / shared-memory / shuffle rates and exit")
+    ap.add_argument("--other-workloads", nargs="*", default=["c1_mamba130m", "c3_long_1m"],
+                    help="scan workloads timed after the main one and reported beside it")
     args = ap.parse_args()
+    if args.pipe_rates:
+        run_pipe_rates(args)
+        return
     if args.oracle_timings:
         run_oracle_timings(args)
         return

@@ -19,8 +19,15 @@
  *
  * Conventions shared by every entry point:
  *   - Pointers are device memory (or memory the device can address) owned by the caller.
- *     The library allocates nothing, keeps no pointer after the call returns, and holds no
- *     global state; calls on different streams are independent.
+ *     The library allocates nothing on a call's path and keeps no pointer after the call
+ *     returns. Its only state, created once per device and kept until the process exits:
+ *       * one device-side error word per device, which any kernel of the library that gives
+ *         up a bounded wait sets, and which selscan_device_status reads and clears; it is
+ *         shared by every stream and every call on that device, so a timeout raised on one
+ *         stream is seen (and, with reset, cleared) by a reader on any other;
+ *       * the fixed scratch array of ssm_scan_fwd_no_alloc;
+ *       * the two copy streams and their events of ssm_scan_fwd_host.
+ *     Apart from these, calls on different streams with different buffers are independent.
  *   - All work is enqueued asynchronously on `stream` (NULL = the legacy default stream).
  *     The returned status covers argument checks and the launch itself. A non-OK status
  *     means nothing was launched and no output was written (SELSCAN_ERR_CUDA excepted:
@@ -88,11 +95,19 @@ typedef enum {
  * dstate must be 16. batch, dim >= 1; seqlen >= 0 (seqlen = 0 writes final_state only).
  * in_dtype applies to u, delta, z, B and C; out_dtype to out. Arithmetic is fp32.
  *
- * workspace / workspace_bytes: scratch device memory of at least
- * ssm_scan_workspace_size(batch, dim, dstate, seqlen) bytes (NULL/0 when that is 0). Long
- * sequences with few (batch, channel) rows are split into time segments that run in
- * parallel; the workspace holds each segment's local end state and its summed Delta. Its
- * contents on entry do not matter. Two calls running at the same time need two workspaces.
+ * workspace / workspace_bytes: scratch device memory of ssm_scan_workspace_size(batch, dim,
+ * dstate, seqlen) bytes (NULL/0 when that is 0). Some blocks of 32 channels are cut into time
+ * segments that run in parallel; the workspace holds each segment's local end state and its
+ * summed Delta. Two cases (ssm_scan_plan reports which one a shape takes):
+ *   - long sequences with few (batch, channel) rows are split for parallelism; the workspace
+ *     is then required (SELSCAN_ERR_WORKSPACE without it);
+ *   - shapes with more channel blocks than the GPU runs at once (bf16 inputs, seqlen % 8 == 0,
+ *     no zero-order hold) have their last, partial wave cut into segments so every SM gets
+ *     the same work; with a smaller workspace (or none) such a shape runs unsplit, correct but
+ *     with an unbalanced last wave.
+ * Its contents on entry do not matter. Two calls running at the same time need two
+ * workspaces. The plan (and so the workspace size) is made for the current device: pass a
+ * `stream` of that device.
  */
 selscan_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
                             const void* C, const float* D, const void* z,
@@ -122,11 +137,29 @@ selscan_status ssm_scan_fwd_ckpt(const void* u, const void* delta, const float* 
                                  selscan_stream_t stream);
 
 /*
- * Workspace bytes ssm_scan_fwd needs for this shape on the CURRENT device (the time split
- * depends on its SM count). 0 means no workspace is needed. Returns 0 for invalid shapes
- * (ssm_scan_fwd then reports the error).
+ * Workspace bytes ssm_scan_fwd uses for this shape on the CURRENT device (the time split
+ * depends on its SM count), including a split that only balances the GPU (taken by bf16 inputs
+ * with seqlen % 8 == 0 and no zero-order hold; other inputs use less of it). 0 means no
+ * workspace is used. Returns 0 for invalid shapes (ssm_scan_fwd then reports the error).
  */
 size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
+
+/*
+ * ssm_scan_plan: how ssm_scan_fwd will launch this shape on the current device for inputs of
+ * `in_dtype`, flag bits `flags` (as delta_softplus) and `workspace_bytes` of workspace. The
+ * paper has no counterpart; it describes the launch for callers that size buffers or report
+ * performance. info[0..7] (int64, host memory):
+ *   [0] rows per lane (1 or 2)        [1] blocks of channels run whole
+ *   [2] blocks cut into time segments [3] segments per cut block (1 = none)
+ *   [4] tokens per segment            [5] channels per block (CTA)
+ *   [6] workspace bytes this plan uses [7] workspace bytes the shape requires (the rest only
+ *       balances the GPU)
+ * Returns SELSCAN_ERR_INVALID_ARG for a NULL info, bad sizes or unknown flags,
+ * SELSCAN_ERR_UNSUPPORTED for dstate != 16, an unknown dtype or a device that is not sm_103.
+ */
+selscan_status ssm_scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                             selscan_dtype in_dtype, int flags, size_t workspace_bytes,
+                             int64_t* info);
 
 /*
  * ssm_state_update: one generated token ("Taken Apart": the head reads one token, computes
@@ -185,9 +218,16 @@ selscan_status ssm_conv_state_update(void* conv_state, const void* x, const floa
  * device memory of every GPU that loads it, held until the process exits. The call allocates
  * nothing and calls no allocating routine.
  *
- *   - Shapes whose ssm_scan_workspace_size() exceeds SELSCAN_NO_ALLOC_SCRATCH_BYTES are
- *     rejected with SELSCAN_ERR_SCRATCH_LIMIT before anything is launched; use ssm_scan_fwd
- *     with a workspace for them.
+ *   - Shapes whose required workspace (ssm_scan_plan info[7]) exceeds
+ *     SELSCAN_NO_ALLOC_SCRATCH_BYTES are rejected with SELSCAN_ERR_SCRATCH_LIMIT before
+ *     anything is launched; use ssm_scan_fwd with a workspace for them. A shape whose time
+ *     split only balances the GPU uses it when it fits the array and runs unsplit otherwise.
+ *     This size check comes before every other argument check: a shape beyond the array gets
+ *     SELSCAN_ERR_SCRATCH_LIMIT even if a pointer is also NULL, misaligned or overlapping (no
+ *     pointer is dereferenced or checked at that point).
+ *   - `stream` must belong to the current device (cudaSetDevice): the array's address is the
+ *     current device's, and a stream of another device is refused with
+ *     SELSCAN_ERR_INVALID_ARG.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *     once per device, with that device current). Make that first call before any stream
  *     capture on that device.
@@ -319,7 +359,10 @@ selscan_status ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A,
  * the library, leaves its outputs incomplete and exits normally, so the GPU and the context
  * stay usable. This call synchronises `stream`, then returns SELSCAN_ERR_DEVICE_TIMEOUT if the
  * flag is set on the current device (SELSCAN_OK otherwise); with `reset` nonzero it also clears
- * the flag. The flag is per device and shared by all streams.
+ * the flag. The flag is one word per device, shared by every stream and call of the library on
+ * that device: a timeout raised by a launch on one stream is reported by a query on any stream,
+ * and a reset from any stream clears it for all. Callers that need to know which call timed out
+ * query right after that call, with no other call of the library in flight on the device.
  */
 selscan_status selscan_device_status(int reset, selscan_stream_t stream);
 

@@ -14,6 +14,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libselscan.so")
+# Pipe-rate microbenchmarks for the measurement (bench.py --pipe-rates); not part of the C ABI.
+PROBE_SRC = "pipe_probe.cu"
+PROBE_LIB = os.path.join(PKG, "libselscan_probe.so")
 SOURCES = ["selscan_api.cu", "scan_fwd.cu", "state_update.cu", "scan_fwd_no_alloc.cu",
            "scan_bwd.cu", "ssd_fwd.cu", "scan_host.cu"]
 HEADERS = ["selscan_device.cuh", "selscan_launch.h", "sm100_async.cuh"]
@@ -34,6 +37,18 @@ def _stale() -> bool:
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     deps.append(os.path.join(ROOT, "include", "selscan.h"))
     return any(os.path.getmtime(p) > t for p in deps)
+
+
+def build_probe(force: bool = False) -> str:
+    src = os.path.join(CSRC, PROBE_SRC)
+    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= os.path.getmtime(src):
+        return PROBE_LIB
+    cmd = [_nvcc(), *ARCH, *FLAGS, "-shared", src, "-o", PROBE_LIB + ".tmp"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {PROBE_SRC}:\n{r.stdout}\n{r.stderr}")
+    os.replace(PROBE_LIB + ".tmp", PROBE_LIB)
+    return PROBE_LIB
 
 
 def build(force: bool = False, ptxas_verbose: bool = False, verbose: bool = False) -> str:
@@ -68,3 +83,4 @@ def build(force: bool = False, ptxas_verbose: bool = False, verbose: bool = Fals
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, ptxas_verbose="--ptxas-v" in sys.argv, verbose=True))
+    print(build_probe(force="--force" in sys.argv))

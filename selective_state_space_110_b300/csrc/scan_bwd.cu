@@ -55,6 +55,22 @@ struct BwdSmem {
 template <typename Tin>
 __device__ __forceinline__ float ld1(const Tin* p) { return to_f32(*p); }
 
+// v * exp(s*a) for s*a <= 0 in fp32 with a small relative error at every decay strength. The
+// product x = s*a is rounded; its rounding error lo = fma(s, a, -x) is carried to first order
+// (exp(x + lo) = exp(x) (1 + lo)), since at |x| ~ 30 the rounding alone would be 2e-6 of the
+// decay. A weak decay is formed as v + expm1(x) v (its distance from 1 exact to rounding), a
+// strong one (x < -ln 2) as expf(x) v.
+__device__ __forceinline__ float precise_decay(float s, float a, float v) {
+    const float x = s * a;
+    const float lo = fmaf(s, a, -x);
+    if (x < -0.69314718f) {
+        const float ev = expf(x) * v;
+        return fmaf(ev, lo, ev);
+    }
+    const float m = expm1f(x);
+    return fmaf(fmaf(lo, m + 1.f, m), v, v);
+}
+
 template <bool kPrecise>
 __device__ __forceinline__ float sigmoid_f(float x) {
     return kPrecise ? 1.f / (1.f + expf(-x)) : rcp_approx(1.f + ex2_approx(-x * kLog2e));
@@ -222,11 +238,14 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
     auto put_bc = [&](int buf, bool withC) {
         if (withC || s_ch < 4) Stage::put(&sm.bc[buf][0][0], s_tt, s_ch, sb);
     };
-    // v * exp(Delta A_n) + add (s = Delta * kScale). fp32 inputs write exp as 1 + expm1: the decay's distance from 1
-    // keeps full relative precision, so a slowly decaying state or adjoint accumulates no bias
-    // from rounding the decay itself over thousands of tokens.
+    // v * exp(Delta A_n) + add (s = Delta * kScale). fp32 inputs write a weak decay as 1 + expm1:
+    // the decay's distance from 1 keeps full relative precision, so a slowly decaying state or
+    // adjoint accumulates no bias from rounding the decay itself over thousands of tokens. A
+    // strong decay (exponent below -ln 2) is taken from expf instead: there 1 + expm1 would
+    // carry expm1's absolute rounding (~6e-8) as a relative error of 6e-8 / exp(x) in the
+    // decayed value, which the gradient of the initial state (a product of decays) shows.
     auto decay_fma = [&](float s, int n, float v, float add) -> float {
-        if (kPrecise) return fmaf(expm1f(s * Av[n]), v, v) + add;
+        if (kPrecise) return precise_decay(s, Av[n], v) + add;
         return fmaf(ex2_approx(s * Av[n]), v, add);
     };
     // The SFU path of four states at once as two packed pairs (the same roundings as decay_fma):
@@ -247,7 +266,7 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
 
     // exp(A_n * S) for a summed Delta S (fold of a segment).
     auto seg_decay_fma = [&](float S, int n, float v, float add) -> float {
-        if (kPrecise) return fmaf(expm1f(S * Av[n]), v, v) + add;
+        if (kPrecise) return precise_decay(S, Av[n], v) + add;
         return fmaf(ex2_approx(S * kLog2e * Av[n]), v, add);
     };
     // Kahan sum of Delta over this lane's owned tokens (local passes).
@@ -494,9 +513,8 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
                     v[4 + n] = ds * hts[n];   // dC term
                     v[n] = gad[n] * k;        // dB term
                     dk = fmaf(gad[n], Bs[n], dk);
-                    // Abar as 1 + expm1 (see decay_fma), and the adjoint times Abar
-                    const float m = expm1f(s * Av[n]);
-                    const float gab = fmaf(m, gad[n], gad[n]);
+                    // the adjoint times Abar (weak decays as 1 + expm1, see decay_fma)
+                    const float gab = precise_decay(s, Av[n], gad[n]);
                     const float w = gab * hps[n];  // dAbar * Abar
                     da = fmaf(w, Av[n], da);
                     dA_chunk[n] = fmaf(w, s, dA_chunk[n]);

@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "selscan_device.cuh"
@@ -48,21 +49,26 @@
 
 namespace selscan {
 
-constexpr int kRowsPerCta = 32;
+constexpr int kRowsPerCta = 32;      // channels per CTA of the default geometry
 constexpr int kMaxChunk = 32;  // time segments are multiples of this many tokens
 
-// Geometry for kR rows per quad (and per lane). kR = 2 halves the B/C shared-memory traffic
-// per element but also the number of warps; the launcher picks it per shape.
-template <int kR>
+// Geometry for kR rows per quad (and per lane) and kW warps per CTA. kR = 2 halves the B/C
+// shared-memory traffic per element but also the number of warps; the launcher picks it per
+// shape. The default CTA holds 32 channels; the wide CTA (8 warps, 128 channels of two rows
+// per quad) is for the balanced launch, where its registers alone keep it to one CTA per SM.
+constexpr int kWideWarps = 8;
+template <int kR, int kW = 4 / kR>
 struct Geo {
     static_assert(kR == 1 || kR == 2, "rows per lane must be 1 or 2");
-    static constexpr int kWarps = 4 / kR;
+    static constexpr int kWarps = kW;
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int kRowsPerWarp = 8 * kR;
+    static constexpr int kRowsPerCta = kRowsPerWarp * kWarps;
     static constexpr int kChunk = 32 / kR;      // tokens per chunk: each lane owns 8 of one row
     static constexpr int kBlocks = kChunk / 4;  // 4-token blocks per chunk
-    static constexpr int kMinCtas = kR == 1 ? 5 : 6;  // register budget per thread
+    static constexpr int kMinCtas = kW != 4 / kR ? 1 : kR == 1 ? 5 : 6;  // register budget
 };
+
 
 // Error bits a kernel can raise; read (and cleared) by read_device_status().
 __device__ unsigned int g_device_status;
@@ -75,7 +81,7 @@ struct ScanStages {
     static constexpr int kTileBytes = 16 * Geo<kR>::kChunk * kInBytes;
 };
 
-template <int kInBytes, int kR>
+template <int kInBytes, int kR, int kW>
 struct __align__(128) ScanSmem {
     using St = ScanStages<kInBytes, kR>;
     static constexpr int kChunk = Geo<kR>::kChunk;
@@ -85,7 +91,7 @@ struct __align__(128) ScanSmem {
     // token t sits at position c ^ (t & 7).
     float bc[2][kChunk][32];
     // Partial readouts: [warp][row of the quad][4-token block][slot] with slot = lane ^ swz.
-    float4 red[Geo<kR>::kWarps][kR][Geo<kR>::kBlocks][32];
+    float4 red[kW][kR][Geo<kR>::kBlocks][32];
     unsigned long long full[St::kStages];
 };
 
@@ -137,6 +143,16 @@ __device__ __forceinline__ float phi_fast(float x2, float abar, float inv_a, flo
     return fabsf(x) < 0.0625f ? p : (abar - 1.f) * inv_a * dinv;
 }
 
+// Compensated (Kahan) accumulation of an increment into a pair of state numbers: nc holds the
+// negated rounding error not yet added. t = h + (inc + nc) is rounded; (h - t) + y recovers
+// what the rounding dropped (exactly, since t and h are close).
+__device__ __forceinline__ void kahan_step(float2& h, float2& nc, float2 inc) {
+    const float2 y = __fadd2_rn(inc, nc);
+    const float2 t = __fadd2_rn(h, y);
+    nc = __fadd2_rn(__fadd2_rn(h, make_float2(-t.x, -t.y)), y);
+    h = t;
+}
+
 // Owner lane (within the quad) of row j, token t of a chunk, and its register slot t & 7.
 template <int kR>
 __device__ __forceinline__ constexpr int owner_of(int j, int t) {
@@ -150,32 +166,46 @@ __device__ __forceinline__ constexpr int red_swz(int j, int q) {
 }
 
 template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, bool kZoh, Mode kMode,
-          bool kCkpt = false>
-__global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
+          bool kCkpt = false, int kW = 4 / kR>
+__global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
     scan_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC) {
     constexpr bool kFull = kMode == Mode::kFull;
-    constexpr int kThreads = Geo<kR>::kThreads;
-    constexpr int kRowsPerWarp = Geo<kR>::kRowsPerWarp;
-    constexpr int kChunk = Geo<kR>::kChunk;
-    constexpr int kBlocks = Geo<kR>::kBlocks;
+    using Gm = Geo<kR, kW>;
+    constexpr int kThreads = Gm::kThreads;
+    constexpr int kRowsPerWarp = Gm::kRowsPerWarp;
+    constexpr int kRowsPerCta = Gm::kRowsPerCta;
+    constexpr int kChunk = Gm::kChunk;
+    constexpr int kBlocks = Gm::kBlocks;
     using St = ScanStages<sizeof(Tin), kR>;
     constexpr int kS = St::kStages;
-    __shared__ ScanSmem<sizeof(Tin), kR> sm;
+    __shared__ ScanSmem<sizeof(Tin), kR, kW> sm;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int quad = lane >> 2;
     const int g = lane & 3;  // quarter of the state owned by this lane
-    const int64_t b = blockIdx.z;
+    // This CTA's block of 32 channels and time segment (grid: channel blocks x segments x
+    // batches, offset by bx0 / b0 when only some blocks are cut into segments).
+    // (Only the wide CTA of the balanced plan is offset or skips blocks; the default geometry
+    // always starts at block 0.)
+    constexpr bool kOffset = kW == kWideWarps;
+    const int64_t b = kOffset ? a.b0 + blockIdx.z : (int64_t)blockIdx.z;
     const int seg = blockIdx.y;
+    const int64_t bx = kOffset ? a.bx0 + blockIdx.x : (int64_t)blockIdx.x;
+    // The whole-block launch of the balanced plan leaves the blocks its segments cover.
+    if (kOffset && a.skip_bx0 >= 0 && b == a.skip_b && bx >= a.skip_bx0) return;
     const int64_t dim = a.dim;
-    const int64_t d0 = (int64_t)blockIdx.x * kRowsPerCta + warp * kRowsPerWarp + quad * kR;
+    const int64_t d0 = bx * kRowsPerCta + warp * kRowsPerWarp + quad * kR;
     const int64_t L = a.seqlen;
     const int64_t t_begin = (int64_t)seg * a.seg_len;
     const int64_t t_end = min(L, t_begin + a.seg_len);
     const int nchunks = t_end > t_begin ? (int)((t_end - t_begin + kChunk - 1) / kChunk) : 0;
     const int nprev = a.nseg - 1;  // segments with a stored local end state
+    // First workspace row of this quad: rows of the cut blocks, in the launch's block order.
+    auto ws_row0 = [&]() -> int64_t {
+        return ((int64_t)blockIdx.z * gridDim.x + blockIdx.x) * kRowsPerCta + warp * kRowsPerWarp + quad * kR;
+    };
 
     // Rows of this quad; inactive rows (past dim) compute on row 0's parameters and store nothing.
     bool act[kR];
@@ -229,18 +259,27 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
 
     // ---- initial state, then fold the local end states of earlier segments ----
     float2 h01[kR], h23[kR];
+    // fp32 inputs: Kahan compensation of each state number (the negated rounding error still
+    // to be added). A decay exp(Delta*A) within a few ulp of 1 changes the state by less than
+    // half an ulp per token, which plain fp32 rounding drops at every token, the same way
+    // each time (up to L/2 ulp of bias over L tokens; at Delta ~ 1e-8 that is 1.4e-5 relative
+    // after 384 tokens). The compensated sum keeps those increments.
+    float2 nc01[kR], nc23[kR];
 #pragma unroll
     for (int j = 0; j < kR; ++j) {
         h01[j] = make_float2(0.f, 0.f);
         h23[j] = make_float2(0.f, 0.f);
+        nc01[j] = make_float2(0.f, 0.f);
+        nc23[j] = make_float2(0.f, 0.f);
         if (!kFull) continue;
         if (a.initial_state) {
             const float4 s = *reinterpret_cast<const float4*>(a.initial_state + row[j] * kN + 4 * g);
             h01[j] = make_float2(s.x, s.y); h23[j] = make_float2(s.z, s.w);
         }
         for (int i = 0; i < seg; ++i) {
-            const float ds = a.ws_dsum[row[j] * nprev + i];
-            const float4 hl = *reinterpret_cast<const float4*>(a.ws_hloc + (row[j] * nprev + i) * kN + 4 * g);
+            const int64_t sr = ws_row0() + j;
+            const float ds = a.ws_dsum[sr * nprev + i];
+            const float4 hl = *reinterpret_cast<const float4*>(a.ws_hloc + (sr * nprev + i) * kN + 4 * g);
             if (kPrecise) {  // exp(A*S) h + h_local, with exp written as 1 + expm1
                 const float m0 = expm1f(A4[j].x * ds), m1 = expm1f(A4[j].y * ds);
                 const float m2 = expm1f(A4[j].z * ds), m3 = expm1f(A4[j].w * ds);
@@ -350,9 +389,11 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
 
         // ---- B and C of this chunk -> fp32 per-token rows (item = chunk-column x token) ----
         if (kVec && !mbar_wait_bounded(&sm.full[stage], parity)) timed_out = true;
+        constexpr int kItems = kChunk * (kFull ? 8 : 4);  // (token, 4-state chunk) pairs
 #pragma unroll
-        for (int cc = 0; cc < (kFull ? 2 : 1); ++cc) {
+        for (int cc = 0; cc < (kItems + kThreads - 1) / kThreads; ++cc) {
             const int item = tid + kThreads * cc;
+            if (kItems < kThreads && item >= kItems) break;
             const int tt = item % kChunk;
             const int ch = item / kChunk;  // 0..7: B quads 0-3, C quads 0-3
             const int isC = ch >> 2, q = ch & 3;
@@ -452,8 +493,9 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
                             kb01 = __fmul2_rn(kb01, make_float2(phi_exact(m01.x, arg[0]), phi_exact(m01.y, arg[1])));
                             kb23 = __fmul2_rn(kb23, make_float2(phi_exact(m23.x, arg[2]), phi_exact(m23.y, arg[3])));
                         }
-                        h01[j] = __fadd2_rn(__ffma2_rn(m01, h01[j], h01[j]), kb01);
-                        h23[j] = __fadd2_rn(__ffma2_rn(m23, h23[j], h23[j]), kb23);
+                        // h <- h + (m h + kb), summed with compensation.
+                        kahan_step(h01[j], nc01[j], __ffma2_rn(m01, h01[j], kb01));
+                        kahan_step(h23[j], nc23[j], __ffma2_rn(m23, h23[j], kb23));
                     } else {
                         const float2 ab01 = make_float2(ex2_approx(arg[0]), ex2_approx(arg[1]));
                         const float2 ab23 = make_float2(ex2_approx(arg[2]), ex2_approx(arg[3]));
@@ -515,6 +557,13 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
         }
     }
 
+    if (kPrecise) {  // fold in what the compensation still holds
+#pragma unroll
+        for (int j = 0; j < kR; ++j) {
+            h01[j] = __fadd2_rn(h01[j], nc01[j]);
+            h23[j] = __fadd2_rn(h23[j], nc23[j]);
+        }
+    }
     if (kFull) {
         if (a.final_state && seg == a.nseg - 1) {
 #pragma unroll
@@ -532,9 +581,9 @@ __global__ void __launch_bounds__(Geo<kR>::kThreads, Geo<kR>::kMinCtas)
 #pragma unroll
         for (int j = 0; j < kR; ++j)
             if (act[j])
-                *reinterpret_cast<float4*>(a.ws_hloc + (row[j] * nprev + seg) * kN + 4 * g) =
+                *reinterpret_cast<float4*>(a.ws_hloc + ((ws_row0() + j) * nprev + seg) * kN + 4 * g) =
                     make_float4(h01[j].x, h01[j].y, h23[j].x, h23[j].y);
-        if (own_act && (kR == 1 ? g == 0 : (g & 1) == 0)) a.ws_dsum[own_row * nprev + seg] = s;
+        if (own_act && (kR == 1 ? g == 0 : (g & 1) == 0)) a.ws_dsum[(ws_row0() + jo) * nprev + seg] = s;
     }
 }
 
@@ -575,37 +624,62 @@ cudaError_t make_bc_map(CUtensorMap* m, const void* base, int64_t batch, int64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, bool kZoh = false>
-cudaError_t launch_typed(const ScanArgs& a, int64_t batch, cudaStream_t stream) {
-    using G = Geo<kR>;
+// The launches of one scan with kW warps per CTA (see ScanArgs for the three plans).
+template <int kR, typename Tin, typename Tout, bool kVec, bool kPrecise, bool kZoh = false,
+          int kW = 4 / kR>
+cudaError_t launch_typed(const ScanArgs& args, int64_t batch, cudaStream_t stream) {
+    using G = Geo<kR, kW>;
     CUtensorMap mB{}, mC{};
-    if (kVec && a.seqlen > 0) {
+    if (kVec && args.seqlen > 0) {
         const bool bf = sizeof(Tin) == 2;
-        cudaError_t e = make_bc_map(&mB, a.B, batch, a.seqlen, bf, G::kChunk);
-        if (e == cudaSuccess) e = make_bc_map(&mC, a.C, batch, a.seqlen, bf, G::kChunk);
+        cudaError_t e = make_bc_map(&mB, args.B, batch, args.seqlen, bf, G::kChunk);
+        if (e == cudaSuccess) e = make_bc_map(&mC, args.C, batch, args.seqlen, bf, G::kChunk);
         if (e != cudaSuccess) return e;
     }
-    const unsigned gx = (unsigned)((a.dim + kRowsPerCta - 1) / kRowsPerCta);
-    if (a.nseg > 1) {
-        dim3 grid(gx, (unsigned)(a.nseg - 1), (unsigned)batch);
-        scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kLocalEnd><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    dim3 grid(gx, (unsigned)a.nseg, (unsigned)batch);
-    if constexpr (!kZoh) {
-        if (a.ckpt) {  // also keep the state before every 16th token
-            scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kFull, true>
-                <<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
-            return cudaGetLastError();
+    const unsigned gx = (unsigned)((args.dim + G::kRowsPerCta - 1) / G::kRowsPerCta);
+    auto full_kernel = [&]() {
+        if constexpr (!kZoh) {
+            if (args.ckpt) return scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kFull, true, kW>;
         }
+        return scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kFull, false, kW>;
+    };
+    constexpr auto local_kernel = scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kLocalEnd, false, kW>;
+    auto launch = [&](auto kernel, dim3 grid, const ScanArgs& a) -> cudaError_t {
+        if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+        kernel<<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
+        return cudaGetLastError();
+    };
+    cudaError_t e = cudaSuccess;
+    if (args.nsplit == 0) {  // whole blocks only
+        ScanArgs a = args;
+        a.nseg = 1; a.seg_len = std::max<int64_t>(a.seqlen, 1); a.bx0 = 0; a.b0 = 0; a.skip_bx0 = -1;
+        return launch(full_kernel(), dim3(gx, 1, (unsigned)batch), a);
     }
-    scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kFull><<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
-    return cudaGetLastError();
+    if (args.nfull == 0) {  // every block cut into segments
+        ScanArgs a = args;
+        a.bx0 = 0; a.b0 = 0; a.skip_bx0 = -1;
+        if (a.nseg > 1) e = launch(local_kernel, dim3(gx, (unsigned)(a.nseg - 1), (unsigned)batch), a);
+        if (e == cudaSuccess) e = launch(full_kernel(), dim3(gx, (unsigned)a.nseg, (unsigned)batch), a);
+        return e;
+    }
+    // Balanced: the cut blocks are the last nsplit blocks of the last batch. Local-end pass of
+    // their first nseg-1 segments, the whole blocks (one CTA per SM), then their segments.
+    const int64_t bx_cut = (int64_t)gx - args.nsplit;
+    ScanArgs cut = args;
+    cut.bx0 = bx_cut; cut.b0 = batch - 1; cut.skip_bx0 = -1;
+    e = launch(local_kernel, dim3((unsigned)args.nsplit, (unsigned)(args.nseg - 1), 1), cut);
+    if (e != cudaSuccess) return e;
+    ScanArgs whole = args;
+    whole.nseg = 1; whole.seg_len = std::max<int64_t>(whole.seqlen, 1); whole.bx0 = 0; whole.b0 = 0;
+    whole.skip_bx0 = bx_cut; whole.skip_b = batch - 1;
+    e = launch(full_kernel(), dim3(gx, 1, (unsigned)batch), whole);
+    if (e != cudaSuccess) return e;
+    return launch(full_kernel(), dim3((unsigned)args.nsplit, (unsigned)args.nseg, 1), cut);
 }
 
 // Two rows per lane only for the fast bf16 vector path (the shapes where it pays off); every
-// other input combination runs one row per lane.
+// other input combination runs one row per lane. The balanced plan runs the wide CTA, which
+// only the fast bf16 path has.
 template <typename Tin, typename Tout>
 cudaError_t launch_io(const ScanArgs& a, int64_t batch, bool vec, bool precise,
                       cudaStream_t stream) {
@@ -618,6 +692,8 @@ cudaError_t launch_io(const ScanArgs& a, int64_t batch, bool vec, bool precise,
                        : launch_typed<1, Tin, Tout, false, false, true>(a, batch, stream);
     }
     if constexpr (sizeof(Tin) == 2) {
+        if (vec && !precise && a.wide)
+            return launch_typed<2, Tin, Tout, true, false, false, kWideWarps>(a, batch, stream);
         if (vec && !precise && a.rows_per_lane == 2)
             return launch_typed<2, Tin, Tout, true, false>(a, batch, stream);
     }
@@ -679,5 +755,6 @@ int scan_rows_per_cta() { return kRowsPerCta; }
 int scan_ctas_per_sm(int rows_per_lane) {
     return rows_per_lane == 2 ? Geo<2>::kMinCtas : Geo<1>::kMinCtas;
 }
+int scan_wide_rows_per_cta() { return Geo<2, kWideWarps>::kRowsPerCta; }
 
 }  // namespace selscan

@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "../../include/selscan.h"
+#include "selscan_launch.h"
 
 #define SELSCAN_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -57,12 +58,25 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd_no_alloc(
     float* final_state, int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
     selscan_dtype in_dtype, selscan_dtype out_dtype, const float* initial_state,
     selscan_stream_t stream) {
-    // The scratch this shape needs on the current device; 0 also for invalid shapes, which
-    // ssm_scan_fwd then reports with its own status.
-    const size_t need = ssm_scan_workspace_size(batch, dim, dstate, seqlen);
-    if (need > kNoAllocScratchBytes) return SELSCAN_ERR_SCRATCH_LIMIT;
+    // The scratch this shape cannot do without on the current device; 0 also for invalid
+    // shapes, which ssm_scan_fwd then reports with its own status. A shape whose time split
+    // only balances the GPU takes it when it fits the array and runs unsplit otherwise.
+    if (dstate == 16 && selscan::scan_required_workspace(batch, dim, seqlen) > kNoAllocScratchBytes)
+        return SELSCAN_ERR_SCRATCH_LIMIT;
+    const size_t want = ssm_scan_workspace_size(batch, dim, dstate, seqlen);
     void* scratch = nullptr;
-    if (need > 0) {
+    if (want > 0) {
+        // The array's address is the current device's: a stream of another device would run
+        // the kernels there with a pointer into this device's memory.
+        if (stream) {
+            int cur = 0, sdev = 0;
+            if (cudaGetDevice(&cur) != cudaSuccess ||
+                cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+                cudaGetLastError();
+                return SELSCAN_ERR_CUDA;
+            }
+            if (sdev != cur) return SELSCAN_ERR_INVALID_ARG;
+        }
         const selscan_status s = scratch_address(&scratch);
         if (s != SELSCAN_OK) return s;
     }
@@ -70,6 +84,6 @@ SELSCAN_EXPORT selscan_status ssm_scan_fwd_no_alloc(
     // entry that the second kernel reads.
     return ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, out, final_state,
                         batch, dim, dstate, seqlen, in_dtype, out_dtype, initial_state,
-                        need > 0 ? scratch : nullptr, need > 0 ? kNoAllocScratchBytes : 0,
+                        want > 0 ? scratch : nullptr, want > 0 ? kNoAllocScratchBytes : 0,
                         stream);
 }

@@ -12,7 +12,8 @@
 namespace {
 
 constexpr int64_t kStateN = 16;
-constexpr int64_t kMinSegTokens = 4096;  // shortest time segment worth a split
+constexpr int64_t kMinSegTokens = 4096;  // shortest time segment worth a split for parallelism
+constexpr int64_t kMinBalanceSegTokens = 64;  // shortest segment of the balanced plan's tail
 constexpr int64_t kTwoRowsMinRows = 16384;  // rows from which two rows per lane pay off
 constexpr int kKnownFlags = SELSCAN_FLAG_SOFTPLUS | SELSCAN_FLAG_ZOH;
 constexpr int64_t kConvTaps = 4;  // width of the block's short convolution
@@ -50,39 +51,135 @@ selscan_status device_sms(int* sms) {
 }
 
 struct Plan {
-    int nseg;
+    int rows_per_lane;
+    int64_t gx;        // blocks of 32 channels per batch
+    int64_t nfull;     // blocks run whole
+    int64_t nsplit;    // blocks cut into time segments
+    int nseg;          // segments per split block
     int64_t seg_len;
+    bool wide;         // balanced plan: wide CTAs (128 channels), one per SM
+    bool optional;     // the split only balances the GPU: without workspace, run unsplit
     size_t hloc_bytes, dsum_bytes, ws_bytes;
 };
 
-// Time segmentation: split the sequence only when the (b, d) rows alone fill less than half of
-// the CTA slots of the GPU (scan_ctas_per_sm per SM). Each extra segment costs a second pass
-// over it (the local-end pass), so rows are always preferred to segments; the number of
-// segments is the largest that still fits every CTA of the full pass into one wave.
-Plan make_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
+// Cost of a launch in units of one whole block's time at two warps per scheduler, with the
+// measured per-scheduler throughput of the scan kernel at 1, 2 and 3+ resident warps (B300:
+// 0.116, 0.154, 0.166 elements per clock): a scheduler with w warps of total work W blocks
+// takes W * 0.154 / rate(w) units, since the warps share its issue slots.
+double sched_time(double blocks_of_work, int warps) {
+    const double rate = warps <= 1 ? 0.116 : warps == 2 ? 0.154 : 0.166;
+    return blocks_of_work * 0.154 / rate;
+}
+
+void set_workspace(Plan& p, int64_t rows_split) {
+    p.hloc_bytes = p.dsum_bytes = 0;
+    if (p.nsplit > 0 && p.nseg > 1) {
+        p.hloc_bytes = round_up((size_t)rows_split * (size_t)(p.nseg - 1) * kStateN * sizeof(float), kWsAlign);
+        p.dsum_bytes = round_up((size_t)rows_split * (size_t)(p.nseg - 1) * sizeof(float), kWsAlign);
+    }
+    p.ws_bytes = p.hloc_bytes + p.dsum_bytes;
+}
+
+// The launch of one scan, in blocks of 32 consecutive channels of one batch (one CTA each).
+//  - Few blocks for the GPU (they fill at most half of its CTA slots): every block is cut into
+//    time segments, as many as fit every segment of the full pass into one wave. Each extra
+//    segment costs a second pass over it (the local-end pass), so segments are used only when
+//    the rows alone leave the GPU idle. The workspace is required.
+//  - More blocks than two warps per scheduler hold (slots): a wave of whole blocks leaves the
+//    remainder r = blocks mod slots for a last, partial wave in which most schedulers idle.
+//    The balanced plan uses the wide CTA (128 channels, 8 warps), which its registers keep to
+//    one per SM: q = blocks / SMs whole blocks per SM, and the r remainder blocks (the last r
+//    blocks of the last batch) cut into as many time segments as there are SMs per remainder
+//    block, so every SM gets the same work up to one segment. The segments run in a launch of
+//    their own after the whole blocks.
+//    It is taken when the cost model says it is faster than letting the hardware stack the
+//    blocks unevenly, and only with a workspace (else the unsplit launch runs).
+Plan make_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms, bool fast) {
     const int64_t chunk = selscan::scan_chunk_tokens();
     const int64_t rows = batch * dim;
-    const int64_t ctas = batch * ((dim + selscan::scan_rows_per_cta() - 1) / selscan::scan_rows_per_cta());
-    const int64_t slots = (int64_t)sms * selscan::scan_ctas_per_sm(2);
-    int64_t n = 1;
-    if (2 * ctas <= slots) {
-        n = slots / ctas;
+    const int64_t rpc = selscan::scan_rows_per_cta();
+    Plan p{};
+    p.gx = (dim + rpc - 1) / rpc;
+    const int64_t blocks = batch * p.gx;
+    p.nfull = blocks;
+    p.nsplit = 0;
+    p.nseg = 1;
+    p.seg_len = std::max<int64_t>(seqlen, 1);
+    p.rows_per_lane = rows >= kTwoRowsMinRows ? 2 : 1;
+
+    // Few rows: time segments on every block.
+    const int64_t slots6 = (int64_t)sms * selscan::scan_ctas_per_sm(2);
+    if (2 * blocks <= slots6) {
+        int64_t n = slots6 / blocks;
         n = std::min<int64_t>(n, seqlen / kMinSegTokens);
         n = std::max<int64_t>(n, 1);
         n = std::min<int64_t>(n, 65535);
+        int64_t seg_len = (std::max<int64_t>(seqlen, 1) + n - 1) / n;
+        seg_len = (seg_len + chunk - 1) / chunk * chunk;
+        n = std::max<int64_t>(1, (seqlen + seg_len - 1) / seg_len);
+        if (n > 1) {
+            p.rows_per_lane = 2;
+            p.nfull = 0;
+            p.nsplit = blocks;
+            p.nseg = (int)n;
+            p.seg_len = seg_len;
+        }
+        set_workspace(p, p.nsplit * rpc);
+        return p;
     }
-    int64_t seg_len = (std::max<int64_t>(seqlen, 1) + n - 1) / n;
-    seg_len = (seg_len + chunk - 1) / chunk * chunk;
-    n = std::max<int64_t>(1, (seqlen + seg_len - 1) / seg_len);
-    Plan p{};
-    p.nseg = (int)n;
-    p.seg_len = seg_len;
-    if (n > 1) {
-        p.hloc_bytes = round_up((size_t)rows * (size_t)(n - 1) * kStateN * sizeof(float), kWsAlign);
-        p.dsum_bytes = round_up((size_t)rows * (size_t)(n - 1) * sizeof(float), kWsAlign);
+
+    // Many rows: balance the last wave, with the wide CTA (128 channels, 8 warps: one per SM by
+    // its registers) of the fast bf16 path.
+    const int64_t wrpc = selscan::scan_wide_rows_per_cta();
+    const int64_t wgx = (dim + wrpc - 1) / wrpc;
+    const int64_t wblocks = batch * wgx;
+    const int64_t q = wblocks / sms, r = wblocks % sms;
+    // (The cut blocks are the last r blocks of the last batch, so r must not exceed its blocks.)
+    if (fast && p.rows_per_lane == 2 && q >= 1 && r > 0 && r <= wgx &&
+        seqlen >= 2 * kMinBalanceSegTokens) {
+        int64_t n = std::min<int64_t>(sms / r, seqlen / kMinBalanceSegTokens);
+        int64_t seg_len = (seqlen + n - 1) / n;
+        seg_len = (seg_len + chunk - 1) / chunk * chunk;
+        n = (seqlen + seg_len - 1) / seg_len;
+        // Unsplit: the hardware spreads the 32-channel blocks over the SMs, and the busiest
+        // scheduler holds ceil(blocks / sms) CTAs' worth of warps (two warps a CTA).
+        const int64_t per_sm = (blocks + sms - 1) / sms;
+        const int warps_sched = (int)((per_sm * 2 + 3) / 4);
+        const double t_unsplit = sched_time((double)warps_sched, warps_sched);
+        // Balanced: two warps per scheduler, q whole wide blocks plus one segment each, after
+        // the local-end pass over the cut blocks' first n-1 segments (about 0.6 of a full pass).
+        const double seg = (double)seg_len / (double)seqlen;
+        const double t_split = sched_time(2.0 * ((double)q + seg), 2) + sched_time(2.0 * 0.6 * seg, 2);
+        if (n >= 2 && t_split < t_unsplit) {
+            p.gx = wgx;
+            p.nfull = wblocks - r;
+            p.nsplit = r;
+            p.nseg = (int)n;
+            p.seg_len = seg_len;
+            p.wide = true;
+            p.optional = true;
+            set_workspace(p, p.nsplit * wrpc);
+            return p;
+        }
     }
-    p.ws_bytes = p.hloc_bytes + p.dsum_bytes;
+    set_workspace(p, p.nsplit * rpc);
     return p;
+}
+
+// The plan to run with `ws_bytes` of workspace: the balanced split is dropped (unsplit launch)
+// when the workspace cannot hold it.
+// `fast`: the call takes the bf16 vector path without the zero-order hold (the only path with
+// the wide CTA); the balanced split is dropped otherwise, or when the workspace cannot hold it.
+Plan plan_for_workspace(int64_t batch, int64_t dim, int64_t seqlen, int sms, size_t ws_bytes,
+                        bool fast) {
+    Plan p = make_plan(batch, dim, seqlen, sms, fast);
+    if (p.optional && ws_bytes < p.ws_bytes) p = make_plan(batch, dim, seqlen, sms, false);
+    return p;
+}
+
+// The bf16 vector path without the zero-order hold: the one the balanced plan's wide CTA has.
+bool fast_path(selscan_dtype in_dtype, int64_t seqlen, int flags) {
+    return in_dtype == SELSCAN_BF16 && seqlen % 8 == 0 && !(flags & SELSCAN_FLAG_ZOH);
 }
 
 bool shape_ok(int64_t batch, int64_t dim, int64_t seqlen) {
@@ -111,8 +208,40 @@ SELSCAN_EXPORT size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_
     if (!shape_ok(batch, dim, seqlen) || dstate != kStateN) return 0;
     int sms = 0;
     if (device_sms(&sms) != SELSCAN_OK) return 0;
-    return make_plan(batch, dim, seqlen, sms).ws_bytes;
+    return make_plan(batch, dim, seqlen, sms, true).ws_bytes;
 }
+
+SELSCAN_EXPORT selscan_status ssm_scan_plan(int64_t batch, int64_t dim, int64_t dstate,
+                                            int64_t seqlen, selscan_dtype in_dtype, int flags,
+                                            size_t workspace_bytes, int64_t* info) {
+    if (!info) return SELSCAN_ERR_INVALID_ARG;
+    if (dstate != kStateN || !dtype_ok(in_dtype)) return SELSCAN_ERR_UNSUPPORTED;
+    if (!shape_ok(batch, dim, seqlen) || (flags & ~kKnownFlags)) return SELSCAN_ERR_INVALID_ARG;
+    int sms = 0;
+    const selscan_status s = device_sms(&sms);
+    if (s != SELSCAN_OK) return s;
+    const Plan p = plan_for_workspace(batch, dim, seqlen, sms, workspace_bytes,
+                                      fast_path(in_dtype, seqlen, flags));
+    info[0] = p.rows_per_lane;
+    info[1] = p.nfull;
+    info[2] = p.nsplit;
+    info[3] = p.nseg;
+    info[4] = p.nsplit > 0 ? p.seg_len : seqlen;
+    info[5] = p.wide ? selscan::scan_wide_rows_per_cta() : selscan::scan_rows_per_cta();
+    info[6] = (int64_t)p.ws_bytes;
+    info[7] = p.optional ? 0 : (int64_t)p.ws_bytes;
+    return SELSCAN_OK;
+}
+
+namespace selscan {
+size_t scan_required_workspace(int64_t batch, int64_t dim, int64_t seqlen) {
+    if (!shape_ok(batch, dim, seqlen)) return 0;
+    int sms = 0;
+    if (device_sms(&sms) != SELSCAN_OK) return 0;
+    const Plan p = make_plan(batch, dim, seqlen, sms, true);
+    return p.optional ? 0 : p.ws_bytes;
+}
+}  // namespace selscan
 
 namespace {
 selscan_status scan_fwd_impl(
@@ -154,7 +283,8 @@ selscan_status scan_fwd_impl(
     int sms = 0;
     selscan_status s = device_sms(&sms);
     if (s != SELSCAN_OK) return s;
-    const Plan plan = make_plan(batch, dim, seqlen, sms);
+    const Plan plan = plan_for_workspace(batch, dim, seqlen, sms, workspace ? workspace_bytes : 0,
+                                         fast_path(in_dtype, seqlen, delta_softplus));
     if (plan.ws_bytes > 0) {
         if (!workspace || workspace_bytes < plan.ws_bytes) return SELSCAN_ERR_WORKSPACE;
         const Range ws_r = range_of(workspace, plan.ws_bytes);
@@ -171,13 +301,14 @@ selscan_status scan_fwd_impl(
     a.ws_hloc = plan.ws_bytes ? static_cast<float*>(workspace) : nullptr;
     a.ws_dsum = plan.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.hloc_bytes) : nullptr;
     a.dim = dim; a.seqlen = seqlen; a.seg_len = plan.seg_len; a.nseg = plan.nseg;
+    a.nfull = plan.nfull; a.nsplit = plan.nsplit; a.wide = plan.wide ? 1 : 0;
     a.softplus = (delta_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
     a.zoh = (delta_softplus & SELSCAN_FLAG_ZOH) ? 1 : 0;
     a.ckpt = ckpt;
     // Two rows per lane halves the shared-memory traffic of B and C but also the warps: worth it
     // once the rows alone give about two warps per scheduler, or when time segments supply
     // the parallelism.
-    a.rows_per_lane = (plan.nseg > 1 || batch * dim >= kTwoRowsMinRows) ? 2 : 1;
+    a.rows_per_lane = plan.rows_per_lane;
     // 128-bit loads of 8 tokens and TMA tiles of B / C need seqlen % 8 == 0 (16-byte row
     // strides) and 32-bit token coordinates.
     const bool vec = (seqlen % 8) == 0 && seqlen < (int64_t(1) << 31) - 64;

@@ -19,12 +19,23 @@ struct ScanArgs {
     void* out;
     float* final_state;
     const float* initial_state;
-    float* ws_hloc;  // (batch*dim, nseg-1, 16): local end state of segments 0..nseg-2
-    float* ws_dsum;  // (batch*dim, nseg-1): sum of Delta over those segments
+    // Work of a scan, in blocks of consecutive channels of one batch (32, or 128 with `wide`):
+    // nfull blocks run whole;
+    // nsplit blocks are cut into nseg time segments of seg_len tokens (all blocks when nfull is
+    // 0; else the last nsplit blocks of the last batch). Per launch, a CTA's block is
+    // (b0 + blockIdx.z, bx0 + blockIdx.x) and its segment blockIdx.y; a whole-block launch
+    // skips the blocks (skip_b, bx >= skip_bx0) that are cut (skip_bx0 = -1: none).
+    float* ws_hloc;  // (cut blocks * 32, nseg-1, 16): local end state of segments 0..nseg-2
+    float* ws_dsum;  // (cut blocks * 32, nseg-1): sum of Delta over those segments
     int64_t dim;
     int64_t seqlen;
+    int64_t nfull;
+    int64_t nsplit;
     int64_t seg_len;  // tokens per time segment, a multiple of the chunk length
     int nseg;         // time segments (1 = no split)
+    int64_t bx0, b0;
+    int64_t skip_bx0, skip_b;
+    int wide;         // balanced plan: CTAs of 8 warps (128 channels), one per SM
     int softplus;
     int rows_per_lane;  // 1 or 2 (2 only honoured on the bf16 vector path)
     int zoh;            // zero-order-hold discretisation of B instead of Euler
@@ -35,8 +46,12 @@ struct ScanArgs {
 cudaError_t launch_scan_fwd(const ScanArgs& a, int64_t batch, bool in_bf16, bool out_bf16,
                             bool vec, bool precise, cudaStream_t stream);
 int scan_chunk_tokens();  // time segments are multiples of this
+// Workspace bytes without which a scan of this shape cannot run on the current device (its
+// time split is needed for parallelism); a split that only balances the GPU is not counted.
+size_t scan_required_workspace(int64_t batch, int64_t dim, int64_t seqlen);
 int scan_rows_per_cta();
 int scan_ctas_per_sm(int rows_per_lane);  // CTAs per SM the scan kernels are built to fit
+int scan_wide_rows_per_cta();  // channels per CTA of the balanced plan's wide CTA
 
 // Copies the device error bits raised by kernels of this library (synchronises `stream`);
 // with `reset`, clears them afterwards.

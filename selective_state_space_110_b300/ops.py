@@ -7,6 +7,8 @@ Shapes and layouts follow include/selscan.h:
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _lib
@@ -43,6 +45,21 @@ def _stream_handle(stream):
 def workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
     """Bytes of workspace ssm_scan_fwd needs on the current device (0 = none)."""
     return int(_lib.lib().ssm_scan_workspace_size(batch, dim, dstate, seqlen))
+
+
+def scan_plan(batch: int, dim: int, dstate: int, seqlen: int, workspace_bytes: int | None = None,
+              in_dtype=torch.bfloat16, softplus: bool = True, zoh: bool = False) -> dict:
+    """How ssm_scan_fwd launches this shape on the current device (ssm_scan_plan). With
+    workspace_bytes None, the plan for a workspace of workspace_size() bytes."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace_size(batch, dim, dstate, seqlen)
+    info = (ctypes.c_int64 * 8)()
+    st = _lib.lib().ssm_scan_plan(batch, dim, dstate, seqlen, _DT[in_dtype], _flags(softplus, zoh),
+                                  workspace_bytes, info)
+    _lib.check("ssm_scan_plan", st)
+    keys = ("rows_per_lane", "whole_blocks", "split_blocks", "segments", "segment_tokens",
+            "channels_per_block", "workspace_bytes", "required_workspace_bytes")
+    return dict(zip(keys, (int(v) for v in info)))
 
 
 def _flags(softplus, zoh):

@@ -36,3 +36,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
                                 x["delta_bias"], True)
     assert_close(out, ref, TOL[torch.bfloat16], "y after a timed-out wait")
     assert_close(fin, rfin, TOL[torch.bfloat16], "final state after a timed-out wait")
+
+
+def test_device_flag_is_shared_by_streams():
+    """The error word is one per device: a timeout raised by a launch on one stream is reported
+    by a query on another stream, and a reset from there clears it for both."""
+    lib = _lib.lib()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    assert lib.selscan_device_status(1, s1.cuda_stream) == OK
+    assert lib.selscan_selftest_wait_timeout(200_000, s1.cuda_stream) == OK
+    s1.synchronize()
+    assert lib.selscan_device_status(0, s2.cuda_stream) == TIMEOUT
+    assert lib.selscan_device_status(1, s2.cuda_stream) == TIMEOUT
+    assert lib.selscan_device_status(0, s1.cuda_stream) == OK

@@ -205,3 +205,38 @@ def test_full_size_config_sampled_rows(name, k):
     tol = TOL[torch.bfloat16]
     assert_close(flat(out), ref, tol, f"{name} y (sampled rows)")
     assert_close(flat(fin), rfin, tol, f"{name} final state (sampled rows)")
+
+
+# More blocks of 128 channels than SMs (bf16 fast path): the balanced plan runs one whole
+# block per SM in wide CTAs and cuts the remainder blocks into time segments (local-end
+# pass + fold) that fill the last wave. Every element checked, with the plan asserted, and the
+# same call with too small a workspace (the unsplit launch) checked too.
+BALANCED = [
+    (5, 4096, 512, "bf16", torch.float32, True),
+    (5, 4096, 520, "bf16", torch.bfloat16, False),  # seqlen % 16 != 0, last segment ragged
+    (3, 6840, 512, "bf16", torch.float32, True),    # dim % 128 != 0: a cut block part-empty
+]
+
+
+@pytest.mark.parametrize("case", BALANCED, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{c[3]}-h0{int(c[5])}")
+def test_balanced_plan_full_check(case):
+    from selective_state_space_110_b300 import scan_plan
+    b, d, L, dt, odt, with_h0 = case
+    in_dt = torch.bfloat16 if dt == "bf16" else torch.float32
+    plan = scan_plan(b, d, 16, L, in_dtype=in_dt)
+    assert plan["split_blocks"] > 0 and plan["whole_blocks"] > 0 and plan["segments"] > 1, plan
+    assert plan["required_workspace_bytes"] == 0 and plan["channels_per_block"] == 128, plan
+    cfg = small_cfg(b, d, L, dt, 60 + d + L)
+    x = make_scan_inputs(cfg, DEV)
+    h0 = torch.randn(b, d, 16, device=DEV, generator=torch.Generator(DEV).manual_seed(9)) if with_h0 else None
+    out, fin = run_gpu(x, out_dtype=odt, initial_state=h0)
+    ref, rfin = run_oracle(x, initial_state=h0)
+    tol = TOL[x["u"].dtype]
+    assert_close(out, ref, tol, "balanced y")
+    assert_close(fin, rfin, tol, "balanced final state")
+    # Without room for the split: the unsplit launch, same results to rounding.
+    tiny = torch.empty(16, dtype=torch.uint8, device=DEV)
+    assert scan_plan(b, d, 16, L, 16, in_dtype=in_dt)["split_blocks"] == 0
+    out2, fin2 = run_gpu(x, out_dtype=odt, initial_state=h0, workspace=tiny)
+    assert_close(out2, ref, tol, "unsplit y")
+    assert_close(fin2, rfin, tol, "unsplit final state")
