@@ -42,9 +42,10 @@ L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the scan kernel on this workload,
 # from one ncu capture of the same kernel code (summarised under profiles/, the file named in
 # SCAN_TRAFFIC_SOURCE); re-taken whenever the kernel changes.
-SCAN_KERNEL_NAME = "scan_kernel (full pass)"
-SCAN_TRAFFIC_BYTES = {}
-SCAN_TRAFFIC_SOURCE = {}
+SCAN_KERNEL_NAME = "scan_kernel: the launches of one scan (local-end pass, whole blocks, segments)"
+SCAN_TRAFFIC_BYTES = {"c2_mamba2p8b": 310_319_360}
+SCAN_TRAFFIC_SOURCE = {"c2_mamba2p8b": "ncu capture in profiles/scan_fwd_c2_mamba2p8b.md: 12.10 + "
+                                       "277.87 + 20.34 MB over the three launches of one scan"}
 
 
 # ------------------------------------------------------------------------------------------

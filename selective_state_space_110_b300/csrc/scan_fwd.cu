@@ -57,6 +57,7 @@ constexpr int kMaxChunk = 32;  // time segments are multiples of this many token
 // shape. The default CTA holds 32 channels; the wide CTA (8 warps, 128 channels of two rows
 // per quad) is for the balanced launch, where its registers alone keep it to one CTA per SM.
 constexpr int kWideWarps = 8;
+constexpr int kPdlTrigger = 1, kPdlWaitStart = 2, kPdlWaitEnd = 4;  // ScanArgs::pdl bits
 template <int kR, int kW = 4 / kR>
 struct Geo {
     static_assert(kR == 1 || kR == 2, "rows per lane must be 1 or 2");
@@ -190,11 +191,24 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
     // (Only the wide CTA of the balanced plan is offset or skips blocks; the default geometry
     // always starts at block 0.)
     constexpr bool kOffset = kW == kWideWarps;
+    if constexpr (kOffset) {
+        if (a.pdl & kPdlWaitStart) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (a.pdl & kPdlTrigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+    // Before any exit of a launch that must not finish ahead of the grids before it.
+    auto pdl_exit = [&]() {
+        if constexpr (kOffset) {
+            if (a.pdl & kPdlWaitEnd) asm volatile("griddepcontrol.wait;" ::: "memory");
+        }
+    };
     const int64_t b = kOffset ? a.b0 + blockIdx.z : (int64_t)blockIdx.z;
     const int seg = blockIdx.y;
     const int64_t bx = kOffset ? a.bx0 + blockIdx.x : (int64_t)blockIdx.x;
     // The whole-block launch of the balanced plan leaves the blocks its segments cover.
-    if (kOffset && a.skip_bx0 >= 0 && b == a.skip_b && bx >= a.skip_bx0) return;
+    if (kOffset && a.skip_bx0 >= 0 && b == a.skip_b && bx >= a.skip_bx0) {
+        pdl_exit();
+        return;
+    }
     const int64_t dim = a.dim;
     const int64_t d0 = bx * kRowsPerCta + warp * kRowsPerWarp + quad * kR;
     const int64_t L = a.seqlen;
@@ -423,6 +437,7 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
                 for (int k = 1; k < kS && c + k < nchunks; ++k)
                     mbar_wait_bounded(&sm.full[(c + k) % kS], (uint32_t)(((c + k) / kS) & 1));
             }
+            pdl_exit();
             return;
         }
         // Every thread has read stage `stage`: refill it with chunk c + kS.
@@ -585,6 +600,7 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
                     make_float4(h01[j].x, h01[j].y, h23[j].x, h23[j].y);
         if (own_act && (kR == 1 ? g == 0 : (g & 1) == 0)) a.ws_dsum[(ws_row0() + jo) * nprev + seg] = s;
     }
+    pdl_exit();
 }
 
 // ---- host side ---------------------------------------------------------------------------------
@@ -646,6 +662,20 @@ cudaError_t launch_typed(const ScanArgs& args, int64_t batch, cudaStream_t strea
     constexpr auto local_kernel = scan_kernel<kR, Tin, Tout, kVec, kPrecise, kZoh, Mode::kLocalEnd, false, kW>;
     auto launch = [&](auto kernel, dim3 grid, const ScanArgs& a) -> cudaError_t {
         if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
+        if (a.pdl & (kPdlWaitStart | kPdlWaitEnd)) {  // may start before the launch before it ends
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = grid;
+            cfg.blockDim = dim3(G::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, mB, mC);
+            return e != cudaSuccess ? e : cudaGetLastError();
+        }
         kernel<<<grid, G::kThreads, 0, stream>>>(a, mB, mC);
         return cudaGetLastError();
     };
@@ -653,27 +683,36 @@ cudaError_t launch_typed(const ScanArgs& args, int64_t batch, cudaStream_t strea
     if (args.nsplit == 0) {  // whole blocks only
         ScanArgs a = args;
         a.nseg = 1; a.seg_len = std::max<int64_t>(a.seqlen, 1); a.bx0 = 0; a.b0 = 0; a.skip_bx0 = -1;
+        a.pdl = 0;
         return launch(full_kernel(), dim3(gx, 1, (unsigned)batch), a);
     }
     if (args.nfull == 0) {  // every block cut into segments
         ScanArgs a = args;
         a.bx0 = 0; a.b0 = 0; a.skip_bx0 = -1;
+        a.pdl = 0;
         if (a.nseg > 1) e = launch(local_kernel, dim3(gx, (unsigned)(a.nseg - 1), (unsigned)batch), a);
         if (e == cudaSuccess) e = launch(full_kernel(), dim3(gx, (unsigned)a.nseg, (unsigned)batch), a);
         return e;
     }
     // Balanced: the cut blocks are the last nsplit blocks of the last batch. Local-end pass of
     // their first nseg-1 segments, the whole blocks (one CTA per SM), then their segments.
+    // The three launches overlap their starts (programmatic dependent launch): the whole
+    // blocks start on the SMs the local-end pass leaves free and wait for it before they exit;
+    // the segments, which fold its results, wait for the whole-block grid (and so for both) before
+    // they begin, but are already launched when it ends.
     const int64_t bx_cut = (int64_t)gx - args.nsplit;
     ScanArgs cut = args;
     cut.bx0 = bx_cut; cut.b0 = batch - 1; cut.skip_bx0 = -1;
+    cut.pdl = kPdlTrigger;
     e = launch(local_kernel, dim3((unsigned)args.nsplit, (unsigned)(args.nseg - 1), 1), cut);
     if (e != cudaSuccess) return e;
     ScanArgs whole = args;
     whole.nseg = 1; whole.seg_len = std::max<int64_t>(whole.seqlen, 1); whole.bx0 = 0; whole.b0 = 0;
     whole.skip_bx0 = bx_cut; whole.skip_b = batch - 1;
+    whole.pdl = kPdlTrigger | kPdlWaitEnd;
     e = launch(full_kernel(), dim3(gx, 1, (unsigned)batch), whole);
     if (e != cudaSuccess) return e;
+    cut.pdl = kPdlWaitStart;
     return launch(full_kernel(), dim3((unsigned)args.nsplit, (unsigned)args.nseg, 1), cut);
 }
 

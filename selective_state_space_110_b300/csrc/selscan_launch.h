@@ -36,6 +36,10 @@ struct ScanArgs {
     int64_t bx0, b0;
     int64_t skip_bx0, skip_b;
     int wide;         // balanced plan: CTAs of 8 warps (128 channels), one per SM
+    // Programmatic dependent launch of the balanced plan's three launches (wide CTA only):
+    // bit 0 lets the next launch in the stream start its CTAs now, bit 1 waits for the earlier
+    // grids before anything else, bit 2 waits for them before the CTA exits.
+    int pdl;
     int softplus;
     int rows_per_lane;  // 1 or 2 (2 only honoured on the bf16 vector path)
     int zoh;            // zero-order-hold discretisation of B instead of Euler
