@@ -376,7 +376,7 @@ SELSCAN_EXPORT selscan_status ssm_state_update(float* state, const void* x, cons
     if (s != SELSCAN_OK) return s;
     selscan::UpdateArgs a{};
     a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
-    a.out = out; a.dt_bias = dt_bias; a.dim = dim; a.rows = (int64_t)rows;
+    a.out = out; a.dt_bias = dt_bias; a.dim = dim; a.rows = (int64_t)rows; a.sms = sms;
     a.softplus = (dt_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
     a.zoh = (dt_softplus & SELSCAN_FLAG_ZOH) ? 1 : 0;
     cudaError_t e = selscan::launch_state_update(a, in_dtype == SELSCAN_BF16,
@@ -452,7 +452,7 @@ SELSCAN_EXPORT selscan_status ssm_conv_state_update(
     if (st != SELSCAN_OK) return st;
     selscan::UpdateArgs a{};
     a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
-    a.out = out; a.dt_bias = dt_bias; a.dim = dim; a.rows = (int64_t)rows;
+    a.out = out; a.dt_bias = dt_bias; a.dim = dim; a.rows = (int64_t)rows; a.sms = sms;
     a.softplus = (dt_flags & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
     a.zoh = (dt_flags & SELSCAN_FLAG_ZOH) ? 1 : 0;
     a.conv_state = conv_state; a.conv_weight = conv_weight; a.conv_bias = conv_bias;

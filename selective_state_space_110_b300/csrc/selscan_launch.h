@@ -79,6 +79,8 @@ struct UpdateArgs {
     int64_t rows;  // batch*dim
     int softplus;
     int zoh;
+    int sms;            // SMs of the device (sizes the launch)
+    int early_trigger;  // set by the launcher: let the next grid start before this one's wait
     // Short causal convolution before the update (conv_state NULL = none); state NULL with a
     // conv_state runs the convolution step alone.
     void* conv_state;          // (rows, 4), input dtype, rolled in place

@@ -110,3 +110,27 @@ def test_ragged_channels_larger_batch():
                                              tok["C"], p["D"], tok["z"], p["dt_bias"], True)
         assert_close(out, ref, TOL[torch.bfloat16], f"step {step} y")
         assert_close(st, ref_state, TOL[torch.bfloat16], f"step {step} state")
+
+
+@pytest.mark.parametrize("dim", [5000, 5120])
+def test_two_rows_per_quad_back_to_back(dim):
+    """Batch 16: one row per lane quad would need a second wave of CTAs, so each quad takes two
+    rows and the next launch is let in early. dim 5,000 leaves the last CTA 8 of its 128 rows.
+    Three steps on the same state run back to back on one stream (each launch's state prefetch
+    comes before the previous step has written that state); every row is checked."""
+    cfg = DECODE_CONFIG.replace(dim=dim)
+    batch = 16
+    p = make_decode_layer_params(cfg, DEV)
+    st = make_decode_state(cfg, batch, 0, DEV)
+    ref_state = st.clone()
+    toks = [make_decode_tokens(cfg, batch, 0, step, DEV) for step in range(3)]
+    outs = []
+    for tok in toks:
+        outs.append(ssm_state_update(st, tok["x"], tok["dt"], p["A"], tok["B"], tok["C"], p["D"],
+                                     tok["z"], dt_bias=p["dt_bias"]))
+    torch.cuda.synchronize()
+    for step, tok in enumerate(toks):
+        ref_state, ref = oracle.state_update(ref_state, tok["x"], tok["dt"], p["A"], tok["B"],
+                                             tok["C"], p["D"], tok["z"], p["dt_bias"], True)
+        assert_close(outs[step], ref, TOL[torch.bfloat16], f"step {step} y")
+    assert_close(st, ref_state, TOL[torch.bfloat16], "state after three steps")
