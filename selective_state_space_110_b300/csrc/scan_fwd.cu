@@ -29,9 +29,13 @@
 //     128-bit load per tensor, issued one chunk ahead), computes Delta and k = Delta*u once per
 //     element in registers, and its quad receives them by width-4 shuffles, which use no
 //     shared-memory bandwidth. The exp2 arguments of two tokens come from one packed multiply.
-//   - Every 4 tokens each lane writes its partial readouts to shared memory; at the end of
-//     the chunk each lane sums the quad's partials of its 8 tokens, applies the D skip and the
-//     silu gate (packed f32x2) and stores 8 outputs with one 128-bit store.
+//   - The quad's 4 partial readouts of a token are summed where the owner lane can use them.
+//     With two rows per quad this is a reduce-scatter in registers (two exchange steps by
+//     shuffles, no shared memory: step 1 pairs the lanes that hold the two rows in swapped
+//     register slots, step 2 the lanes that own the two halves of the chunk); with one row,
+//     each lane writes its partials to shared memory every 4 tokens and the owner sums them
+//     at the end of the chunk. The owner applies the D skip and the silu gate (packed f32x2)
+//     and stores its 8 outputs with one 128-bit store.
 //   - Long sequences with few rows are cut into time segments that run in parallel
 //     (grid.y). A first pass (kLocalEnd) scans segments 0..S-2 from a zero state and keeps
 //     each segment's end state and summed Delta. The full pass then starts segment s from the
@@ -222,19 +226,31 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
     };
 
     // Rows of this quad; inactive rows (past dim) compute on row 0's parameters and store nothing.
+    // With two rows per quad the full pass sums the quad's partial readouts in registers
+    // (kQuadSum, below); for that, register slot j of lane g holds row j ^ (g >> 1) of the quad,
+    // so slot 0 is always the row the lane owns.
+    constexpr bool kQuadSum = kR == 2 && kFull;
+    const int jbit = kQuadSum ? (g >> 1) : 0;
     bool act[kR];
     int64_t row[kR];
 #pragma unroll
     for (int j = 0; j < kR; ++j) {
-        act[j] = d0 + j < dim;
-        row[j] = b * dim + (act[j] ? d0 + j : 0);
+        act[j] = d0 + (j ^ jbit) < dim;
+        row[j] = b * dim + (act[j] ? d0 + (j ^ jbit) : 0);
     }
     // The row and tokens this lane owns: Delta, k, the epilogue and the stores.
     const int jo = kR == 1 ? 0 : (g >> 1);
     const int to = 8 * (kR == 1 ? g : (g & 1));
-    const bool own_act = act[jo];
-    const int64_t own_row = row[jo];
+    const bool own_act = kQuadSum ? act[0] : act[jo];
+    const int64_t own_row = kQuadSum ? row[0] : row[jo];
     const int64_t own_d = own_row - b * dim;
+    // Lane (within the quad) that owns slot j's row for tokens 8h..8h+7 of a chunk.
+    int src_lane[kR][2];
+#pragma unroll
+    for (int j = 0; j < kR; ++j) {
+        src_lane[j][0] = owner_of<kR>(j ^ jbit, 0);
+        src_lane[j][1] = owner_of<kR>(j ^ jbit, 8);
+    }
 
     // ---- TMA ring: initialise the barriers and start the first stages ----
     if (kVec) {
@@ -291,7 +307,7 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
             h01[j] = make_float2(s.x, s.y); h23[j] = make_float2(s.z, s.w);
         }
         for (int i = 0; i < seg; ++i) {
-            const int64_t sr = ws_row0() + j;
+            const int64_t sr = ws_row0() + (j ^ jbit);
             const float ds = a.ws_dsum[sr * nprev + i];
             const float4 hl = *reinterpret_cast<const float4*>(a.ws_hloc + (sr * nprev + i) * kN + 4 * g);
             if (kPrecise) {  // exp(A*S) h + h_local, with exp written as 1 + expm1
@@ -450,6 +466,8 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
 
         // ---- the recurrence over the chunk's tokens, 4 at a time ----
         const float* const bcb = &sm.bc[buf][0][0];
+        float wk[2][4];  // kQuadSum: blocks 0 and 1 summed over lanes g and g ^ 2
+        float Yo[8];     // kQuadSum: the quad's sums of the lane's 8 owned tokens
 #pragma unroll
         for (int q = 0; q < kBlocks; ++q) {
             // The state before every 16th token, for a backward pass that reuses it.
@@ -472,7 +490,8 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int t = 4 * q + e;
-                    dq[j][e] = __shfl_sync(0xffffffffu, dl[t & 7], owner_of<kR>(j, t), 4);
+                    const int src = kQuadSum ? src_lane[j][(t >> 3) & 1] : owner_of<kR>(j, t);
+                    dq[j][e] = __shfl_sync(0xffffffffu, dl[t & 7], src, 4);
                 }
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {
@@ -490,7 +509,8 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
                 const float4 Cv = *reinterpret_cast<const float4*>(rowp + ((m & 4) ? 0 : 16));
 #pragma unroll
                 for (int j = 0; j < kR; ++j) {
-                    const float kt = __shfl_sync(0xffffffffu, kl[t & 7], owner_of<kR>(j, t), 4);
+                    const int src = kQuadSum ? src_lane[j][(t >> 3) & 1] : owner_of<kR>(j, t);
+                    const float kt = __shfl_sync(0xffffffffu, kl[t & 7], src, 4);
                     const float2 kk = f2(kt);
                     float arg[4];
 #pragma unroll
@@ -531,7 +551,27 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
                     }
                 }
             }
-            if (kFull) {
+            if constexpr (kQuadSum) {
+                // The quad's sums of the block's 4 readouts of each of its 2 rows, reduce-
+                // scattered in registers. Step 1 (lanes g, g ^ 2): slot 0 (the own row) plus the
+                // partner's slot 1, which holds the same row.
+                float w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[e] = yq[0][e] + __shfl_xor_sync(0xffffffffu, yq[1][e], 2);
+                if (q < 2) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) wk[q][e] = w[e];
+                } else {
+                    // Step 2 (lanes g, g ^ 1), with block q - 2: lane g keeps the block in the
+                    // half of the chunk it owns (tokens 8 (g & 1)..) and adds the partner's copy.
+                    const bool hi = (g & 1) != 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float keep = hi ? w[e] : wk[q - 2][e], send = hi ? wk[q - 2][e] : w[e];
+                        Yo[4 * (q - 2) + e] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                    }
+                }
+            } else if (kFull) {
 #pragma unroll
                 for (int j = 0; j < kR; ++j)
                     sm.red[warp][j][q][lane ^ red_swz<kR>(j, q)] =
@@ -541,18 +581,23 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
 
         if (kFull) {
             // ---- sum the quad's partial readouts of the owned tokens ----
-            __syncwarp();
             float2 Y[4];
+            if constexpr (kQuadSum) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) Y[i] = make_float2(0.f, 0.f);
+                for (int i = 0; i < 4; ++i) Y[i] = make_float2(Yo[2 * i], Yo[2 * i + 1]);
+            } else {
+                __syncwarp();
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int q = to / 4 + jj;
+                for (int i = 0; i < 4; ++i) Y[i] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int gp = 0; gp < 4; ++gp) {
-                    const float4 v = sm.red[warp][jo][q][(4 * quad + gp) ^ g];
-                    Y[2 * jj] = __fadd2_rn(Y[2 * jj], make_float2(v.x, v.y));
-                    Y[2 * jj + 1] = __fadd2_rn(Y[2 * jj + 1], make_float2(v.z, v.w));
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int q = to / 4 + jj;
+#pragma unroll
+                    for (int gp = 0; gp < 4; ++gp) {
+                        const float4 v = sm.red[warp][jo][q][(4 * quad + gp) ^ g];
+                        Y[2 * jj] = __fadd2_rn(Y[2 * jj], make_float2(v.x, v.y));
+                        Y[2 * jj + 1] = __fadd2_rn(Y[2 * jj + 1], make_float2(v.z, v.w));
+                    }
                 }
             }
             // ---- D skip, silu gate, store ----
@@ -568,7 +613,7 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
                 out8[2 * i] = y.x; out8[2 * i + 1] = y.y;
             }
             store8<Tout, kVec>(o_row + tl, nval, out8);
-            __syncwarp();  // the quad's partials are consumed before the next chunk rewrites them
+            if (!kQuadSum) __syncwarp();  // the partials are read before the next chunk rewrites them
         }
     }
 
