@@ -43,9 +43,9 @@ L2_FLUSH_BYTES = 256 << 20
 # from one ncu capture of the same kernel code (summarised under profiles/, the file named in
 # SCAN_TRAFFIC_SOURCE); re-taken whenever the kernel changes.
 SCAN_KERNEL_NAME = "scan_kernel: the launches of one scan (local-end pass, whole blocks, segments)"
-SCAN_TRAFFIC_BYTES = {"c2_mamba2p8b": 310_319_360}
+SCAN_TRAFFIC_BYTES = {"c2_mamba2p8b": 312_382_720}
 SCAN_TRAFFIC_SOURCE = {"c2_mamba2p8b": "ncu capture in profiles/scan_fwd_c2_mamba2p8b.md: 12.10 + "
-                                       "277.87 + 20.34 MB over the three launches of one scan"}
+                                       "280.07 + 20.20 MB over the three launches of one scan"}
 
 
 # ------------------------------------------------------------------------------------------
@@ -644,7 +644,7 @@ def run_ours(args):
 
 
 def run_profile(args):
-    """One scan of the workload (plus one decode layer-step at batch 64), or with
+    """One scan of the workload (plus one decode layer-step at batch 64 and one at 16), or with
     --profile-op bwd two backward calls: a small, bounded program for ncu captures."""
     from selective_state_space_110_b300 import ssm_scan_fwd, ssm_state_update
     cfg = scan_config(args.workload)
@@ -674,9 +674,11 @@ def run_profile(args):
     out, fin = ssm_scan_fwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
                             x["delta_bias"], x["delta_softplus"])
     p = make_decode_layer_params(DECODE_CONFIG, "cuda")
-    st = make_decode_state(DECODE_CONFIG, 64, 0, "cuda")
-    t = make_decode_tokens(DECODE_CONFIG, 64, 0, 0, "cuda")
-    ssm_state_update(st, t["x"], t["dt"], p["A"], t["B"], t["C"], p["D"], t["z"], dt_bias=p["dt_bias"])
+    for batch in (64, 16):
+        st = make_decode_state(DECODE_CONFIG, batch, 0, "cuda")
+        t = make_decode_tokens(DECODE_CONFIG, batch, 0, 0, "cuda")
+        ssm_state_update(st, t["x"], t["dt"], p["A"], t["B"], t["C"], p["D"], t["z"],
+                         dt_bias=p["dt_bias"])
     torch.cuda.synchronize()
     print(json.dumps({"profile": cfg.name, "finite": bool(torch.isfinite(out).all().item())}))
 
