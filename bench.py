@@ -331,15 +331,17 @@ def ssd_work(cfg):
 
 def time_ssd(cfg, steps, warmup, flush, stream):
     """ssd_chunk_scan_fwd on the Mamba-2 layer workload, L2 flushed before every step."""
-    from selective_state_space_110_b300 import ssd_chunk_scan_fwd
+    from selective_state_space_110_b300 import ssd_chunk_scan_fwd, ssd_workspace_size
     from workloads import make_ssd_inputs
     x = make_ssd_inputs(cfg, "cuda")
     y = torch.empty(x["x"].shape, dtype=torch.bfloat16, device="cuda")
     fin = torch.empty(cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate, device="cuda")
+    need = ssd_workspace_size(cfg.batch, cfg.seqlen, cfg.nheads)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda") if need else None
 
     def call():
         ssd_chunk_scan_fwd(x["x"], x["dt"], x["A"], x["B"], x["C"], x["D"], x["z"], x["dt_bias"],
-                           x["dt_softplus"], y=y, final_state=fin, stream=stream)
+                           x["dt_softplus"], y=y, final_state=fin, workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):

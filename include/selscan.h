@@ -341,7 +341,15 @@ size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, i
  * SELSCAN_FLAG_SOFTPLUS. Arithmetic: fp32 accumulation on the tensor cores; the products the
  * layer derives (the masked decay matrix, the decayed inputs, the state) enter as the sum of two
  * bf16 parts, which keeps about 16 significand bits. The state of each (b, h) stays on chip for
- * the whole sequence; nothing but y and the final state is written. No workspace.
+ * the whole sequence; nothing but y and the final state is written to the outputs.
+ *
+ * workspace (device, 16-byte aligned, owned by the caller, not read before it is written):
+ * optional. One CTA per SM takes one (b, h) chain; when the chains fill whole waves of SMs and a
+ * remainder, the remainder's chains are cut into time segments run in parallel (their end
+ * states from zero in a first pass, folded into each segment's initial state, then the whole
+ * chains and the segments), which needs ssd_chunk_scan_workspace_size() bytes. With NULL or
+ * fewer bytes the chains run unsplit; the results agree to rounding. The workspace must not
+ * overlap any input or output (SELSCAN_ERR_INVALID_ARG).
  */
 selscan_status ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A, const void* B,
                                   const void* C, const float* D, const void* z,
@@ -349,7 +357,16 @@ selscan_status ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A,
                                   float* final_state, const float* initial_state, int64_t batch,
                                   int64_t seqlen, int64_t nheads, int64_t headdim,
                                   int64_t ngroups, int64_t dstate, selscan_dtype in_dtype,
-                                  selscan_dtype out_dtype, selscan_stream_t stream);
+                                  selscan_dtype out_dtype, void* workspace,
+                                  size_t workspace_bytes, selscan_stream_t stream);
+
+/*
+ * ssd_chunk_scan_workspace_size: bytes of workspace ssd_chunk_scan_fwd uses to balance the
+ * last wave of (batch x nheads) chains of seqlen tokens on the current device (0 = the chains
+ * run unsplit: they fit one wave, fill whole waves, or are too short to cut; also 0 for
+ * invalid shapes or without a device).
+ */
+size_t ssd_chunk_scan_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads);
 
 /*
  * selscan_device_status: errors that kernels of this library detected on the device.

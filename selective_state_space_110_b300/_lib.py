@@ -30,7 +30,7 @@ STATUS = {
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selscan_status_string",
            "ssm_scan_fwd_no_alloc", "selscan_device_status", "selscan_selftest_wait_timeout",
            "ssm_conv_state_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
-           "ssd_chunk_scan_fwd", "ssm_scan_fwd_host", "ssm_scan_fwd_host_workspace_size",
+           "ssd_chunk_scan_fwd", "ssd_chunk_scan_workspace_size", "ssm_scan_fwd_host", "ssm_scan_fwd_host_workspace_size",
            "ssm_scan_fwd_ckpt", "ssm_scan_plan")
 
 # Size of the fixed scratch array behind ssm_scan_fwd_no_alloc (SELSCAN_NO_ALLOC_SCRATCH_BYTES).
@@ -80,7 +80,9 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_bwd_workspace_size.argtypes = [_I64] * 4 + [ctypes.c_int]
     lib.ssd_chunk_scan_fwd.restype = ctypes.c_int
     lib.ssd_chunk_scan_fwd.argtypes = ([_VP] * 8 + [ctypes.c_int] + [_VP] * 3 + [_I64] * 6 +
-                                       [ctypes.c_int, ctypes.c_int, _VP])
+                                       [ctypes.c_int, ctypes.c_int, _VP, ctypes.c_size_t, _VP])
+    lib.ssd_chunk_scan_workspace_size.restype = ctypes.c_size_t
+    lib.ssd_chunk_scan_workspace_size.argtypes = [_I64] * 3
     lib.ssm_scan_fwd_host.restype = ctypes.c_int
     lib.ssm_scan_fwd_host.argtypes = ([_VP] * 8 + [ctypes.c_int, _VP, _VP] + [_I64] * 4 +
                                       [ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_size_t, _VP])

@@ -593,12 +593,19 @@ SELSCAN_EXPORT selscan_status ssm_scan_bwd(
     return e == cudaSuccess ? SELSCAN_OK : SELSCAN_ERR_CUDA;
 }
 
+SELSCAN_EXPORT size_t ssd_chunk_scan_workspace_size(int64_t batch, int64_t seqlen,
+                                                    int64_t nheads) {
+    int sms = 0;
+    if (batch < 1 || nheads < 1 || seqlen < 0 || device_sms(&sms) != SELSCAN_OK) return 0;
+    return selscan::ssd_plan(batch, nheads, seqlen, sms).workspace_bytes;
+}
+
 SELSCAN_EXPORT selscan_status ssd_chunk_scan_fwd(
     const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
     const void* z, const float* dt_bias, int dt_softplus, void* y, float* final_state,
     const float* initial_state, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
     int64_t ngroups, int64_t dstate, selscan_dtype in_dtype, selscan_dtype out_dtype,
-    selscan_stream_t stream) {
+    void* workspace, size_t workspace_bytes, selscan_stream_t stream) {
     if (headdim != 64 || dstate != 128 || in_dtype != SELSCAN_BF16 || !dtype_ok(out_dtype))
         return SELSCAN_ERR_UNSUPPORTED;
     if (batch < 1 || batch > 65535 || nheads < 1 || nheads > 65535 || ngroups < 1 ||
@@ -607,7 +614,7 @@ SELSCAN_EXPORT selscan_status ssd_chunk_scan_fwd(
         return SELSCAN_ERR_INVALID_ARG;
     const bool has_tokens = seqlen > 0;
     if (!A || (has_tokens && (!x || !dt || !B || !C || !y))) return SELSCAN_ERR_INVALID_ARG;
-    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, y, final_state, initial_state};
+    const void* ptrs[] = {x, dt, A, B, C, D, z, dt_bias, y, final_state, initial_state, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SELSCAN_ERR_ALIGNMENT;
     const size_t eout = dtype_size(out_dtype);
@@ -629,12 +636,22 @@ SELSCAN_EXPORT selscan_status ssd_chunk_scan_fwd(
     int sms = 0;
     selscan_status s = device_sms(&sms);
     if (s != SELSCAN_OK) return s;
+    // The workspace only balances the last wave: without enough of it the chains run unsplit.
+    const size_t ws_need = selscan::ssd_plan(batch, nheads, seqlen, sms).workspace_bytes;
+    if (!workspace || workspace_bytes < ws_need) workspace = nullptr;
+    if (workspace && ws_need) {
+        const Range ws_r = range_of(workspace, ws_need);
+        for (const Range& r : in_r)
+            if (overlaps(ws_r, r)) return SELSCAN_ERR_INVALID_ARG;
+        if (overlaps(ws_r, y_r) || overlaps(ws_r, fin_r)) return SELSCAN_ERR_INVALID_ARG;
+    }
     selscan::SsdArgs a{};
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
     a.y = y; a.final_state = final_state; a.initial_state = initial_state;
     a.batch = batch; a.seqlen = seqlen; a.nheads = nheads; a.ngroups = ngroups;
     a.softplus = (dt_softplus & SELSCAN_FLAG_SOFTPLUS) ? 1 : 0;
-    cudaError_t e = selscan::launch_ssd_fwd(a, out_dtype == SELSCAN_BF16,
+    cudaError_t e = selscan::launch_ssd_fwd(a, out_dtype == SELSCAN_BF16, workspace,
+                                            workspace ? workspace_bytes : 0, sms,
                                             reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();

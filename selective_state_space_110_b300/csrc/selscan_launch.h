@@ -163,8 +163,28 @@ struct SsdArgs {
     int64_t nheads;
     int64_t ngroups;
     int softplus;
+    // Balanced launch (set by launch_ssd_fwd): the first n_whole (batch, head) chains run whole,
+    // the others are cut into nseg segments of seg_chunks chunks. job_mode 0: one CTA per chain
+    // on a (nheads, batch) grid; 1: the local ends of segments 0..nseg-2 of the cut chains,
+    // then the whole chains; 2: every segment of the cut chains.
+    int job_mode;
+    int64_t n_whole;
+    int nseg;
+    int seg_chunks;
+    float* ws_sloc;   // (cut chains, nseg - 1, 64, 128): end states of segments from zero
+    float* ws_sinit;  // (cut chains, nseg - 1, 64, 128): initial states of segments 1..nseg-1
+    float* ws_dsum;   // (cut chains, nseg - 1): summed Delta*A*log2(e) of segments 0..nseg-2
 };
-cudaError_t launch_ssd_fwd(const SsdArgs& a, bool out_bf16, cudaStream_t stream);
+// The balanced launch of an SSD call: cut chains, segments, chunks per segment and the
+// workspace bytes it needs (all 0 / 1 when it does not pay).
+struct SsdPlan {
+    int64_t n_whole, n_cut;
+    int nseg, seg_chunks;
+    size_t workspace_bytes;
+};
+SsdPlan ssd_plan(int64_t batch, int64_t nheads, int64_t seqlen, int sms);
+cudaError_t launch_ssd_fwd(const SsdArgs& a, bool out_bf16, void* workspace,
+                           size_t workspace_bytes, int sms, cudaStream_t stream);
 // Error bits raised by the SSD kernel (timeouts of its bounded waits); see read_device_status.
 cudaError_t read_ssd_status(unsigned int* status, bool reset, cudaStream_t stream);
 

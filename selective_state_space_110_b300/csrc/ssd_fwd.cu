@@ -48,6 +48,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "selscan_device.cuh"
@@ -162,6 +163,51 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// The job of a CTA: chain ci = b * H + h, chunks [c_first, c_first + nchunks), and for a cut
+// chain its index tc among the cut chains and its segment.
+struct SsdJob {
+    int64_t ci, tc;
+    int c_first, nchunks, seg;
+    bool cut;
+};
+__device__ __forceinline__ SsdJob ssd_job(const SsdArgs& a, int nchunks_all) {
+    SsdJob j{0, 0, 0, nchunks_all, 0, false};
+    // job_mode 1: the local-end jobs (n_cut x (nseg - 1) of them) first, then the whole chains
+    const int64_t n_local = a.job_mode == 1 ? (a.batch * a.nheads - a.n_whole) * (a.nseg - 1) : 0;
+    if (a.job_mode == 0) {
+        j.ci = (int64_t)blockIdx.y * a.nheads + blockIdx.x;
+    } else if (a.job_mode == 1 && (int64_t)blockIdx.x >= n_local) {
+        j.ci = (int64_t)blockIdx.x - n_local;
+    } else {
+        const int64_t k = blockIdx.x;
+        const int per = a.job_mode == 1 ? a.nseg - 1 : a.nseg;  // jobs per cut chain
+        j.tc = k / per;
+        j.seg = (int)(k % per);
+        j.ci = a.n_whole + j.tc;
+        j.c_first = j.seg * a.seg_chunks;
+        j.nchunks = min(a.seg_chunks, nchunks_all - j.c_first);
+        j.cut = true;
+    }
+    return j;
+}
+
+// Initial state of a job (NULL = zeros), where its end state goes (NULL = nowhere), and where
+// the local-end pass puts a segment's summed Delta*A.
+__device__ __forceinline__ const float* ssd_job_init(const SsdArgs& a, const SsdJob& j) {
+    constexpr int64_t kStateElems = (int64_t)kHeadDim * kSsdState;
+    const float* chain_init = a.initial_state ? a.initial_state + j.ci * kStateElems : nullptr;
+    if (!j.cut || j.seg == 0) return chain_init;
+    if (a.job_mode == 1) return nullptr;  // a later segment's end state from zero (local end)
+    return a.ws_sinit + (j.tc * (a.nseg - 1) + j.seg - 1) * kStateElems;  // folded
+}
+__device__ __forceinline__ float* ssd_job_final(const SsdArgs& a, const SsdJob& j) {
+    constexpr int64_t kStateElems = (int64_t)kHeadDim * kSsdState;
+    float* chain_final = a.final_state ? a.final_state + j.ci * kStateElems : nullptr;
+    if (!j.cut) return chain_final;
+    if (a.job_mode == 1) return a.ws_sloc + (j.tc * (a.nseg - 1) + j.seg) * kStateElems;
+    return j.seg == a.nseg - 1 ? chain_final : nullptr;
+}
+
 template <typename Tout>
 __global__ void __launch_bounds__(kSsdThreads, 1)
     ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tmX,
@@ -185,16 +231,32 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __shared__ __align__(16) float s_cf[kQ];
     __shared__ float s_span[kQ / 16];
     __shared__ int s_ok;
+    // Where this CTA's end state and (local-end jobs) summed Delta*A go, and whether it writes
+    // y: set once by thread 0, read at the end, so that no register holds them meanwhile.
+    __shared__ float* sh_final;
+    __shared__ float* sh_dsum;
+    __shared__ int sh_store_y;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     auto tile = [&](int i) { return sm + i * kTile; };
     auto tile_addr = [&](int i) { return smem_u32(sm) + (uint32_t)(i * kTile); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, b = blockIdx.y;
     const int64_t H = a.nheads, L = a.seqlen;
+    const int nchunks_all = (int)((L + kQ - 1) / kQ);
+    constexpr int64_t kStateElems = (int64_t)kHeadDim * kSsdState;
+    // This CTA's job (one chain, or a segment of a cut chain in the balanced launch).
+    const SsdJob job = ssd_job(a, nchunks_all);
+    const int nchunks = job.nchunks;
+    const int h = (int)(job.ci % H), b = (int)(job.ci / H);
     const int g = (int)(h / (H / a.ngroups));
-    const int nchunks = (int)((L + kQ - 1) / kQ);
-    const bool init_state = a.initial_state != nullptr;
+    const int t_base = job.c_first * kQ;  // first token of this CTA's chunks (< 2^31)
+    const bool init_state = ssd_job_init(a, job) != nullptr;
+    if (tid == 0) {
+        const bool local_end = a.job_mode == 1 && job.cut;  // writes no output
+        sh_final = ssd_job_final(a, job);
+        sh_dsum = local_end ? a.ws_dsum + job.tc * (a.nseg - 1) + job.seg : nullptr;
+        sh_store_y = local_end ? 0 : 1;
+    }
 
     if (warp == 0) tmem_alloc(&tmem_slot, kTmemCols);
     if (tid == 0) {
@@ -234,7 +296,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     };
     if (init_state && warp < kWorkers / 32) {  // initial state (p, n) -> S[n][p], split
         float v[32];
-        const float* src = a.initial_state + ((int64_t)b * H + h) * kHeadDim * kSsdState + row;
+        const float* src = ssd_job_init(a, job) + row;
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = src[(int64_t)(32 * half + i) * kSsdState];
         tmem_st32(tmem + tlane + kColS + 32 * half, v);
@@ -255,11 +317,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                 const int base = kInTiles * (c & 1);
                 unsigned long long* bar = &bar_tma[c & 1];
                 mbar_arrive_expect_tx(bar, kInTiles * kTile);
-                tma_load_4d(tile(base + kInC), &tmC, bar, 0, g, c * kQ, b);
-                tma_load_4d(tile(base + kInC + 1), &tmC, bar, 64, g, c * kQ, b);
-                tma_load_4d(tile(base + kInB), &tmB, bar, 0, g, c * kQ, b);
-                tma_load_4d(tile(base + kInB + 1), &tmB, bar, 64, g, c * kQ, b);
-                tma_load_4d(tile(base + kInX), &tmX, bar, 0, h, c * kQ, b);
+                const int tc0 = t_base + c * kQ;
+                tma_load_4d(tile(base + kInC), &tmC, bar, 0, g, tc0, b);
+                tma_load_4d(tile(base + kInC + 1), &tmC, bar, 64, g, tc0, b);
+                tma_load_4d(tile(base + kInB), &tmB, bar, 0, g, tc0, b);
+                tma_load_4d(tile(base + kInB + 1), &tmB, bar, 64, g, tc0, b);
+                tma_load_4d(tile(base + kInX), &tmX, bar, 0, h, tc0, b);
             };
             // Waits for the output of chunk cc to be read (per-buffer barrier, one phase per
             // two chunks).
@@ -367,18 +430,19 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         auto load_dt = [&](int c) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int64_t t = (int64_t)c * kQ + 4 * lane + i;
+                const int64_t t = (int64_t)(t_base + c * kQ + 4 * lane + i);
                 raw[i] = (c < nchunks && t < L) ? __bfloat162float(dt[((int64_t)b * L + t) * H + h]) : 0.f;
             }
         };
         load_dt(0);
         bool ok = true;
+        float dsum = 0.f;  // lane 31: the sum of the chunk totals
         for (int c = 0; c < nchunks; ++c) {
             float dl[4], al[4], cs[4];
             float run = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int64_t t = (int64_t)c * kQ + 4 * lane + i;
+                const int64_t t = (int64_t)(t_base + c * kQ + 4 * lane + i);
                 const float v = raw[i] + bias;
                 dl[i] = t < L ? (a.softplus ? softplus_f<true>(v) : v) : 0.f;
                 al[i] = dl[i] * A2;
@@ -433,7 +497,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             *reinterpret_cast<float4*>(&s_cf[4 * lane]) = make_float4(cf[0], cf[1], cf[2], cf[3]);
             if ((lane & 3) == 0) s_span[lane >> 2] = span;
             mbar_arrive(&bar_sums);
+            dsum += incl;  // lane 31: the chunk's total
         }
+        // the local-end pass: the segment's summed Delta*A*log2(e), for the fold
+        if (ok && lane == 31 && sh_dsum) *sh_dsum = dsum;
         if (!ok) s_ok = 0;
     } else {
         // ---------------- 256 worker threads ----------------
@@ -445,7 +512,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         // ahead of the output step.
         uint4 z0 = make_uint4(0u, 0u, 0u, 0u), z1 = z0, z2 = z0, z3 = z0;
         auto load_z = [&](int cc) {
-            const int64_t t_row = (int64_t)cc * kQ + row;
+            const int64_t t_row = (int64_t)(t_base + cc * kQ + row);
             if (zp && t_row < L) {
                 const uint4* zq = reinterpret_cast<const uint4*>(
                     zp + ((int64_t)b * L + t_row) * H * kHeadDim + (int64_t)h * kHeadDim + 32 * half);
@@ -454,7 +521,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         };
         // y of chunk cc = exp(cs_i) C S + M X + D x, times silu(z); e = exp(cs_i) of its row.
         auto output = [&](int cc, float e, bool with_state) {
-            const int64_t t_row = (int64_t)cc * kQ + row;
+            const int64_t t_row = (int64_t)(t_base + cc * kQ + row);
             const int64_t yoff = ((int64_t)b * L + t_row) * H * kHeadDim + (int64_t)h * kHeadDim + 32 * half;
             ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g2, (uint32_t)(cc & 1)));
             tc_fence_after_sync();
@@ -467,7 +534,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                     tmem_ld16_async(tmem + tlane + kColMX + 32 * half + 16 * hq, mx);
                     if (with_state) tmem_ld16_async(tmem + tlane + ccol + 32 * half + 16 * hq, cs);
                     tmem_wait_ld();
-                    if (t_row < L) {
+                    if (sh_store_y && t_row < L) {
                         float yd[16];
 #pragma unroll
                         for (int qq = 0; qq < 2; ++qq) {
@@ -498,7 +565,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         float e_prev = 0.f;      // exp(cs_i) of the previous chunk (its output is pending)
         bool prev_state = false;
         for (int c = 0; c < nchunks; ++c) {
-            const int64_t t0 = (int64_t)c * kQ;
+            const int64_t t0 = (int64_t)(t_base + c * kQ);
             const uint32_t par = (uint32_t)(c & 1);
             const int in = kInTiles * (c & 1);
             const uint32_t gcol = (c & 1) ? kColG1 : kColG0;
@@ -635,7 +702,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         }
         if (ok && nchunks > 0) output(nchunks - 1, e_prev, prev_state);
 
-        if (ok && a.final_state) {  // S[n][p] -> final_state (p, n)
+        float* const s_final = sh_final;
+        if (ok && s_final) {  // S[n][p] -> final_state (p, n)
             float v[32];
             if (nchunks > 0 || init_state) {
                 tmem_ld32(tmem + tlane + kColS + 32 * half, v);
@@ -643,7 +711,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
             }
-            float* dst = a.final_state + ((int64_t)b * H + h) * kHeadDim * kSsdState + row;
+            float* dst = s_final + row;
 #pragma unroll
             for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * half + i) * kSsdState] = v[i];
         }
@@ -653,6 +721,38 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __syncthreads();
     if (tid == 0 && !s_ok) atomicOr(&g_ssd_status, 1u);
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// The initial states of segments 1..nseg-1 of the cut chains from the local-end pass: segment
+// s+1 starts from 2^(dsum_s) times segment s's initial state plus segment s's end state from
+// zero (the recurrence is linear in the state); segment 0's end state already started from the
+// chain's initial state. One thread per (cut chain, state element), in segment order.
+__global__ void ssd_fold_kernel(const SsdArgs a) {
+    constexpr int64_t kStateElems = (int64_t)kHeadDim * kSsdState;
+    constexpr int kBatch = 8;  // segments whose loads are issued together
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t tc = blockIdx.y;
+    if (e >= kStateElems) return;
+    const int64_t base = tc * (a.nseg - 1);
+    const float* __restrict__ sloc = a.ws_sloc + base * kStateElems + e;
+    const float* __restrict__ dsum = a.ws_dsum + base;
+    float* __restrict__ sinit = a.ws_sinit + base * kStateElems + e;
+    float v = 0.f;
+    for (int s0 = 0; s0 < a.nseg - 1; s0 += kBatch) {
+        float l[kBatch], d[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const bool in = s0 + i < a.nseg - 1;
+            l[i] = in ? sloc[(int64_t)(s0 + i) * kStateElems] : 0.f;
+            d[i] = in && s0 + i > 0 ? dsum[s0 + i] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (s0 + i >= a.nseg - 1) break;
+            v = s0 + i == 0 ? l[i] : fmaf(exp2f(d[i]), v, l[i]);
+            sinit[(int64_t)(s0 + i) * kStateElems] = v;
+        }
+    }
 }
 
 // ---- host side ---------------------------------------------------------------------------------
@@ -693,26 +793,87 @@ cudaError_t make_ssd_map(CUtensorMap* m, const void* base, int64_t inner, int64_
 }
 
 template <typename Tout>
-cudaError_t launch_ssd_typed(const SsdArgs& a, cudaStream_t stream) {
+cudaError_t launch_ssd_typed(const SsdArgs& a0, void* workspace, size_t workspace_bytes, int sms,
+                             cudaStream_t stream) {
     CUtensorMap mX{}, mB{}, mC{};
-    if (a.seqlen > 0) {
-        cudaError_t e = make_ssd_map(&mX, a.x, kHeadDim, a.nheads, a.seqlen, a.batch);
-        if (e == cudaSuccess) e = make_ssd_map(&mB, a.B, kSsdState, a.ngroups, a.seqlen, a.batch);
-        if (e == cudaSuccess) e = make_ssd_map(&mC, a.C, kSsdState, a.ngroups, a.seqlen, a.batch);
+    if (a0.seqlen > 0) {
+        cudaError_t e = make_ssd_map(&mX, a0.x, kHeadDim, a0.nheads, a0.seqlen, a0.batch);
+        if (e == cudaSuccess) e = make_ssd_map(&mB, a0.B, kSsdState, a0.ngroups, a0.seqlen, a0.batch);
+        if (e == cudaSuccess) e = make_ssd_map(&mC, a0.C, kSsdState, a0.ngroups, a0.seqlen, a0.batch);
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaFuncSetAttribute(ssd_fwd_kernel<Tout>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSsdSmemBytes);
     if (e != cudaSuccess) return e;
-    ssd_fwd_kernel<Tout><<<dim3((unsigned)a.nheads, (unsigned)a.batch), kSsdThreads, kSsdSmemBytes,
-                           stream>>>(a, mX, mB, mC);
+    SsdArgs a = a0;
+    const SsdPlan plan = ssd_plan(a.batch, a.nheads, a.seqlen, sms);
+    if (plan.n_cut == 0 || !workspace || workspace_bytes < plan.workspace_bytes) {
+        a.job_mode = 0;  // one CTA per chain
+        ssd_fwd_kernel<Tout><<<dim3((unsigned)a.nheads, (unsigned)a.batch), kSsdThreads,
+                               kSsdSmemBytes, stream>>>(a, mX, mB, mC);
+        return cudaGetLastError();
+    }
+    // The balanced launch: the local ends of the cut chains' segments 0..nseg-2 (listed first,
+    // so they run on the first wave's SMs) with the whole chains; their fold into initial
+    // states; then every segment of the cut chains (the last wave).
+    constexpr size_t kStateBytes = (size_t)kHeadDim * kSsdState * sizeof(float);
+    const size_t nslots = (size_t)plan.n_cut * (size_t)(plan.nseg - 1);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.n_whole = plan.n_whole;
+    a.nseg = plan.nseg;
+    a.seg_chunks = plan.seg_chunks;
+    a.ws_sloc = reinterpret_cast<float*>(ws);
+    a.ws_sinit = reinterpret_cast<float*>(ws + nslots * kStateBytes);
+    a.ws_dsum = reinterpret_cast<float*>(ws + 2 * nslots * kStateBytes);
+    a.job_mode = 1;
+    ssd_fwd_kernel<Tout><<<(unsigned)(nslots + plan.n_whole), kSsdThreads, kSsdSmemBytes, stream>>>(
+        a, mX, mB, mC);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (plan.nseg > 1) {
+        ssd_fold_kernel<<<dim3((unsigned)((kHeadDim * kSsdState + 255) / 256), (unsigned)plan.n_cut),
+                          256, 0, stream>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    a.job_mode = 2;
+    const int64_t jobs = plan.n_cut * plan.nseg;
+    ssd_fwd_kernel<Tout><<<(unsigned)jobs, kSsdThreads, kSsdSmemBytes, stream>>>(a, mX, mB, mC);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_ssd_fwd(const SsdArgs& a, bool out_bf16, cudaStream_t stream) {
-    return out_bf16 ? launch_ssd_typed<__nv_bfloat16>(a, stream) : launch_ssd_typed<float>(a, stream);
+// The chains (batch x heads, one CTA each, one CTA per SM) fill n full waves plus a remainder
+// of r < sms chains that would run alone for a whole chain's time. Those r chains are cut into
+// segments of seg_chunks chunks, as many as keep the r x nseg segments in one wave, at least two
+// chunks each: the local-end pass and the segments' full pass then take about 2 seg_chunks
+// chunk-times instead of nchunks. Not when the chains fit in one wave (nothing waits on a
+// remainder) or the cut saves less than a third of that time.
+SsdPlan ssd_plan(int64_t batch, int64_t nheads, int64_t seqlen, int sms) {
+    SsdPlan p{batch * nheads, 0, 1, 0, 0};
+    const int64_t chains = batch * nheads;
+    const int64_t nchunks = (seqlen + kQ - 1) / kQ;
+    if (sms <= 0 || chains <= sms || nchunks < 4) return p;
+    const int64_t r = chains % sms;
+    if (r == 0) return p;
+    const int64_t nseg_target = std::min<int64_t>(sms / r, nchunks / 2);
+    if (nseg_target < 2) return p;
+    const int64_t seg_chunks = (nchunks + nseg_target - 1) / nseg_target;
+    const int64_t nseg = (nchunks + seg_chunks - 1) / seg_chunks;
+    if (nseg < 2 || 3 * (2 * seg_chunks) > 2 * nchunks) return p;
+    constexpr size_t kStateBytes = (size_t)kHeadDim * kSsdState * sizeof(float);
+    const size_t nslots = (size_t)r * (size_t)(nseg - 1);
+    p.n_whole = chains - r;
+    p.n_cut = r;
+    p.nseg = (int)nseg;
+    p.seg_chunks = (int)seg_chunks;
+    p.workspace_bytes = 2 * nslots * kStateBytes + (nslots * sizeof(float) + 255) / 256 * 256;
+    return p;
+}
+
+cudaError_t launch_ssd_fwd(const SsdArgs& a, bool out_bf16, void* workspace,
+                           size_t workspace_bytes, int sms, cudaStream_t stream) {
+    return out_bf16 ? launch_ssd_typed<__nv_bfloat16>(a, workspace, workspace_bytes, sms, stream)
+                    : launch_ssd_typed<float>(a, workspace, workspace_bytes, sms, stream);
 }
 
 cudaError_t read_ssd_status(unsigned int* status, bool reset, cudaStream_t stream) {

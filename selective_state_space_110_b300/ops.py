@@ -336,11 +336,20 @@ def ssm_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
     return g
 
 
+def ssd_workspace_size(batch: int, seqlen: int, nheads: int) -> int:
+    """Bytes of workspace ssd_chunk_scan_fwd uses on the current device to balance the last wave
+    of (batch x nheads) chains (0 = it runs them unsplit)."""
+    return int(_lib.lib().ssd_chunk_scan_workspace_size(batch, seqlen, nheads))
+
+
 def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True,
                        initial_state=None, out_dtype=None, y=None, final_state=None,
-                       return_final_state=True, stream=None):
+                       return_final_state=True, workspace=None, balance=True, stream=None):
     """Mamba-2 SSD layer. x (batch, seqlen, nheads, 64) bf16, dt (batch, seqlen, nheads) bf16,
-    A (nheads) fp32, B/C (batch, seqlen, ngroups, 128) bf16. Returns (y, final_state or None)."""
+    A (nheads) fp32, B/C (batch, seqlen, ngroups, 128) bf16. Returns (y, final_state or None).
+    With balance (the default) and no workspace given, one of ssd_workspace_size() bytes is
+    allocated, so that the last wave of chains is cut into time segments; balance=False runs
+    every chain unsplit."""
     if x.dim() != 4:
         raise ValueError("x must be (batch, seqlen, nheads, headdim)")
     batch, seqlen, nheads, headdim = x.shape
@@ -369,11 +378,19 @@ def ssd_chunk_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus
         final_state = torch.empty((batch, nheads, headdim, dstate), dtype=torch.float32, device=dev)
     _check_dev("final_state", final_state, torch.float32, (batch, nheads, headdim, dstate), dev)
     with torch.cuda.device(dev):
+        if balance and workspace is None:
+            need = ssd_workspace_size(batch, seqlen, nheads)
+            if need:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if not balance:
+            workspace = None
+        _check_dev("workspace", workspace, None, None, dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
         st = _lib.lib().ssd_chunk_scan_fwd(
             _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
             _flags(dt_softplus, False), _ptr(y), _ptr(final_state), _ptr(initial_state), batch,
-            seqlen, nheads, headdim, ngroups, dstate, _DT[in_dt], _DT[y.dtype],
-            _stream_handle(stream))
+            seqlen, nheads, headdim, ngroups, dstate, _DT[in_dt], _DT[y.dtype], _ptr(workspace),
+            ws_bytes, _stream_handle(stream))
     _lib.check("ssd_chunk_scan_fwd", st)
     return y, final_state
 

@@ -237,12 +237,13 @@ def call_ssd(lib, **kw):
     a = dict(x=fake(0), dt=fake(1), A=fake(2), B=fake(3), C=fake(4), D=fake(5), z=fake(6),
              dt_bias=fake(7), flags=1, y=fake(8), fin=fake(9), h0=None, batch=2, seqlen=256,
              nheads=8, headdim=64, ngroups=1, dstate=128, in_dtype=_lib.BF16, out_dtype=_lib.BF16,
-             stream=None)
+             ws=None, ws_bytes=0, stream=None)
     a.update(kw)
     return lib.ssd_chunk_scan_fwd(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
                                   a["dt_bias"], a["flags"], a["y"], a["fin"], a["h0"], a["batch"],
                                   a["seqlen"], a["nheads"], a["headdim"], a["ngroups"],
-                                  a["dstate"], a["in_dtype"], a["out_dtype"], a["stream"])
+                                  a["dstate"], a["in_dtype"], a["out_dtype"], a["ws"],
+                                  a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -260,6 +261,7 @@ def call_ssd(lib, **kw):
     (dict(fin=fake(8) + 16), INVALID),       # final state inside y
     (dict(h0=fake(9)), INVALID),             # final state over the initial state
     (dict(B=fake(3) + 8), ALIGN),
+    (dict(ws=fake(10) + 8, ws_bytes=1 << 20), ALIGN),
 ])
 def test_ssd_rejects(lib, kw, expect):
     assert call_ssd(lib, **kw) == expect
@@ -271,6 +273,9 @@ def test_ssd_valid_args_reach_the_device_check(lib):
         pytest.skip("device present: covered by the GPU tests")
     assert call_ssd(lib) == CUDA
     assert call_ssd(lib, seqlen=0, x=None, dt=None, B=None, C=None, y=None) == CUDA
+    assert call_ssd(lib, ws=fake(10), ws_bytes=1 << 30) == CUDA
+    # The balanced plan depends on the device's SM count; without a device it is 0 bytes.
+    assert lib.ssd_chunk_scan_workspace_size(4, 2048, 80) == 0
 
 
 def call_host(lib, **kw):

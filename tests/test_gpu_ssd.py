@@ -154,3 +154,32 @@ def test_strong_decay(dt_range):
     ry, rf = _oracle(x)
     assert_close(y, ry, TOL_BF16, "y")
     assert_close(fin, rf, TOL_BF16, "final state")
+
+
+@pytest.mark.parametrize("seqlen,dt_range", [(1024, None), (1000, (0.2, 0.5))],
+                         ids=["1024-tokens", "1000-tokens-mixed-decay"])
+def test_balanced_launch(seqlen, dt_range):
+    """160 chains (2 x 80 heads) on 148 SMs: the last 12 chains (batch 1, heads 68-79) are cut
+    into time segments (their local end states from a first pass, folded into each segment's
+    initial state). Sampled heads on both sides of the cut, with an initial state, against the
+    oracle; every output against the unsplit launch; and a workspace too small for the plan
+    runs unsplit, bit for bit."""
+    from selective_state_space_110_b300 import ssd_workspace_size
+    kw = {} if dt_range is None else dict(dt_min=dt_range[0], dt_max=dt_range[1])
+    cfg = SsdConfig("bal", 2, seqlen, 80, 64, 1, 128, 91 + seqlen, **kw)
+    need = ssd_workspace_size(2, seqlen, 80)
+    assert need > 0, "the plan should cut the last wave's chains on this device"
+    x = make_ssd_inputs(cfg, DEV)
+    h0 = torch.randn(2, 80, 64, 128, device=DEV, generator=torch.Generator(DEV).manual_seed(5))
+    y, fin = _gpu(x, out_dtype=torch.float32, initial_state=h0)
+    y0, fin0 = _gpu(x, out_dtype=torch.float32, initial_state=h0, balance=False)
+    small = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    y1, fin1 = _gpu(x, out_dtype=torch.float32, initial_state=h0, workspace=small)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y0) and torch.equal(fin1, fin0)
+    assert_close(y, y0.double(), TOL_BF16, "balanced y vs unsplit")
+    assert_close(fin, fin0.double(), TOL_BF16, "balanced final state vs unsplit")
+    idx = torch.tensor([3, 67, 68, 74, 79], device=DEV)
+    ry, rf = _oracle(_heads(x, idx), h0[:, idx].contiguous())
+    assert_close(y[:, :, idx], ry, TOL_BF16, "sampled heads y")
+    assert_close(fin[:, idx], rf, TOL_BF16, "sampled heads final state")
