@@ -165,8 +165,8 @@ struct SsdArgs {
     int softplus;
     // Balanced launch (set by launch_ssd_fwd): the first n_whole (batch, head) chains run whole,
     // the others are cut into nseg segments of seg_chunks chunks. job_mode 0: one CTA per chain
-    // on a (nheads, batch) grid; 1: the local ends of segments 0..nseg-2 of the cut chains,
-    // then the whole chains; 2: every segment of the cut chains.
+    // on a (nheads, batch) grid; 1: the local end states of segments 0..nseg-2 of the cut
+    // chains (the state-only kernel); 2: every segment of the cut chains; 3: the whole chains.
     int job_mode;
     int64_t n_whole;
     int nseg;

@@ -172,12 +172,10 @@ struct SsdJob {
 };
 __device__ __forceinline__ SsdJob ssd_job(const SsdArgs& a, int nchunks_all) {
     SsdJob j{0, 0, 0, nchunks_all, 0, false};
-    // job_mode 1: the local-end jobs (n_cut x (nseg - 1) of them) first, then the whole chains
-    const int64_t n_local = a.job_mode == 1 ? (a.batch * a.nheads - a.n_whole) * (a.nseg - 1) : 0;
     if (a.job_mode == 0) {
         j.ci = (int64_t)blockIdx.y * a.nheads + blockIdx.x;
-    } else if (a.job_mode == 1 && (int64_t)blockIdx.x >= n_local) {
-        j.ci = (int64_t)blockIdx.x - n_local;
+    } else if (a.job_mode == 3) {
+        j.ci = blockIdx.x;
     } else {
         const int64_t k = blockIdx.x;
         const int per = a.job_mode == 1 ? a.nseg - 1 : a.nseg;  // jobs per cut chain
@@ -208,10 +206,15 @@ __device__ __forceinline__ float* ssd_job_final(const SsdArgs& a, const SsdJob& 
     return j.seg == a.nseg - 1 ? chain_final : nullptr;
 }
 
-template <typename Tout>
+// kStateOnly: the local-end jobs of the balanced launch, which need a segment's end state
+// alone: per chunk the sums, w X and the state decay and update, no C B^T, C S, M, M X or output.
+template <typename Tout, bool kStateOnly>
 __global__ void __launch_bounds__(kSsdThreads, 1)
     ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
+    // The whole-chain launch that follows the local-end jobs does not depend on them: let it
+    // start on the SMs they leave free.
+    if (a.job_mode == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t dyn_smem[];
     // Completion of the TMA loads (per input buffer) and of the MMA groups (tcgen05.commit: G
     // per buffer, the state update, M X); hand-offs from the 256 worker threads to the issuer
@@ -243,7 +246,6 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t H = a.nheads, L = a.seqlen;
     const int nchunks_all = (int)((L + kQ - 1) / kQ);
-    constexpr int64_t kStateElems = (int64_t)kHeadDim * kSsdState;
     // This CTA's job (one chain, or a segment of a cut chain in the balanced launch).
     const SsdJob job = ssd_job(a, nchunks_all);
     const int nchunks = job.nchunks;
@@ -316,10 +318,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             auto issue_tma = [&](int c) {  // chunk c -> input buffer c & 1
                 const int base = kInTiles * (c & 1);
                 unsigned long long* bar = &bar_tma[c & 1];
-                mbar_arrive_expect_tx(bar, kInTiles * kTile);
+                // (the state-only jobs read no C)
+                mbar_arrive_expect_tx(bar, (kStateOnly ? kInTiles - 2 : kInTiles) * kTile);
                 const int tc0 = t_base + c * kQ;
-                tma_load_4d(tile(base + kInC), &tmC, bar, 0, g, tc0, b);
-                tma_load_4d(tile(base + kInC + 1), &tmC, bar, 64, g, tc0, b);
+                if (!kStateOnly) {
+                    tma_load_4d(tile(base + kInC), &tmC, bar, 0, g, tc0, b);
+                    tma_load_4d(tile(base + kInC + 1), &tmC, bar, 64, g, tc0, b);
+                }
                 tma_load_4d(tile(base + kInB), &tmB, bar, 0, g, tc0, b);
                 tma_load_4d(tile(base + kInB + 1), &tmB, bar, 64, g, tc0, b);
                 tma_load_4d(tile(base + kInX), &tmX, bar, 0, h, tc0, b);
@@ -334,78 +339,107 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             const uint32_t i_cs = umma_idesc_bf16(128, 64, false, true);    // C S, M X
             const uint32_t i_s = umma_idesc_bf16(128, 64, true, true);      // B^T (w X)
             bool ok = true;
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const int in = kInTiles * (c & 1);
-                const uint32_t par = (uint32_t)(c & 1);
-                const uint32_t gcol = (c & 1) ? kColG1 : kColG0;
-                const bool had_state = c > 0 || init_state;
-                ok = mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
-                if (ok) tma_landed = c + 1;
-                // G buffer c & 1 (M of chunk c-2) and C S buffer c & 1 are free once the
-                // output of chunk c-2 has been read.
-                if (ok && c >= 2) ok = wait_y(c - 2);
-                if (!ok) break;
-                tc_fence_after_sync();
-                // G = C B^T
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t off = (uint32_t)(k & 3) * 32;
-                    umma_bf16(tmem + gcol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
-                              umma_desc_sw128(tile_addr(in + kInB + (k >> 2)) + off, 16, 1024), i_g1, k > 0);
-                }
-                umma_commit(&bar_gg[c & 1]);
-                // C S = C S_hi + C S_lo, the state as it was before this chunk
-                if (had_state) {
-                    if (c > 0) {
-                        ok = mbar_wait_bounded(&bar_s, par ^ 1u);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                    }
-                    const uint32_t ccol = (c & 1) ? kColCS1 : kColCS0;
+            if constexpr (kStateOnly) {
+                for (int c = 0; c < nchunks && ok; ++c) {
+                    const uint32_t par = (uint32_t)(c & 1);
+                    const int in = kInTiles * (c & 1);
+                    const bool had_state = c > 0 || init_state;
+                    ok = mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
+                    if (ok) tma_landed = c + 1;
+                    // S (+)= B^T (wX)_hi + B^T (wX)_lo, after the workers decayed S and wrote w X
+                    if (ok) ok = mbar_wait_bounded(&bar_x, par);
+                    if (!ok) break;
+                    tc_fence_after_sync();
 #pragma unroll
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const uint32_t off = (uint32_t)(k & 3) * 32;
-                            umma_bf16(tmem + ccol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
-                                      umma_desc_sw128(tile_addr(part ? kTSL : kTSH) + (uint32_t)k * 2048, kTile, 1024),
-                                      i_cs, (part || k) ? 1u : 0u);
-                        }
-                }
-                // S (+)= B^T (wX)_hi + B^T (wX)_lo, after the workers decayed S and wrote w X
-                ok = mbar_wait_bounded(&bar_x, par);
-                if (!ok) break;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        umma_bf16(tmem + kColS, umma_desc_sw128(tile_addr(in + kInB) + (uint32_t)k * 2048, kTile, 1024),
-                                  umma_desc_sw128(tile_addr(part ? kTXL : kTXH) + (uint32_t)k * 2048, kTile, 1024), i_s,
-                                  (had_state || part || k) ? 1u : 0u);
-                umma_commit(&bar_g4);
-                // Once the previous chunk's output is read: its input buffer takes chunk c + 1,
-                // and the M X accumulator is free.
-                if (c > 0) {
-                    ok = wait_y(c - 1);
-                    if (!ok) break;
-                    if (c + 1 < nchunks) {
-                        issue_tma(c + 1);
-                        tma_issued = c + 2;
+                        for (int k = 0; k < 8; ++k)
+                            umma_bf16(tmem + kColS, umma_desc_sw128(tile_addr(in + kInB) + (uint32_t)k * 2048, kTile, 1024),
+                                      umma_desc_sw128(tile_addr(part ? kTXL : kTXH) + (uint32_t)k * 2048, kTile, 1024), i_s,
+                                      (had_state || part || k) ? 1u : 0u);
+                    umma_commit(&bar_g4);
+                    // Once that product has read input buffer c & 1, it takes chunk c + 2.
+                    if (c + 2 < nchunks) {
+                        ok = mbar_wait_bounded(&bar_g4, par);
+                        if (!ok) break;
+                        issue_tma(c + 2);
+                        tma_issued = c + 3;
                     }
                 }
-                // M X = M_hi X + M_lo X, M read from tensor memory (in place of G)
-                ok = mbar_wait_bounded(&bar_m, par);
-                if (!ok) break;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        umma_bf16_ts(tmem + kColMX, tmem + gcol + 16 * k + (part ? 8 : 0),
-                                     umma_desc_sw128(tile_addr(in + kInX) + (uint32_t)k * 2048, kTile, 1024), i_cs,
-                                     (part || k) ? 1u : 0u);
-                umma_commit(&bar_g2);
+            } else {
+                for (int c = 0; c < nchunks && ok; ++c) {
+                    const int in = kInTiles * (c & 1);
+                    const uint32_t par = (uint32_t)(c & 1);
+                    const uint32_t gcol = (c & 1) ? kColG1 : kColG0;
+                    const bool had_state = c > 0 || init_state;
+                    ok = mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
+                    if (ok) tma_landed = c + 1;
+                    // G buffer c & 1 (M of chunk c-2) and C S buffer c & 1 are free once the
+                    // output of chunk c-2 has been read.
+                    if (ok && c >= 2) ok = wait_y(c - 2);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    // G = C B^T
+    #pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = (uint32_t)(k & 3) * 32;
+                        umma_bf16(tmem + gcol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
+                                  umma_desc_sw128(tile_addr(in + kInB + (k >> 2)) + off, 16, 1024), i_g1, k > 0);
+                    }
+                    umma_commit(&bar_gg[c & 1]);
+                    // C S = C S_hi + C S_lo, the state as it was before this chunk
+                    if (had_state) {
+                        if (c > 0) {
+                            ok = mbar_wait_bounded(&bar_s, par ^ 1u);
+                            if (!ok) break;
+                            tc_fence_after_sync();
+                        }
+                        const uint32_t ccol = (c & 1) ? kColCS1 : kColCS0;
+    #pragma unroll
+                        for (int part = 0; part < 2; ++part)
+    #pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const uint32_t off = (uint32_t)(k & 3) * 32;
+                                umma_bf16(tmem + ccol, umma_desc_sw128(tile_addr(in + kInC + (k >> 2)) + off, 16, 1024),
+                                          umma_desc_sw128(tile_addr(part ? kTSL : kTSH) + (uint32_t)k * 2048, kTile, 1024),
+                                          i_cs, (part || k) ? 1u : 0u);
+                            }
+                    }
+                    // S (+)= B^T (wX)_hi + B^T (wX)_lo, after the workers decayed S and wrote w X
+                    ok = mbar_wait_bounded(&bar_x, par);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+    #pragma unroll
+                    for (int part = 0; part < 2; ++part)
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            umma_bf16(tmem + kColS, umma_desc_sw128(tile_addr(in + kInB) + (uint32_t)k * 2048, kTile, 1024),
+                                      umma_desc_sw128(tile_addr(part ? kTXL : kTXH) + (uint32_t)k * 2048, kTile, 1024), i_s,
+                                      (had_state || part || k) ? 1u : 0u);
+                    umma_commit(&bar_g4);
+                    // Once the previous chunk's output is read: its input buffer takes chunk c + 1,
+                    // and the M X accumulator is free.
+                    if (c > 0) {
+                        ok = wait_y(c - 1);
+                        if (!ok) break;
+                        if (c + 1 < nchunks) {
+                            issue_tma(c + 1);
+                            tma_issued = c + 2;
+                        }
+                    }
+                    // M X = M_hi X + M_lo X, M read from tensor memory (in place of G)
+                    ok = mbar_wait_bounded(&bar_m, par);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+    #pragma unroll
+                    for (int part = 0; part < 2; ++part)
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            umma_bf16_ts(tmem + kColMX, tmem + gcol + 16 * k + (part ? 8 : 0),
+                                         umma_desc_sw128(tile_addr(in + kInX) + (uint32_t)k * 2048, kTile, 1024), i_cs,
+                                         (part || k) ? 1u : 0u);
+                    umma_commit(&bar_g2);
+                }
             }
             if (!ok) {
                 // A wait gave up: record it, then give the copies and products this CTA still
@@ -564,7 +598,58 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
 
         float e_prev = 0.f;      // exp(cs_i) of the previous chunk (its output is pending)
         bool prev_state = false;
-        for (int c = 0; c < nchunks; ++c) {
+        if constexpr (kStateOnly) {
+            for (int c = 0; c < nchunks; ++c) {
+                const uint32_t par = (uint32_t)(c & 1);
+                const int in = kInTiles * (c & 1);
+                const bool had_state = c > 0 || init_state;
+                ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_sums, par));
+                const float cs_last = s_cs[kQ - 1];
+                ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1)));
+                if (ok && half == 0) {  // w * X (hi / lo), row j = row
+                    const float w = s_w[row];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        float v[8];
+                        unpack8(*reinterpret_cast<const uint4*>(tile(in + kInX) + sw128(row, ch)), v);
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const float2 p2 = __fmul2_rn(make_float2(v[e], v[e + 1]), f2(w));
+                            v[e] = p2.x;
+                            v[e + 1] = p2.y;
+                        }
+                        uint4 hi, lo;
+                        split8(v, hi, lo);
+                        *reinterpret_cast<uint4*>(tile(kTXH) + sw128(row, ch)) = hi;
+                        *reinterpret_cast<uint4*>(tile(kTXL) + sw128(row, ch)) = lo;
+                    }
+                } else if (ok && had_state) {  // the carried state decays by exp(cs_last)
+                    const float dec = ex2_approx(cs_last);
+#pragma unroll 1
+                    for (int part = 0; part < 2; ++part) {
+                        float v[32];
+                        tmem_ld32(tmem + tlane + kColS + 32 * part, v);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 d2 = __fmul2_rn(make_float2(v[i], v[i + 1]), f2(dec));
+                            v[i] = d2.x;
+                            v[i + 1] = d2.y;
+                        }
+                        tmem_st32(tmem + tlane + kColS + 32 * part, v);
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&bar_x);
+                mbar_arrive(&bar_free);  // this chunk's sums are no longer read
+                // The state update has read w X and written S before either is touched again.
+                ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(&bar_g4, par));
+                tc_fence_after_sync();
+                if (!ok) break;
+            }
+        }
+        for (int c = 0; c < (kStateOnly ? 0 : nchunks); ++c) {
             const int64_t t0 = (int64_t)(t_base + c * kQ);
             const uint32_t par = (uint32_t)(c & 1);
             const int in = kInTiles * (c & 1);
@@ -700,7 +785,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
             load_z(c);
             if (!ok) break;
         }
-        if (ok && nchunks > 0) output(nchunks - 1, e_prev, prev_state);
+        if (!kStateOnly && ok && nchunks > 0) output(nchunks - 1, e_prev, prev_state);
 
         float* const s_final = sh_final;
         if (ok && s_final) {  // S[n][p] -> final_state (p, n)
@@ -717,6 +802,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         }
         if (!ok) s_ok = 0;
     }
+    // The whole chains, launched beside the local-end jobs: finish only after them, so that the
+    // fold after this launch sees their end states.
+    if (a.job_mode == 3) asm volatile("griddepcontrol.wait;" ::: "memory");
     tc_fence_before_sync();
     __syncthreads();
     if (tid == 0 && !s_ok) atomicOr(&g_ssd_status, 1u);
@@ -802,19 +890,22 @@ cudaError_t launch_ssd_typed(const SsdArgs& a0, void* workspace, size_t workspac
         if (e == cudaSuccess) e = make_ssd_map(&mC, a0.C, kSsdState, a0.ngroups, a0.seqlen, a0.batch);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = cudaFuncSetAttribute(ssd_fwd_kernel<Tout>,
+    cudaError_t e = cudaFuncSetAttribute(ssd_fwd_kernel<Tout, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSsdSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(ssd_fwd_kernel<Tout, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSsdSmemBytes);
     if (e != cudaSuccess) return e;
     SsdArgs a = a0;
     const SsdPlan plan = ssd_plan(a.batch, a.nheads, a.seqlen, sms);
     if (plan.n_cut == 0 || !workspace || workspace_bytes < plan.workspace_bytes) {
         a.job_mode = 0;  // one CTA per chain
-        ssd_fwd_kernel<Tout><<<dim3((unsigned)a.nheads, (unsigned)a.batch), kSsdThreads,
-                               kSsdSmemBytes, stream>>>(a, mX, mB, mC);
+        ssd_fwd_kernel<Tout, false><<<dim3((unsigned)a.nheads, (unsigned)a.batch), kSsdThreads,
+                                      kSsdSmemBytes, stream>>>(a, mX, mB, mC);
         return cudaGetLastError();
     }
-    // The balanced launch: the local ends of the cut chains' segments 0..nseg-2 (listed first,
-    // so they run on the first wave's SMs) with the whole chains; their fold into initial
+    // The balanced launch: the end states of the cut chains' segments 0..nseg-2 (state only),
+    // with the whole chains starting on the SMs those leave free; their fold into initial
     // states; then every segment of the cut chains (the last wave).
     constexpr size_t kStateBytes = (size_t)kHeadDim * kSsdState * sizeof(float);
     const size_t nslots = (size_t)plan.n_cut * (size_t)(plan.nseg - 1);
@@ -826,9 +917,24 @@ cudaError_t launch_ssd_typed(const SsdArgs& a0, void* workspace, size_t workspac
     a.ws_sinit = reinterpret_cast<float*>(ws + nslots * kStateBytes);
     a.ws_dsum = reinterpret_cast<float*>(ws + 2 * nslots * kStateBytes);
     a.job_mode = 1;
-    ssd_fwd_kernel<Tout><<<(unsigned)(nslots + plan.n_whole), kSsdThreads, kSsdSmemBytes, stream>>>(
-        a, mX, mB, mC);
+    ssd_fwd_kernel<Tout, true><<<(unsigned)nslots, kSsdThreads, kSsdSmemBytes, stream>>>(a, mX, mB, mC);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+        SsdArgs w = a;
+        w.job_mode = 3;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)plan.n_whole, 1, 1);
+        cfg.blockDim = dim3(kSsdThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSsdSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, ssd_fwd_kernel<Tout, false>, w, mX, mB, mC);
+        if (e != cudaSuccess) return e;
+    }
     if (plan.nseg > 1) {
         ssd_fold_kernel<<<dim3((unsigned)((kHeadDim * kSsdState + 255) / 256), (unsigned)plan.n_cut),
                           256, 0, stream>>>(a);
@@ -836,7 +942,7 @@ cudaError_t launch_ssd_typed(const SsdArgs& a0, void* workspace, size_t workspac
     }
     a.job_mode = 2;
     const int64_t jobs = plan.n_cut * plan.nseg;
-    ssd_fwd_kernel<Tout><<<(unsigned)jobs, kSsdThreads, kSsdSmemBytes, stream>>>(a, mX, mB, mC);
+    ssd_fwd_kernel<Tout, false><<<(unsigned)jobs, kSsdThreads, kSsdSmemBytes, stream>>>(a, mX, mB, mC);
     return cudaGetLastError();
 }
 
