@@ -183,3 +183,25 @@ def test_balanced_launch(seqlen, dt_range):
     ry, rf = _oracle(_heads(x, idx), h0[:, idx].contiguous())
     assert_close(y[:, :, idx], ry, TOL_BF16, "sampled heads y")
     assert_close(fin[:, idx], rf, TOL_BF16, "sampled heads final state")
+
+
+def test_balanced_launch_groups_no_gate_bf16_out():
+    """300 chains (3 x 100 heads) on 148 SMs leave 4 chains to cut; 700 tokens end in a
+    part-filled chunk; two groups of B / C, no z, bf16 output."""
+    from selective_state_space_110_b300 import ssd_workspace_size
+    cfg = SsdConfig("bal2", 3, 700, 100, 64, 2, 128, 97, has_z=False)
+    assert ssd_workspace_size(3, 700, 100) > 0
+    x = make_ssd_inputs(cfg, DEV)
+    y, fin = _gpu(x, out_dtype=torch.bfloat16)
+    # the unsplit reference in fp32: two bf16 roundings of nearly equal values can differ by a
+    # whole ulp, more than the allowance of a bf16 output against an exact value
+    y0, fin0 = _gpu(x, out_dtype=torch.float32, balance=False)
+    torch.cuda.synchronize()
+    assert_close(y, y0.double(), TOL_BF16, "balanced y vs unsplit")
+    assert_close(fin, fin0.double(), TOL_BF16, "balanced final state vs unsplit")
+    # heads 96-99 of batch 2 are cut; two heads of each group, so that the 4-head subset keeps
+    # every head's group of B / C (group = head // (heads / 2))
+    idx = torch.tensor([0, 49, 96, 99], device=DEV)
+    ry, rf = _oracle(_heads(x, idx))
+    assert_close(y[:, :, idx], ry, TOL_BF16, "sampled heads y")
+    assert_close(fin[:, idx], rf, TOL_BF16, "sampled heads final state")
