@@ -145,20 +145,22 @@ selscan_status ssm_scan_fwd_ckpt(const void* u, const void* delta, const float* 
 size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
 
 /*
- * ssm_scan_plan: how ssm_scan_fwd will launch this shape on the current device for inputs of
- * `in_dtype`, flag bits `flags` (as delta_softplus) and `workspace_bytes` of workspace. The
- * paper has no counterpart; it describes the launch for callers that size buffers or report
+ * ssm_scan_plan: how ssm_scan_fwd will launch this shape for inputs of `in_dtype`, flag bits
+ * `flags` (as delta_softplus) and `workspace_bytes` of workspace, on a GPU of `sms` SMs (0 =
+ * the current device; a positive count plans for that many SMs without touching any device).
+ * The paper has no counterpart; it describes the launch for callers that size buffers or report
  * performance. info[0..7] (int64, host memory):
  *   [0] rows per lane (1 or 2)        [1] blocks of channels run whole
  *   [2] blocks cut into time segments [3] segments per cut block (1 = none)
  *   [4] tokens per segment            [5] channels per block (CTA)
  *   [6] workspace bytes this plan uses [7] workspace bytes the shape requires (the rest only
  *       balances the GPU)
- * Returns SELSCAN_ERR_INVALID_ARG for a NULL info, bad sizes or unknown flags,
- * SELSCAN_ERR_UNSUPPORTED for dstate != 16, an unknown dtype or a device that is not sm_103.
+ * Returns SELSCAN_ERR_INVALID_ARG for a NULL info, bad sizes, unknown flags or sms outside
+ * 0..4096, SELSCAN_ERR_UNSUPPORTED for dstate != 16, an unknown dtype or (sms 0) a current
+ * device that is not sm_103.
  */
 selscan_status ssm_scan_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                             selscan_dtype in_dtype, int flags, size_t workspace_bytes,
+                             selscan_dtype in_dtype, int flags, size_t workspace_bytes, int sms,
                              int64_t* info);
 
 /*
@@ -367,6 +369,17 @@ selscan_status ssd_chunk_scan_fwd(const void* x, const void* dt, const float* A,
  * invalid shapes or without a device).
  */
 size_t ssd_chunk_scan_workspace_size(int64_t batch, int64_t seqlen, int64_t nheads);
+
+/*
+ * ssd_chunk_scan_plan: the balanced launch of ssd_chunk_scan_fwd for (batch x nheads) chains of
+ * seqlen tokens on a GPU of `sms` SMs (0 = the current device; a positive count touches no
+ * device). info[0..4] (int64, host memory): [0] chains run whole, [1] chains cut into time
+ * segments (0 = none), [2] segments per cut chain, [3] chunks of 128 tokens per segment,
+ * [4] workspace bytes. SELSCAN_ERR_INVALID_ARG for a NULL info, bad sizes or sms outside
+ * 0..4096.
+ */
+selscan_status ssd_chunk_scan_plan(int64_t batch, int64_t seqlen, int64_t nheads, int sms,
+                                   int64_t* info);
 
 /*
  * selscan_device_status: errors that kernels of this library detected on the device.

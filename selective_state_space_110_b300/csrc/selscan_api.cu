@@ -213,13 +213,14 @@ SELSCAN_EXPORT size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_
 
 SELSCAN_EXPORT selscan_status ssm_scan_plan(int64_t batch, int64_t dim, int64_t dstate,
                                             int64_t seqlen, selscan_dtype in_dtype, int flags,
-                                            size_t workspace_bytes, int64_t* info) {
-    if (!info) return SELSCAN_ERR_INVALID_ARG;
+                                            size_t workspace_bytes, int sms, int64_t* info) {
+    if (!info || sms < 0 || sms > 4096) return SELSCAN_ERR_INVALID_ARG;
     if (dstate != kStateN || !dtype_ok(in_dtype)) return SELSCAN_ERR_UNSUPPORTED;
     if (!shape_ok(batch, dim, seqlen) || (flags & ~kKnownFlags)) return SELSCAN_ERR_INVALID_ARG;
-    int sms = 0;
-    const selscan_status s = device_sms(&sms);
-    if (s != SELSCAN_OK) return s;
+    if (sms == 0) {
+        const selscan_status s = device_sms(&sms);
+        if (s != SELSCAN_OK) return s;
+    }
     const Plan p = plan_for_workspace(batch, dim, seqlen, sms, workspace_bytes,
                                       fast_path(in_dtype, seqlen, flags));
     info[0] = p.rows_per_lane;
@@ -598,6 +599,23 @@ SELSCAN_EXPORT size_t ssd_chunk_scan_workspace_size(int64_t batch, int64_t seqle
     int sms = 0;
     if (batch < 1 || nheads < 1 || seqlen < 0 || device_sms(&sms) != SELSCAN_OK) return 0;
     return selscan::ssd_plan(batch, nheads, seqlen, sms).workspace_bytes;
+}
+
+SELSCAN_EXPORT selscan_status ssd_chunk_scan_plan(int64_t batch, int64_t seqlen, int64_t nheads,
+                                                  int sms, int64_t* info) {
+    if (!info || batch < 1 || nheads < 1 || seqlen < 0 || sms < 0 || sms > 4096)
+        return SELSCAN_ERR_INVALID_ARG;
+    if (sms == 0) {
+        const selscan_status s = device_sms(&sms);
+        if (s != SELSCAN_OK) return s;
+    }
+    const selscan::SsdPlan p = selscan::ssd_plan(batch, nheads, seqlen, sms);
+    info[0] = p.n_whole;
+    info[1] = p.n_cut;
+    info[2] = p.nseg;
+    info[3] = p.seg_chunks;
+    info[4] = (int64_t)p.workspace_bytes;
+    return SELSCAN_OK;
 }
 
 SELSCAN_EXPORT selscan_status ssd_chunk_scan_fwd(

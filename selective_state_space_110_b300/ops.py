@@ -48,17 +48,29 @@ def workspace_size(batch: int, dim: int, dstate: int, seqlen: int) -> int:
 
 
 def scan_plan(batch: int, dim: int, dstate: int, seqlen: int, workspace_bytes: int | None = None,
-              in_dtype=torch.bfloat16, softplus: bool = True, zoh: bool = False) -> dict:
-    """How ssm_scan_fwd launches this shape on the current device (ssm_scan_plan). With
-    workspace_bytes None, the plan for a workspace of workspace_size() bytes."""
+              in_dtype=torch.bfloat16, softplus: bool = True, zoh: bool = False,
+              sms: int = 0) -> dict:
+    """How ssm_scan_fwd launches this shape (ssm_scan_plan) on the current device, or with sms > 0
+    on a GPU of that many SMs (no device needed). With workspace_bytes None, the plan for a
+    workspace large enough for it (what workspace_size() returns on that GPU)."""
     if workspace_bytes is None:
-        workspace_bytes = workspace_size(batch, dim, dstate, seqlen)
+        workspace_bytes = 1 << 62
     info = (ctypes.c_int64 * 8)()
     st = _lib.lib().ssm_scan_plan(batch, dim, dstate, seqlen, _DT[in_dtype], _flags(softplus, zoh),
-                                  workspace_bytes, info)
+                                  workspace_bytes, sms, info)
     _lib.check("ssm_scan_plan", st)
     keys = ("rows_per_lane", "whole_blocks", "split_blocks", "segments", "segment_tokens",
             "channels_per_block", "workspace_bytes", "required_workspace_bytes")
+    return dict(zip(keys, (int(v) for v in info)))
+
+
+def ssd_plan(batch: int, seqlen: int, nheads: int, sms: int = 0) -> dict:
+    """The balanced launch of ssd_chunk_scan_fwd (ssd_chunk_scan_plan) on the current device, or
+    with sms > 0 on a GPU of that many SMs (no device needed)."""
+    info = (ctypes.c_int64 * 5)()
+    st = _lib.lib().ssd_chunk_scan_plan(batch, seqlen, nheads, sms, info)
+    _lib.check("ssd_chunk_scan_plan", st)
+    keys = ("whole_chains", "cut_chains", "segments", "segment_chunks", "workspace_bytes")
     return dict(zip(keys, (int(v) for v in info)))
 
 

@@ -320,3 +320,17 @@ def test_fwd_ckpt_rejects(lib):
     assert lib.ssm_scan_fwd_ckpt(*base, 3, *tail, fake(12), None) == UNSUP        # zero-order hold
     assert lib.ssm_scan_fwd_ckpt(*base, 1, *tail, fake(12) + 8, None) == ALIGN
     assert lib.ssm_scan_fwd_ckpt(*base, 1, *tail, fake(8) + 16, None) == INVALID  # inside out
+
+
+def test_plan_entry_points_reject_bad_arguments(lib):
+    import ctypes
+    info = (ctypes.c_int64 * 8)()
+    assert lib.ssm_scan_plan(4, 5120, 16, 2048, _lib.BF16, 1, 0, -1, info) == INVALID
+    assert lib.ssm_scan_plan(4, 5120, 16, 2048, _lib.BF16, 1, 0, 5000, info) == INVALID
+    assert lib.ssm_scan_plan(4, 5120, 16, 2048, _lib.BF16, 1, 0, 148, None) == INVALID
+    assert lib.ssm_scan_plan(4, 5120, 8, 2048, _lib.BF16, 1, 0, 148, info) == UNSUP
+    assert lib.ssm_scan_plan(4, 5120, 16, 2048, _lib.BF16, 1, 0, 148, info) == 0
+    assert lib.ssd_chunk_scan_plan(4, 2048, 80, 148, None) == INVALID
+    assert lib.ssd_chunk_scan_plan(0, 2048, 80, 148, info) == INVALID
+    assert lib.ssd_chunk_scan_plan(4, 2048, 80, -3, info) == INVALID
+    assert lib.ssd_chunk_scan_plan(4, 2048, 80, 148, info) == 0 and info[1] == 24
