@@ -356,7 +356,10 @@ def time_ssd(cfg, steps, warmup, flush, stream):
             call()
             ev[s][1].record(stream)
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in ev], 1
+    # launches of one call: unsplit one; balanced the state-only pass, the whole chains, the
+    # fold and the segments
+    launches = 4 if ws is not None else 1
+    return [a.elapsed_time(b) for a, b in ev], launches
 
 
 def time_scan_e2e(cfg, steps, warmup, x, stream):
@@ -487,8 +490,11 @@ def ssd_summary(scfg, ms, launches, world, scan_ms, scan_cfg):
     _, _, tflops_peak = read_tensor_peak()
     hbm_peak, _ = read_peaks()
     sec = ms * 1e-3
+    from selective_state_space_110_b300 import ssd_plan
+    plan = ssd_plan(scfg.batch, scfg.seqlen, scfg.nheads)
     out = {"what": "ssd_chunk_scan_fwd: Mamba-2 SSD layer, 128-token chunks on tcgen05, "
                    "state in tensor memory (ssd_fwd_kernel)",
+           "plan": plan,
            "workload": scfg.name,
            "shape": {"batch": scfg.batch, "seqlen": scfg.seqlen, "nheads": scfg.nheads,
                      "headdim": scfg.headdim, "ngroups": scfg.ngroups, "dstate": scfg.dstate},
