@@ -420,6 +420,17 @@ __global__ void __launch_bounds__(Geo<kR, kW>::kThreads, Geo<kR, kW>::kMinCtas)
         // ---- B and C of this chunk -> fp32 per-token rows (item = chunk-column x token) ----
         if (kVec && !mbar_wait_bounded(&sm.full[stage], parity)) timed_out = true;
         constexpr int kItems = kChunk * (kFull ? 8 : 4);  // (token, 4-state chunk) pairs
+        if constexpr (kVec && kFull && kW == kWideWarps && 2 * kItems == kThreads) {
+            // The wide CTA: one half chunk (2 states) per thread, so that no thread idles. Lane
+            // order (half, token, chunk): a half-warp's 8-byte stores cover 8 tokens x 2 halves,
+            // 16 distinct bank pairs through the XOR swizzle.
+            const int hf = tid & 1, tt = (tid >> 1) % kChunk, ch = (tid >> 1) / kChunk;
+            const int isC = ch >> 2, q = ch & 3;
+            const Tin* tile = reinterpret_cast<const Tin*>(sm.raw[stage][isC]);
+            const float2 v = make_float2(to_f32(tile[(4 * q + 2 * hf + 0) * kChunk + tt]),
+                                         to_f32(tile[(4 * q + 2 * hf + 1) * kChunk + tt]));
+            *reinterpret_cast<float2*>(&sm.bc[buf][tt][4 * (ch ^ (tt & 7)) + 2 * hf]) = v;
+        } else
 #pragma unroll
         for (int cc = 0; cc < (kItems + kThreads - 1) / kThreads; ++cc) {
             const int item = tid + kThreads * cc;
