@@ -28,7 +28,7 @@
 //
 // dB and dC are sums over every channel of a batch: each warp reduce-scatters its 8 rows' terms
 // in three shuffle rounds (lane (q, g) ends with one of the 32 dB | dC sums of the token), the
-// CTA adds its 4 warps in shared memory and writes one partial per token and value. dA, dD and
+// CTA adds its 6 warps in shared memory and writes one partial per token and value. dA, dD and
 // dbias are kept per (batch, channel). A second kernel adds the partials in a fixed order, so
 // the gradients are deterministic (no atomics).
 #include "selscan_device.cuh"
@@ -37,14 +37,16 @@
 namespace selscan {
 
 constexpr int kBChunk = 16;                 // tokens per chunk (and per checkpoint)
-constexpr int kBWarps = 4;
-constexpr int kBThreads = 32 * kBWarps;     // 128: 32 channels
-constexpr int kBRows = 32;                  // channels per CTA
+constexpr int kBWarps = 6;
+constexpr int kBThreads = 32 * kBWarps;     // 192: 48 channels
+constexpr int kBRows = 8 * kBWarps;         // channels per CTA
 constexpr int kBSlots = 32;                 // dB[0..15], dC[0..15] per token
-// CTAs per SM the kernel is built to fit: 5 (96 registers) when the grid needs the slots, 4
-// (128 registers, no spills) when it fits one wave at 4 per SM.
-constexpr int kBMinCtas = 5;
-constexpr int kBMinCtasRoomy = 4;
+// CTAs of 6 warps (48 channels, 64 KB of shared memory): 3 fit an SM. A grid of Mamba-2.8B size
+// (4 x 107 CTAs on 148 SMs) then holds at most 144 channels on any SM, where CTAs of 4 warps at
+// 5 per SM held 160. Built for 3 per SM (96 registers: 18 warps leave 5 on some schedulers) when
+// the grid needs the slots, for 2 (159-168 registers, no spills) when it fits one wave at 2.
+constexpr int kBMinCtas = 3;
+constexpr int kBMinCtasRoomy = 2;
 
 struct BwdSmem {
     float bc[2][kBChunk][32];                // B | C per token (layout: BcStage)
@@ -191,7 +193,8 @@ enum BwdMode : int { kBwdFull = 0, kBwdFwdLocal = 1, kBwdAdjLocal = 2 };
 
 template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode, int kMinCtas>
 __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const BwdArgs a) {
-    __shared__ __align__(16) BwdSmem sm;
+    extern __shared__ __align__(16) unsigned char bwd_smem[];
+    BwdSmem& sm = *reinterpret_cast<BwdSmem*>(bwd_smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = lane >> 2, g = lane & 3;
     const int64_t b = blockIdx.z;
@@ -223,20 +226,22 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
     const Tg* o_row = static_cast<const Tg*>(a.dout) + row * L;
     float* ckpt = a.ws_ckpt + (row * nchunks) * kN + 4 * g;
 
-    // B | C staging: thread -> token s_tt of the chunk, granule s_ch (0..3 B, 4..7 C).
+    // B | C staging: thread -> token s_tt of the chunk, granule s_ch (0..3 B, 4..7 C); the first
+    // 16 x 8 threads stage.
     const int s_tt = tid & 15, s_ch = tid >> 4;
+    const bool stager = s_ch < 8;
     const Tin* s_src = (s_ch < 4 ? static_cast<const Tin*>(a.B) : static_cast<const Tin*>(a.C)) +
                        b * kN * L + (int64_t)(4 * (s_ch & 3)) * L;
     float sb[4];
     auto fetch_bc = [&](int c, bool withC) {
         const int64_t t = (int64_t)c * kBChunk + s_tt;
-        const bool ok = t < L && (withC || s_ch < 4);
+        const bool ok = stager && t < L && (withC || s_ch < 4);
 #pragma unroll
         for (int j = 0; j < 4; ++j) sb[j] = ok ? ld1(s_src + j * L + t) : 0.f;
     };
     using Stage = BcStage<Tin>;
     auto put_bc = [&](int buf, bool withC) {
-        if (withC || s_ch < 4) Stage::put(&sm.bc[buf][0][0], s_tt, s_ch, sb);
+        if (stager && (withC || s_ch < 4)) Stage::put(&sm.bc[buf][0][0], s_tt, s_ch, sb);
     };
     // v * exp(Delta A_n) + add (s = Delta * kScale). fp32 inputs write a weak decay as 1 + expm1:
     // the decay's distance from 1 keeps full relative precision, so a slowly decaying state or
@@ -586,15 +591,19 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
             store4<Tg, kVec>(dd_row, tl, Lr, ddv);
         }
         __syncthreads();  // every warp's dB | dC sums of the chunk are in P
-        // CTA sums of dB_t / dC_t over the 4 warps -> this CTA's partials [t][slot].
+        // CTA sums of dB_t / dC_t over the kBWarps warps -> this CTA's partials [t][slot].
 #pragma unroll
-        for (int r = 0; r < kBSlots * kBChunk / kBThreads; ++r) {
+        for (int r = 0; r < (kBSlots * kBChunk + kBThreads - 1) / kBThreads; ++r) {
             const int item = tid + r * kBThreads;
+            if (item >= kBSlots * kBChunk) break;
             const int slot = item & 31, tt = item >> 5;
             const int64_t t = t0 + tt;
-            if (t < L)
-                part[t * kBSlots + slot] = sm.P[0][tt][slot] + sm.P[1][tt][slot] +
-                                           sm.P[2][tt][slot] + sm.P[3][tt][slot];
+            if (t < L) {
+                float acc = sm.P[0][tt][slot];
+#pragma unroll
+                for (int w = 1; w < kBWarps; ++w) acc += sm.P[w][tt][slot];
+                part[t * kBSlots + slot] = acc;
+            }
         }
     }
 
@@ -666,10 +675,16 @@ __global__ void scan_bwd_reduce_kernel(const BwdArgs a, int64_t nblk) {
 
 template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode>
 static void launch_bwd_one(const BwdArgs& a, dim3 grid, cudaStream_t stream) {
-    if ((int64_t)grid.x * grid.y * grid.z <= (int64_t)a.sms * kBMinCtasRoomy)
-        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtasRoomy><<<grid, kBThreads, 0, stream>>>(a);
-    else
-        scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtas><<<grid, kBThreads, 0, stream>>>(a);
+    constexpr int smem = (int)sizeof(BwdSmem);
+    if ((int64_t)grid.x * grid.y * grid.z <= (int64_t)a.sms * kBMinCtasRoomy) {
+        auto k = scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtasRoomy>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        k<<<grid, kBThreads, smem, stream>>>(a);
+    } else {
+        auto k = scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtas>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        k<<<grid, kBThreads, smem, stream>>>(a);
+    }
 }
 
 template <typename Tin, typename Tg, bool kPrecise, bool kVec>

@@ -172,9 +172,10 @@ def test_bwd_mamba2p8b_layer_sampled():
 
 
 def _unsplit_workspace_bytes(b, d, L):
-    """Workspace of the backward without time segments (mirrors its layout, 256-byte parts)."""
+    """Workspace of the backward without time segments (mirrors its layout: CTAs of 48 channels,
+    256-byte parts)."""
     up = lambda x: (x + 63) // 64 * 64
-    rows, chunks, blocks = b * d, (L + 15) // 16, (d + 31) // 32
+    rows, chunks, blocks = b * d, (L + 15) // 16, (d + 47) // 48
     return 4 * (up(rows * chunks * 16) + up(blocks * b * L * 32) + up(rows * 16) + 2 * up(rows))
 
 
