@@ -26,11 +26,16 @@
 // h <- exp(A sum Delta) h + h_local_end, and its adjoint from the fold of the later ones,
 // g <- g_local_start + exp(A sum Delta) g (the adjoint recurrence is linear in g as well).
 //
-// dB and dC are sums over every channel of a batch: each warp reduce-scatters its 8 rows' terms
-// in three shuffle rounds (lane (q, g) ends with one of the 32 dB | dC sums of the token), the
-// CTA adds its 6 warps in shared memory and writes one partial per token and value. dA, dD and
+// dB and dC are sums over every channel of a batch. Each warp sums its 8 rows' terms: built for
+// 3 CTAs per SM, by a per-token reduce-scatter in three shuffle rounds (lane (q, g) ends with
+// one of the 32 dB | dC sums of the token); built for 2, by two contractions per chunk from
+// shared memory (dC_t = sum ds_t h_t over the stored states; dB_t = sum g_t k_t over the
+// adjoints, stored in place of the states). The CTA adds its 6 warps in shared memory and
+// writes one partial per token and value. dA, dD and
 // dbias are kept per (batch, channel). A second kernel adds the partials in a fixed order, so
 // the gradients are deterministic (no atomics).
+#include <cstddef>
+
 #include "selscan_device.cuh"
 #include "selscan_launch.h"
 
@@ -41,6 +46,8 @@ constexpr int kBWarps = 6;
 constexpr int kBThreads = 32 * kBWarps;     // 192: 48 channels
 constexpr int kBRows = 8 * kBWarps;         // channels per CTA
 constexpr int kBSlots = 32;                 // dB[0..15], dC[0..15] per token
+// Row stride of the per-(row, token) coefficient tiles of the contractions (one 16-token chunk).
+constexpr int kBCoefStride = kBChunk;
 // CTAs of 6 warps (48 channels, 64 KB of shared memory): 3 fit an SM. A grid of Mamba-2.8B size
 // (4 x 107 CTAs on 148 SMs) then holds at most 144 channels on any SM, where CTAs of 4 warps at
 // 5 per SM held 160. Built for 3 per SM (96 registers: 18 warps leave 5 on some schedulers) when
@@ -50,8 +57,10 @@ constexpr int kBMinCtasRoomy = 2;
 
 struct BwdSmem {
     float bc[2][kBChunk][32];                // B | C per token (layout: BcStage)
-    float4 H[kBWarps][kBChunk][32];          // recomputed states h_t of the chunk
+    float4 H[kBWarps][kBChunk][32];          // recomputed states h_t, then adjoints g_t
     float P[kBWarps][kBChunk][kBSlots];      // warp sums of dB | dC per token
+    float DS[kBWarps][8][kBCoefStride];      // ds_t per row of the warp and token
+    float K[kBWarps][8][kBCoefStride];       // k_t = Delta_t u_t per row of the warp and token
 };
 
 template <typename Tin>
@@ -191,10 +200,39 @@ struct BcStage<__nv_bfloat16> {
 // (segments 0..S-2) and the adjoint local-start pass (segments 1..S-1).
 enum BwdMode : int { kBwdFull = 0, kBwdFwdLocal = 1, kBwdAdjLocal = 2 };
 
+// One warp's sums over its 8 rows for the 16 tokens of a chunk: P[t][slot0 + n] =
+// sum_r coef[r][t] V[t][r][n] for the 16 states n, with V the warp's [token][lane] float4 tile
+// (lane 4r + j holds states 4j..4j+3 of row r). Lane (tq, j) takes tokens tq and tq + 8 and
+// states 4j..4j+3, and visits the rows in the order (i + tq) & 7, so that each quarter-warp's
+// 16-byte loads fall on 8 different bank groups and its coefficient loads on distinct banks.
+__device__ __forceinline__ void warp_rows_contract(const float4* V, const float* coef, float* P,
+                                                   int slot0, int lane) {
+    const int tq = lane >> 2, j = lane & 3;
+    float2 a01 = f2(0.f), a23 = f2(0.f), b01 = f2(0.f), b23 = f2(0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (i + tq) & 7;
+        const float4 v0 = V[tq * 32 + 4 * r + j], v1 = V[(tq + 8) * 32 + 4 * r + j];
+        const float2 c0 = f2(coef[r * kBCoefStride + tq]), c1 = f2(coef[r * kBCoefStride + tq + 8]);
+        a01 = __ffma2_rn(c0, make_float2(v0.x, v0.y), a01);
+        a23 = __ffma2_rn(c0, make_float2(v0.z, v0.w), a23);
+        b01 = __ffma2_rn(c1, make_float2(v1.x, v1.y), b01);
+        b23 = __ffma2_rn(c1, make_float2(v1.z, v1.w), b23);
+    }
+    *reinterpret_cast<float4*>(P + tq * kBSlots + slot0 + 4 * j) = make_float4(a01.x, a01.y, a23.x, a23.y);
+    *reinterpret_cast<float4*>(P + (tq + 8) * kBSlots + slot0 + 4 * j) =
+        make_float4(b01.x, b01.y, b23.x, b23.y);
+}
+
 template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode, int kMinCtas>
 __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) unsigned char bwd_smem[];
     BwdSmem& sm = *reinterpret_cast<BwdSmem*>(bwd_smem);
+    // The dB | dC sums over a warp's rows: with the registers of 2 CTAs per SM, two contractions
+    // per chunk from shared memory (the states, then the adjoints written over them); at 3 per SM
+    // (96 registers) a per-token shuffle reduce-scatter, which needs fewer live registers.
+    constexpr bool kContract = kMinCtas <= 2;
+    static_assert(kContract == (kMinCtas == kBMinCtasRoomy), "launch sizes shared memory by this");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = lane >> 2, g = lane & 3;
     const int64_t b = blockIdx.z;
@@ -386,9 +424,6 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
     Tg* dd_row = static_cast<Tg*>(a.ddelta) + row * L;
     Tg* dz_row = a.z ? static_cast<Tg*>(a.dz) + row * L : nullptr;
     float* part = a.ws_part + ((int64_t)blockIdx.x * a.batch + b) * L * kBSlots;  // [t][slot]
-    // After the reduce-scatter lane (q, g) holds dB of state 4g+q (q < 4) or dC of 4g+q-4.
-    const int my_slot = (quad >> 2) * 16 + 4 * g + (quad & 3);
-    const bool x16 = (lane >> 4) & 1, x8 = (lane >> 3) & 1, x4 = (lane >> 2) & 1;
 
     Quad4<Tin, kVec> pd, pu, pz;
     Quad4<Tg, kVec> po;
@@ -454,6 +489,10 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
             continue;
         }
 
+        if constexpr (kContract) {  // ds_t and k_t of the quad's row for the contractions
+            *reinterpret_cast<float4*>(&sm.DS[warp][quad][4 * g]) = make_float4(dsl[0], dsl[1], dsl[2], dsl[3]);
+            *reinterpret_cast<float4*>(&sm.K[warp][quad][4 * g]) = make_float4(kl[0], kl[1], kl[2], kl[3]);
+        }
         // Recompute the chunk's states (into shared memory) and the readouts s_t - D u_t.
         float sl[4];
         {
@@ -493,13 +532,19 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
             store4<Tg, kVec>(dz_row, tl, Lr, dzv);
         }
         __syncwarp();
+        if constexpr (kContract) {
+            // dC_t = sum over the warp's 8 rows of ds_t h_t, from the states just stored.
+            warp_rows_contract(Hw, &sm.DS[warp][0][0], &sm.P[warp][0][0], 16, lane);
+            __syncwarp();  // H is read before the adjoints overwrite it
+        }
 
         // Adjoint recurrence, last token of the chunk first. The chunk's dA terms are summed
         // apart and then added to the running sum: two-level summation keeps the rounding of
         // sums over hundreds of thousands of tokens near that of the per-chunk sums.
         float dkl[4], dal[4];  // owner: dk_t and the Abar part of dDelta_t
         float dA_chunk[4] = {0.f, 0.f, 0.f, 0.f};
-        float4 ht = Hw[(kBChunk - 1) * 32 + lane];
+        float4 ht = make_float4(0.f, 0.f, 0.f, 0.f);  // h_t, for the reduce-scattered dC terms
+        if constexpr (!kContract) ht = Hw[(kBChunk - 1) * 32 + lane];
 #pragma unroll
         for (int t = kBChunk - 1; t >= 0; --t) {
             const float s = __shfl_sync(0xffffffffu, dl[t & 3], t >> 2, 4);
@@ -510,13 +555,16 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
             const float4 hp = t > 0 ? Hw[(t - 1) * 32 + lane] : hk4;
             const float Bs[4] = {Bv.x, Bv.y, Bv.z, Bv.w}, Cs[4] = {Cv.x, Cv.y, Cv.z, Cv.w};
             const float hts[4] = {ht.x, ht.y, ht.z, ht.w}, hps[4] = {hp.x, hp.y, hp.z, hp.w};
-            float dk = 0.f, da = 0.f, v[8];
+            float dk = 0.f, da = 0.f, v[8];  // v: dB terms g_t k_t, then dC terms ds_t h_t
             if constexpr (kPrecise) {
 #pragma unroll
+                for (int n = 0; n < 4; ++n) gad[n] = fmaf(ds, Cs[n], gad[n]);
+                if constexpr (kContract)  // g_t replaces h_t, which the token after it last read
+                    Hw[t * 32 + lane] = make_float4(gad[0], gad[1], gad[2], gad[3]);
+#pragma unroll
                 for (int n = 0; n < 4; ++n) {
-                    gad[n] = fmaf(ds, Cs[n], gad[n]);
-                    v[4 + n] = ds * hts[n];   // dC term
-                    v[n] = gad[n] * k;        // dB term
+                    v[4 + n] = ds * hts[n];
+                    v[n] = gad[n] * k;
                     dk = fmaf(gad[n], Bs[n], dk);
                     // the adjoint times Abar (weak decays as 1 + expm1, see decay_fma)
                     const float gab = precise_decay(s, Av[n], gad[n]);
@@ -529,9 +577,15 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
                 const float2 s2 = f2(s), k2 = f2(k), ds2 = f2(ds);
                 float2 g01 = __ffma2_rn(ds2, make_float2(Cs[0], Cs[1]), make_float2(gad[0], gad[1]));
                 float2 g23 = __ffma2_rn(ds2, make_float2(Cs[2], Cs[3]), make_float2(gad[2], gad[3]));
-                const float2 vc01 = __fmul2_rn(ds2, make_float2(hts[0], hts[1]));
-                const float2 vc23 = __fmul2_rn(ds2, make_float2(hts[2], hts[3]));
-                const float2 vb01 = __fmul2_rn(g01, k2), vb23 = __fmul2_rn(g23, k2);
+                if constexpr (kContract) {
+                    Hw[t * 32 + lane] = make_float4(g01.x, g01.y, g23.x, g23.y);
+                } else {
+                    const float2 vc01 = __fmul2_rn(ds2, make_float2(hts[0], hts[1]));
+                    const float2 vc23 = __fmul2_rn(ds2, make_float2(hts[2], hts[3]));
+                    const float2 vb01 = __fmul2_rn(g01, k2), vb23 = __fmul2_rn(g23, k2);
+                    v[0] = vb01.x; v[1] = vb01.y; v[2] = vb23.x; v[3] = vb23.y;
+                    v[4] = vc01.x; v[5] = vc01.y; v[6] = vc23.x; v[7] = vc23.y;
+                }
                 float2 dk2 = __fmul2_rn(g01, make_float2(Bs[0], Bs[1]));
                 dk2 = __ffma2_rn(g23, make_float2(Bs[2], Bs[3]), dk2);
                 const float2 x01 = __fmul2_rn(s2, A01), x23 = __fmul2_rn(s2, A23);
@@ -545,8 +599,6 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
                 const float2 c23 = __ffma2_rn(w23, s2, make_float2(dA_chunk[2], dA_chunk[3]));
                 dA_chunk[0] = c01.x; dA_chunk[1] = c01.y; dA_chunk[2] = c23.x; dA_chunk[3] = c23.y;
                 gad[0] = g01.x; gad[1] = g01.y; gad[2] = g23.x; gad[3] = g23.y;
-                v[0] = vb01.x; v[1] = vb01.y; v[2] = vb23.x; v[3] = vb23.y;
-                v[4] = vc01.x; v[5] = vc01.y; v[6] = vc23.x; v[7] = vc23.y;
                 dk = dk2.x + dk2.y;
                 da = da2.x + da2.y;
             }
@@ -556,32 +608,43 @@ __global__ void __launch_bounds__(kBThreads, kMinCtas) scan_bwd_kernel(const Bwd
             da += __shfl_xor_sync(0xffffffffu, da, 1);
             da += __shfl_xor_sync(0xffffffffu, da, 2);
             if (g == (t >> 2)) { dkl[t & 3] = dk; dal[t & 3] = da; }
-            // Sums of the 8 rows' dB | dC terms, reduce-scattered over lane bits 4, 3, 2.
-            float w4[4], w2[2];
+            if constexpr (!kContract) {
+                // Sums of the 8 rows' dB | dC terms, reduce-scattered over lane bits 4, 3, 2:
+                // lane (q, g) ends with dB of state 4g+q (q < 4) or dC of state 4g+q-4.
+                const bool x16 = (lane >> 4) & 1, x8 = (lane >> 3) & 1, x4 = (lane >> 2) & 1;
+                float w4[4], w2[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float send = x16 ? v[i] : v[i + 4], keep = x16 ? v[i + 4] : v[i];
-                w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-            }
+                for (int i = 0; i < 4; ++i) {
+                    const float send = x16 ? v[i] : v[i + 4], keep = x16 ? v[i + 4] : v[i];
+                    w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float send = x8 ? w4[i] : w4[i + 2], keep = x8 ? w4[i + 2] : w4[i];
-                w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                for (int i = 0; i < 2; ++i) {
+                    const float send = x8 ? w4[i] : w4[i + 2], keep = x8 ? w4[i + 2] : w4[i];
+                    w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                }
+                const float send = x4 ? w2[0] : w2[1], keep = x4 ? w2[1] : w2[0];
+                sm.P[warp][t][(quad >> 2) * 16 + 4 * g + (quad & 3)] =
+                    keep + __shfl_xor_sync(0xffffffffu, send, 4);
             }
-            const float send = x4 ? w2[0] : w2[1], keep = x4 ? w2[1] : w2[0];
-            sm.P[warp][t][my_slot] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        if constexpr (kContract) {
+            __syncwarp();
+            // dB_t = sum over the warp's 8 rows of g_t k_t, from the adjoints just stored.
+            warp_rows_contract(Hw, &sm.K[warp][0][0], &sm.P[warp][0][0], 0, lane);
         }
 #pragma unroll
         for (int n = 0; n < 4; ++n) dA_acc[n] += dA_chunk[n];
         // Owner: per-token gradients of its tokens.
         {
             float duv[4], ddv[4], dD_c = 0.f, db_c = 0.f;
+            const float* dso = dsl;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                duv[i] = fmaf(dkl[i], dl[i] * (1.f / kScale), dsl[i] * Dd);
+                duv[i] = fmaf(dkl[i], dl[i] * (1.f / kScale), dso[i] * Dd);
                 ddv[i] = fmaf(dkl[i], ul[i], dal[i]) * sgx[i];
                 if (tl + i < Lr) {
-                    dD_c = fmaf(dsl[i], ul[i], dD_c);
+                    dD_c = fmaf(dso[i], ul[i], dD_c);
                     db_c += ddv[i];
                 }
             }
@@ -675,15 +738,19 @@ __global__ void scan_bwd_reduce_kernel(const BwdArgs a, int64_t nblk) {
 
 template <typename Tin, typename Tg, bool kPrecise, bool kVec, int kMode>
 static void launch_bwd_one(const BwdArgs& a, dim3 grid, cudaStream_t stream) {
-    constexpr int smem = (int)sizeof(BwdSmem);
+    // The contraction tiles (DS, K: the last members) only for the instantiation that uses them:
+    // 3 CTAs per SM without them take 192 KB of shared memory and leave more of the SM's
+    // 256 KB to the L1 cache.
+    constexpr int smem_contract = (int)sizeof(BwdSmem);
+    constexpr int smem_shuffle = (int)offsetof(BwdSmem, DS);
     if ((int64_t)grid.x * grid.y * grid.z <= (int64_t)a.sms * kBMinCtasRoomy) {
         auto k = scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtasRoomy>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        k<<<grid, kBThreads, smem, stream>>>(a);
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_contract);
+        k<<<grid, kBThreads, smem_contract, stream>>>(a);
     } else {
         auto k = scan_bwd_kernel<Tin, Tg, kPrecise, kVec, kMode, kBMinCtas>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        k<<<grid, kBThreads, smem, stream>>>(a);
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_shuffle);
+        k<<<grid, kBThreads, smem_shuffle, stream>>>(a);
     }
 }
 
