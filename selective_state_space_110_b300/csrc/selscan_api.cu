@@ -465,8 +465,16 @@ SELSCAN_EXPORT selscan_status ssm_conv_state_update(
 }
 
 namespace {
-// Time segments of the backward, on the forward's rule: split only when the rows alone fill less
-// than half of the CTA slots; as many segments as fill one wave, each at least kMinSegTokens.
+// Time segments of the backward: split only when the rows alone fill less than half of the CTA
+// slots (as the forward does). Of the segment counts that fit one wave (segments of at least
+// kMinSegTokens), take the one with the least estimated time: with n segments the grid holds
+// ctas * n CTAs, the most loaded SM p = ceil(ctas * n / sms) of them, each seqlen / n tokens
+// long, and an SM's throughput depends on p. Measured on B300 (CTAs of 48 channels, 2,048
+// tokens, one wave): 1, 2 and 3 CTAs per SM process 22.6, 33.9 and 31.2 G elements/s per
+// SM-load, so the time is taken as p * kBwdSmCost[p] / n; ties go to fewer segments. 32 blocks on
+// 148 SMs: 9 segments (2 CTAs per SM) rather than the 13 that fill the slots (3 per SM),
+// 73.3 -> 69.1 ms for a million tokens.
+constexpr int64_t kBwdSmCost[4] = {0, 150, 100, 109};  // 1 / relative throughput, x 100
 struct BwdPlan {
     int nseg;
     int64_t seg_len;
@@ -475,13 +483,24 @@ BwdPlan make_bwd_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
     const int64_t chunk = selscan::scan_bwd_chunk_tokens();
     const int64_t rows_per_cta = selscan::scan_bwd_rows_per_cta();
     const int64_t ctas = batch * ((dim + rows_per_cta - 1) / rows_per_cta);
-    const int64_t slots = (int64_t)sms * selscan::scan_bwd_ctas_per_sm();
+    const int ctas_per_sm = selscan::scan_bwd_ctas_per_sm();
+    const int64_t slots = (int64_t)sms * ctas_per_sm;
     int64_t n = 1;
     if (2 * ctas <= slots) {
-        n = slots / ctas;
-        n = std::min<int64_t>(n, seqlen / kMinSegTokens);
-        n = std::max<int64_t>(n, 1);
-        n = std::min<int64_t>(n, 65535);
+        int64_t nmax = slots / ctas;
+        nmax = std::min<int64_t>(nmax, seqlen / kMinSegTokens);
+        nmax = std::max<int64_t>(nmax, 1);
+        nmax = std::min<int64_t>(nmax, 65535);
+        // minimise cost(k) / k, compared as cost(k) * n < cost(n) * k
+        int64_t best_cost = -1;
+        for (int64_t k = 1; k <= nmax; ++k) {
+            const int64_t per_sm = std::min<int64_t>((ctas * k + sms - 1) / sms, ctas_per_sm);
+            const int64_t cost = per_sm * kBwdSmCost[std::min<int64_t>(per_sm, 3)];
+            if (best_cost < 0 || cost * n < best_cost * k) {
+                n = k;
+                best_cost = cost;
+            }
+        }
     }
     int64_t seg_len = (std::max<int64_t>(seqlen, 1) + n - 1) / n;
     seg_len = (seg_len + chunk - 1) / chunk * chunk;
