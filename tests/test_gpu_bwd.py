@@ -111,8 +111,12 @@ def test_bwd_empty_sequence():
         assert torch.count_nonzero(got[k]) == 0, k
 
 
-def test_bwd_is_deterministic():
-    x = _problem(2, 96, 600, "bf16", 77)
+@pytest.mark.parametrize("shape", [(2, 96, 600), (4, 5120, 64)], ids=["2x96x600", "4x5120x64"])
+def test_bwd_is_deterministic(shape):
+    """Bit-identical gradients on a repeat call: in the CTA instantiation built for 2 per SM
+    (per-chunk contractions for dB | dC) and in the one built for 3 (the 428 CTAs of a
+    5120-channel, 4-batch grid; per-token shuffle reduce-scatter)."""
+    x = _problem(*shape, "bf16", 77)
     a = _gpu(x)
     b = _gpu(x)
     torch.cuda.synchronize()
