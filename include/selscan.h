@@ -96,9 +96,9 @@ typedef enum {
  * in_dtype applies to u, delta, z, B and C; out_dtype to out. Arithmetic is fp32.
  *
  * workspace / workspace_bytes: scratch device memory of ssm_scan_workspace_size(batch, dim,
- * dstate, seqlen) bytes (NULL/0 when that is 0). Some blocks of 32 channels are cut into time
- * segments that run in parallel; the workspace holds each segment's local end state and its
- * summed Delta. Two cases (ssm_scan_plan reports which one a shape takes):
+ * dstate, seqlen) bytes (NULL/0 when that is 0). Some channel blocks (32 channels, or 128 in
+ * the wide CTA of the balanced case below) are cut into time segments that run in parallel;
+ * the workspace holds each segment's local end state and its summed Delta. Two cases (ssm_scan_plan reports which one a shape takes):
  *   - long sequences with few (batch, channel) rows are split for parallelism; the workspace
  *     is then required (SELSCAN_ERR_WORKSPACE without it);
  *   - shapes with more channel blocks than the GPU runs at once (bf16 inputs, seqlen % 8 == 0,
@@ -303,7 +303,8 @@ size_t ssm_scan_fwd_host_workspace_size(int64_t batch, int64_t dim, int64_t dsta
  *
  * workspace: at least ssm_scan_bwd_workspace_size(..., checkpoints != NULL) bytes on the CURRENT
  * device (always > 0: without checkpoints the state every 16 tokens, 4 bytes per (b, d, token);
- * per-block partial sums of dB and dC, 4*batch*32*seqlen bytes per 32 channels; per-row sums;
+ * per-block partial sums of dB and dC, 4*batch*32*seqlen bytes per block of 48 channels;
+ * per-row sums;
  * and, for long sequences with few rows, which are split into time segments as in the forward,
  * each segment's local end state and start adjoint). Its contents on entry do not matter.
  */
