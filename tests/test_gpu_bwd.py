@@ -188,6 +188,7 @@ SEG_SHAPES = [
     (1, 32, 40000, "bf16", torch.float32),
     (1, 40, 20001, "f32", torch.float32),    # ragged length (scalar loads), fp32
     (2, 16, 16384, "bf16", torch.bfloat16),
+    (2, 768, 8192, "bf16", torch.float32),   # 16 blocks per batch, each cut in two segments
 ]
 
 
