@@ -702,7 +702,9 @@ def run_reference(args):
     import oracle
     cfg = scan_config(args.workload)
     x = make_scan_inputs(cfg.replace(batch=1), "cpu")
-    rows_per_step = 96  # a bounded sample: 96 rows x all tokens per step
+    # a bounded sample: up to 2,048 rows x all tokens per step (enough work that the oracle's
+    # thread start-up does not set its rate)
+    rows_per_step = min(2048, cfg.dim)
     rows = torch.arange(rows_per_step)
     flat = lambda t: t.view(cfg.dim, -1)[rows]
     args_ = [rows.numpy(), flat(x["u"]), flat(x["delta"]), x["A"], x["B"], x["C"], x["D"],
