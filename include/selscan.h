@@ -325,6 +325,22 @@ size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t dstate, i
                                    int checkpoints_given);
 
 /*
+ * ssm_scan_bwd_plan: the launch plan of ssm_scan_bwd for a shape on a GPU of `sms` SMs (0 = the
+ * current device; a positive count touches no device). Rows are taken in CTAs of 48 channels;
+ * when they fill less than half of the CTA slots, the sequence is cut into time segments
+ * (each at least 4,096 tokens), as many as give the least work on the most loaded SM, weighted
+ * by the measured throughput of an SM holding 1, 2 or 3 of these CTAs. info[0..5] (int64, host
+ * memory): [0] time segments, [1] tokens per segment (a multiple of 16), [2] channels per CTA,
+ * [3] CTAs of the full pass (channel blocks x batch x segments), [4] CTAs per SM its
+ * instantiation is built for (2: 168 registers, dB / dC by per-chunk contractions; 3: 96
+ * registers, by per-token shuffles), [5] workspace bytes (as ssm_scan_bwd_workspace_size with
+ * checkpoints_given). SELSCAN_ERR_INVALID_ARG for a NULL info, bad sizes, dstate != 16 or sms
+ * outside 0..4096.
+ */
+selscan_status ssm_scan_bwd_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                                 int checkpoints_given, int sms, int64_t* info);
+
+/*
  * ssd_chunk_scan_fwd: the Mamba-2 layer core, state space duality (SSD). "Mamba and State Space
  * Models" (world.lapla.si), section "Mamba-2": A is one number per head times the identity, so
  * the layer is one lower-triangular matrix per head (entry i, j = C_i . B_j times the decay

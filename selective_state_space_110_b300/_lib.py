@@ -31,7 +31,7 @@ EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_state_update", "selsc
            "ssm_scan_fwd_no_alloc", "selscan_device_status", "selscan_selftest_wait_timeout",
            "ssm_conv_state_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
            "ssd_chunk_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_chunk_scan_plan", "ssm_scan_fwd_host", "ssm_scan_fwd_host_workspace_size",
-           "ssm_scan_fwd_ckpt", "ssm_scan_plan")
+           "ssm_scan_fwd_ckpt", "ssm_scan_plan", "ssm_scan_bwd_plan")
 
 # Size of the fixed scratch array behind ssm_scan_fwd_no_alloc (SELSCAN_NO_ALLOC_SCRATCH_BYTES).
 NO_ALLOC_SCRATCH_BYTES = 524288
@@ -62,6 +62,8 @@ def load() -> ctypes.CDLL:
                                    ctypes.c_int, ctypes.POINTER(_I64)]
     lib.ssd_chunk_scan_plan.restype = ctypes.c_int
     lib.ssd_chunk_scan_plan.argtypes = [_I64] * 3 + [ctypes.c_int, ctypes.POINTER(_I64)]
+    lib.ssm_scan_bwd_plan.restype = ctypes.c_int
+    lib.ssm_scan_bwd_plan.argtypes = [_I64] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(_I64)]
     lib.ssm_state_update.restype = ctypes.c_int
     lib.ssm_state_update.argtypes = ([_VP] * 9 + [_VP, ctypes.c_int] + [_I64] * 3 +
                                      [ctypes.c_int, ctypes.c_int, _VP])

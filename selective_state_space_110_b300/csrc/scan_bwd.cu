@@ -810,5 +810,6 @@ BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int 
 int scan_bwd_chunk_tokens() { return kBChunk; }
 int scan_bwd_rows_per_cta() { return kBRows; }
 int scan_bwd_ctas_per_sm() { return kBMinCtas; }
+int scan_bwd_ctas_per_sm_roomy() { return kBMinCtasRoomy; }
 
 }  // namespace selscan

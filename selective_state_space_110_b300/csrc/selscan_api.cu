@@ -522,6 +522,28 @@ SELSCAN_EXPORT size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, in
     return bwd_workspace_bytes(batch, dim, seqlen, sms, checkpoints_given != 0);
 }
 
+SELSCAN_EXPORT selscan_status ssm_scan_bwd_plan(int64_t batch, int64_t dim, int64_t dstate,
+                                                int64_t seqlen, int checkpoints_given, int sms,
+                                                int64_t* info) {
+    if (!info || !shape_ok(batch, dim, seqlen) || dstate != kStateN || sms < 0 || sms > 4096)
+        return SELSCAN_ERR_INVALID_ARG;
+    if (sms == 0) {
+        const selscan_status s = device_sms(&sms);
+        if (s != SELSCAN_OK) return s;
+    }
+    const BwdPlan p = make_bwd_plan(batch, dim, seqlen, sms);
+    const int64_t rows_per_cta = selscan::scan_bwd_rows_per_cta();
+    const int64_t ctas = batch * ((dim + rows_per_cta - 1) / rows_per_cta) * p.nseg;
+    info[0] = p.nseg;
+    info[1] = p.seg_len;
+    info[2] = rows_per_cta;
+    info[3] = ctas;
+    const int roomy = selscan::scan_bwd_ctas_per_sm_roomy();
+    info[4] = ctas <= (int64_t)sms * roomy ? roomy : selscan::scan_bwd_ctas_per_sm();
+    info[5] = (int64_t)bwd_workspace_bytes(batch, dim, seqlen, sms, checkpoints_given != 0);
+    return SELSCAN_OK;
+}
+
 SELSCAN_EXPORT selscan_status ssm_scan_bwd(
     const void* u, const void* delta, const float* A, const void* B, const void* C,
     const float* D, const void* z, const float* delta_bias, int delta_softplus,

@@ -142,6 +142,7 @@ BwdWorkspace scan_bwd_workspace(int64_t batch, int64_t dim, int64_t seqlen, int 
 int scan_bwd_chunk_tokens();   // time segments are multiples of this
 int scan_bwd_rows_per_cta();
 int scan_bwd_ctas_per_sm();
+int scan_bwd_ctas_per_sm_roomy();  // the instantiation a grid of at most sms x this many CTAs takes
 // Launches the backward kernel and the reduction of its partial sums on `stream`.
 cudaError_t launch_scan_bwd(const BwdArgs& a, bool in_bf16, bool grad_bf16, cudaStream_t stream);
 

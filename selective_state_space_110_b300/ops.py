@@ -74,6 +74,18 @@ def ssd_plan(batch: int, seqlen: int, nheads: int, sms: int = 0) -> dict:
     return dict(zip(keys, (int(v) for v in info)))
 
 
+def bwd_plan(batch: int, dim: int, dstate: int, seqlen: int, checkpoints: bool = False,
+             sms: int = 0) -> dict:
+    """How ssm_scan_bwd launches this shape (ssm_scan_bwd_plan) on the current device, or with
+    sms > 0 on a GPU of that many SMs (no device needed)."""
+    info = (ctypes.c_int64 * 6)()
+    st = _lib.lib().ssm_scan_bwd_plan(batch, dim, dstate, seqlen, int(checkpoints), sms, info)
+    _lib.check("ssm_scan_bwd_plan", st)
+    keys = ("segments", "segment_tokens", "channels_per_cta", "ctas", "ctas_per_sm",
+            "workspace_bytes")
+    return dict(zip(keys, (int(v) for v in info)))
+
+
 def _flags(softplus, zoh):
     return (_lib.FLAG_SOFTPLUS if softplus else 0) | (_lib.FLAG_ZOH if zoh else 0)
 

@@ -251,3 +251,17 @@ def test_forward_with_checkpoints_gives_the_same_outputs(shape):
     y1, f1, _ = ssm_scan_fwd_ckpt(*args, initial_state=x["initial_state"], out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(y0, y1) and torch.equal(f0, f1)
+
+
+@pytest.mark.parametrize("shape", [(4, 5120, 2048), (1, 1536, 1 << 20), (1, 32, 40000)],
+                         ids=lambda s: f"{s[0]}x{s[1]}x{s[2]}")
+def test_bwd_plan_on_the_device_matches_the_workspace(shape):
+    """ssm_scan_bwd_plan for the current device reports the workspace ssm_scan_bwd_workspace_size
+    gives, and the plan for the device's own SM count."""
+    from selective_state_space_110_b300 import bwd_plan, bwd_workspace_size
+    b, d, L = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for ck in (False, True):
+        p = bwd_plan(b, d, 16, L, checkpoints=ck)
+        assert p == bwd_plan(b, d, 16, L, checkpoints=ck, sms=sms)
+        assert p["workspace_bytes"] == bwd_workspace_size(b, d, 16, L, ck)

@@ -1,10 +1,12 @@
-"""Launch plans of the scan and of the SSD layer, on the CPU: ssm_scan_plan and
-ssd_chunk_scan_plan with an explicit SM count touch no device. The expected plans follow from
-the planning rules (one CTA per SM for the wide scan CTA and for the SSD layer's chains; time
-segments only where the last wave or the row count leaves SMs idle), for a GPU of 148 SMs."""
+"""Launch plans of the scan, its backward and the SSD layer, on the CPU: ssm_scan_plan,
+ssm_scan_bwd_plan and ssd_chunk_scan_plan with an explicit SM count touch no device. The
+expected plans follow from the planning rules (one CTA per SM for the wide scan CTA and for the
+SSD layer's chains; time segments only where the last wave or the row count leaves SMs idle;
+for the backward, the segment count with the least weighted work on the most loaded SM), for a
+GPU of 148 SMs."""
 import torch
 
-from selective_state_space_110_b300 import scan_plan, ssd_plan
+from selective_state_space_110_b300 import bwd_plan, scan_plan, ssd_plan
 
 SMS = 148
 STATE_BYTES = 64 * 128 * 4  # one (head, 64 x 128 fp32) SSD state
@@ -72,3 +74,48 @@ def test_ssd_plan_leaves_whole_waves_and_short_sequences_alone():
                  (4, 300, 80)]:   # 3 chunks: too short to cut
         p = ssd_plan(*args, sms=SMS)
         assert p["cut_chains"] == 0 and p["segments"] == 1 and p["workspace_bytes"] == 0, args
+
+
+def test_bwd_plan_layers_run_unsplit():
+    # 4 x 5120 channels: 4 x 107 CTAs of 48 channels fill the 3-per-SM slots, one wave
+    p = bwd_plan(4, 5120, 16, 2048, sms=SMS)
+    assert {k: p[k] for k in ("segments", "segment_tokens", "channels_per_cta", "ctas", "ctas_per_sm")} == \
+        dict(segments=1, segment_tokens=2048, channels_per_cta=48, ctas=428, ctas_per_sm=3)
+    # 8 x 1536: 256 CTAs, more than half the slots (no split), few enough for the 2-per-SM build
+    p = bwd_plan(8, 1536, 16, 2048, sms=SMS)
+    assert (p["segments"], p["ctas"], p["ctas_per_sm"]) == (1, 256, 2)
+
+
+def test_bwd_plan_long_sequence_weighs_the_most_loaded_sm():
+    # 1536 channels x 1M tokens: 32 blocks. 13 segments would fill the 444 slots (3 CTAs on an
+    # SM, 3/13 of the sequence each), 9 put 2 CTAs on an SM (2/9, at the faster 2-per-SM rate):
+    # the plan takes 9, segments of ceil(2^20 / 9) tokens rounded up to the 16-token chunk.
+    p = bwd_plan(1, 1536, 16, 1 << 20, sms=SMS)
+    assert {k: p[k] for k in ("segments", "segment_tokens", "ctas", "ctas_per_sm")} == \
+        dict(segments=9, segment_tokens=116512, ctas=288, ctas_per_sm=2)
+    assert 9 * 116512 >= 1 << 20 > 8 * 116512 and 116512 % 16 == 0
+    # 48 blocks: 3 segments (1 per SM) and 9 (3 per SM) leave the same work on the most loaded
+    # SM, 6 (2 per SM) less at the faster rate
+    p = bwd_plan(1, 2304, 16, 1 << 20, sms=SMS)
+    assert (p["segments"], p["segment_tokens"], p["ctas"], p["ctas_per_sm"]) == (6, 174768, 288, 2)
+
+
+def test_bwd_plan_segments_are_at_least_4096_tokens():
+    p = bwd_plan(1, 32, 16, 40000, sms=SMS)  # one block: at most 40000 // 4096 = 9 segments
+    assert (p["segments"], p["segment_tokens"], p["ctas"]) == (9, 4448, 9)
+    p = bwd_plan(1, 32, 16, 2048, sms=SMS)   # too short to cut
+    assert (p["segments"], p["segment_tokens"]) == (1, 2048)
+
+
+def test_bwd_plan_workspace_and_rejections():
+    from selective_state_space_110_b300 import SelscanError
+    import pytest
+    full = bwd_plan(1, 1536, 16, 1 << 20, sms=SMS)["workspace_bytes"]
+    given = bwd_plan(1, 1536, 16, 1 << 20, checkpoints=True, sms=SMS)["workspace_bytes"]
+    # the state every 16 tokens (4 bytes per (row, token)) is the difference
+    assert full - given >= 1536 * (1 << 20) * 4 and given > 0
+    for kw in (dict(sms=5000), dict(sms=-1)):
+        with pytest.raises(SelscanError, match="INVALID_ARG"):
+            bwd_plan(1, 32, 16, 2048, **kw)
+    with pytest.raises(SelscanError, match="INVALID_ARG"):
+        bwd_plan(1, 32, 8, 2048, sms=SMS)
