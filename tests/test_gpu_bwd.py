@@ -67,6 +67,10 @@ SHAPES = [
     (1, 33, 77, "f32", torch.bfloat16),
     (1, 1, 1, "bf16", torch.float32),
     (2, 128, 2048, "bf16", torch.float32),  # several channel blocks and 128 chunks
+    (1, 49, 300, "bf16", torch.float32),    # one full 48-channel CTA and one row beyond it
+    # more than 2 CTAs per SM of 148: the build for 3 per SM (per-token shuffle sums of dB | dC)
+    (4, 3600, 64, "bf16", torch.float32),   # 4 x 75 CTAs
+    (3, 4801, 40, "f32", torch.float32),    # 3 x 101 CTAs, the last of each batch one row
 ]
 
 
@@ -265,3 +269,15 @@ def test_bwd_plan_on_the_device_matches_the_workspace(shape):
         p = bwd_plan(b, d, 16, L, checkpoints=ck)
         assert p == bwd_plan(b, d, 16, L, checkpoints=ck, sms=sms)
         assert p["workspace_bytes"] == bwd_workspace_size(b, d, 16, L, ck)
+
+
+def test_bwd_parity_shapes_reach_both_builds():
+    """The parity shapes above run both CTA builds on this GPU: the 3-per-SM one (shuffle sums)
+    for grids of more than 2 CTAs per SM, the 2-per-SM one (contractions) otherwise."""
+    from selective_state_space_110_b300 import bwd_plan
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for b, d, L in [(4, 3600, 64), (3, 4801, 40)]:
+        p = bwd_plan(b, d, 16, L)
+        assert p["ctas"] > 2 * sms and p["ctas_per_sm"] == 3, (b, d, L, p)
+    for b, d, L in [(1, 49, 300), (2, 128, 2048)]:
+        assert bwd_plan(b, d, 16, L)["ctas_per_sm"] == 2
